@@ -1,0 +1,219 @@
+"""CPU oracle for the Q8_0 decode hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does, and this
+package never imports the product: the two share no code.
+
+Thin numpy/ctypes wrappers around ``libmemra_oracle.so`` (``memra_oracle.cpp``).
+Array conventions follow the library's planes: ``wq`` int8 [N, K], ``wd`` uint16
+fp16 bits [N, K/32], ``xq`` int8 [M, K], ``xd`` float32 [M, K/32], ``y`` float32
+[M, N].
+"""
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+_i64 = ctypes.c_int64
+_ptr = ctypes.c_void_p
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_f16.restype = ctypes.c_uint16
+        L.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+        L.oracle_f16_to_f32.restype = ctypes.c_float
+        L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        L.oracle_bf16_to_f32.restype = ctypes.c_float
+        L.oracle_exp_cw.argtypes = [ctypes.c_float]
+        L.oracle_exp_cw.restype = ctypes.c_float
+        L.oracle_quantize_q8_0.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
+        L.oracle_quantize_q8_1_f32.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
+        L.oracle_quantize_q8_1_bf16.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
+        L.oracle_block_dots.argtypes = [_ptr, _i64, _i64, _ptr, _i64, _ptr]
+        L.oracle_q8_0_gemm.argtypes = [_ptr, _ptr, _i64, _i64, _i64, _ptr, _ptr, _ptr,
+                                       ctypes.c_int]
+        L.oracle_dequant_gemm_f64.argtypes = [_ptr, _ptr, _i64, _i64, _i64, _ptr, _ptr, _ptr]
+        L.oracle_swiglu_f32.argtypes = [_ptr, _i64, _i64, _ptr]
+        L.oracle_swiglu_quantize_q8_1.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
+        L.oracle_q8_0_moe_gemv.argtypes = [_ptr, _ptr, _i64, _i64, _i64, _ptr, _ptr, _i64,
+                                           _ptr, _ptr, ctypes.c_int, _ptr]
+        L.oracle_q8_0_moe_gemv.restype = ctypes.c_int
+        L.oracle_moe_ffn.argtypes = [_ptr, _i64, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64,
+                                     _ptr, _ptr, _i64, _ptr]
+        L.oracle_moe_ffn.restype = ctypes.c_int
+        L.oracle_openmp_max_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def f32_to_f16_bits(values):
+    """fp32 -> IEEE binary16 bits, round to nearest even (element by element)."""
+    v = np.asarray(values, dtype=np.float32).ravel()
+    L = lib()
+    out = np.array([L.oracle_f32_to_f16(float(x)) for x in v], dtype=np.uint16)
+    return out.reshape(np.shape(values))
+
+
+def f16_bits_to_f32(bits):
+    b = np.asarray(bits, dtype=np.uint16).ravel()
+    L = lib()
+    out = np.array([L.oracle_f16_to_f32(int(x)) for x in b], dtype=np.float32)
+    return out.reshape(np.shape(bits))
+
+
+def bf16_bits_to_f32(bits):
+    b = np.asarray(bits, dtype=np.uint16).ravel()
+    L = lib()
+    out = np.array([L.oracle_bf16_to_f32(int(x)) for x in b], dtype=np.float32)
+    return out.reshape(np.shape(bits))
+
+
+def exp_cw(values):
+    v = np.asarray(values, dtype=np.float32).ravel()
+    L = lib()
+    out = np.array([L.oracle_exp_cw(float(x)) for x in v], dtype=np.float32)
+    return out.reshape(np.shape(values))
+
+
+def quantize_q8_0(w):
+    """Weights fp32 [N, K] -> (wq int8 [N, K], wd fp16 bits uint16 [N, K/32])."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert K % 32 == 0
+    q = np.empty((N, K), np.int8)
+    d = np.empty((N, K // 32), np.uint16)
+    lib().oracle_quantize_q8_0(_p(w), N, K, _p(q), _p(d))
+    return q, d
+
+
+def quantize_q8_1(x):
+    """Activations [M, K] (float32, or uint16 holding bf16 bits) -> (xq int8, xd float32)."""
+    x = np.asarray(x)
+    M, K = x.shape
+    assert K % 32 == 0
+    q = np.empty((M, K), np.int8)
+    d = np.empty((M, K // 32), np.float32)
+    if x.dtype == np.uint16:
+        x = _c(x, np.uint16)
+        lib().oracle_quantize_q8_1_bf16(_p(x), M, K, _p(q), _p(d))
+    else:
+        x = _c(x, np.float32)
+        lib().oracle_quantize_q8_1_f32(_p(x), M, K, _p(q), _p(d))
+    return q, d
+
+
+def block_dots(wq, xq):
+    """int32 s[M, N, K/32]."""
+    wq = _c(wq, np.int8)
+    xq = _c(xq, np.int8)
+    N, K = wq.shape
+    M = xq.shape[0]
+    s = np.empty((M, N, K // 32), np.int32)
+    lib().oracle_block_dots(_p(wq), N, K, _p(xq), M, _p(s))
+    return s
+
+
+def gemm(wq, wd, xq, xd, threads=1):
+    """y[M, N] float32 = Q8_0 W times q8_1 x, per row sequential fp32 accumulation."""
+    wq = _c(wq, np.int8)
+    wd = _c(wd, np.uint16)
+    xq = _c(xq, np.int8)
+    xd = _c(xd, np.float32)
+    N, K = wq.shape
+    M = xq.shape[0]
+    y = np.empty((M, N), np.float32)
+    lib().oracle_q8_0_gemm(_p(wq), _p(wd), N, K, M, _p(xq), _p(xd), _p(y), int(threads))
+    return y
+
+
+def dequant_gemm_f64(wq, wd, xq, xd):
+    wq = _c(wq, np.int8)
+    wd = _c(wd, np.uint16)
+    xq = _c(xq, np.int8)
+    xd = _c(xd, np.float32)
+    N, K = wq.shape
+    M = xq.shape[0]
+    y = np.empty((M, N), np.float64)
+    lib().oracle_dequant_gemm_f64(_p(wq), _p(wd), N, K, M, _p(xq), _p(xd), _p(y))
+    return y
+
+
+def swiglu(gu):
+    gu = _c(gu, np.float32)
+    R, F2 = gu.shape
+    F = F2 // 2
+    h = np.empty((R, F), np.float32)
+    lib().oracle_swiglu_f32(_p(gu), R, F, _p(h))
+    return h
+
+
+def swiglu_quantize_q8_1(gu):
+    gu = _c(gu, np.float32)
+    R, F2 = gu.shape
+    F = F2 // 2
+    assert F % 32 == 0
+    hq = np.empty((R, F), np.int8)
+    hd = np.empty((R, F // 32), np.float32)
+    lib().oracle_swiglu_quantize_q8_1(_p(gu), R, F, _p(hq), _p(hd))
+    return hq, hd
+
+
+def moe_gemv(wq_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert):
+    """Returns (y, n_bad_ids). y is [top_k, N] without gate weights, [N] with."""
+    wq_bank = _c(wq_bank, np.int8)
+    wd_bank = _c(wd_bank, np.uint16)
+    E, N, K = wq_bank.shape
+    ids = _c(ids, np.int32)
+    top_k = ids.shape[0]
+    xq = _c(xq, np.int8)
+    xd = _c(xd, np.float32)
+    if gate_w is None:
+        y = np.empty((top_k, N), np.float32)
+        gp = None
+    else:
+        gate_w = _c(gate_w, np.float32)
+        y = np.empty((N,), np.float32)
+        gp = _p(gate_w)
+    bad = lib().oracle_q8_0_moe_gemv(_p(wq_bank), _p(wd_bank), E, N, K, _p(ids), gp, top_k,
+                                     _p(xq), _p(xd), int(x_per_expert), _p(y))
+    return y, bad
+
+
+def moe_ffn(x, gu_q, gu_d, dn_q, dn_d, ids, gate_w):
+    """One routed MoE FFN layer for one token. x fp32 [K]; returns (y [N_out], n_bad)."""
+    x = _c(x, np.float32)
+    gu_q = _c(gu_q, np.int8)
+    gu_d = _c(gu_d, np.uint16)
+    dn_q = _c(dn_q, np.int8)
+    dn_d = _c(dn_d, np.uint16)
+    E, F2, K = gu_q.shape
+    F = F2 // 2
+    N_out = dn_q.shape[1]
+    assert dn_q.shape == (E, N_out, F)
+    ids = _c(ids, np.int32)
+    gate_w = _c(gate_w, np.float32)
+    y = np.empty((N_out,), np.float32)
+    bad = lib().oracle_moe_ffn(_p(x), K, _p(gu_q), _p(gu_d), _p(dn_q), _p(dn_d), E, F, N_out,
+                               _p(ids), _p(gate_w), ids.shape[0], _p(y))
+    return y, bad
+
+
+def max_threads():
+    return int(lib().oracle_openmp_max_threads())

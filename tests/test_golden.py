@@ -1,0 +1,44 @@
+"""The oracle against the stored fixtures under tests/golden/ (see make_golden.py)."""
+import json
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def from_hex(h, shape):
+    return np.array([int(v, 16) for v in h], np.uint32).view(np.float32).reshape(shape)
+
+
+def test_hand_block(orc):
+    g = load("q8_0_hand_block.json")
+    w = np.array(g["w"], np.float32)[None]
+    x = np.array(g["x"], np.float32)[None]
+    wq, wd = orc.quantize_q8_0(w)
+    xq, xd = orc.quantize_q8_1(x)
+    assert wq.ravel().tolist() == g["wq"] and int(wd[0, 0]) == g["wd_f16_bits"]
+    assert xq.ravel().tolist() == g["xq"] and float(xd[0, 0]) == g["xd"]
+    assert int(orc.block_dots(wq, xq)[0, 0, 0]) == g["block_sum"]
+    assert float(orc.gemm(wq, wd, xq, xd)[0, 0]) == g["y"]
+
+
+def test_small_gemm_fixture(orc):
+    g = load("q8_0_gemm_small.json")
+    N, K, M = g["N"], g["K"], g["M"]
+    w = from_hex(g["w_f32_hex"], (N, K))
+    x = from_hex(g["x_f32_hex"], (M, K))
+    wq, wd = orc.quantize_q8_0(w)
+    xq, xd = orc.quantize_q8_1(x)
+    assert wq.ravel().tolist() == g["wq"]
+    assert wd.ravel().tolist() == g["wd_f16_bits"]
+    assert xq.ravel().tolist() == g["xq"]
+    assert np.array_equal(xd, from_hex(g["xd_f32_hex"], xd.shape))
+    assert orc.block_dots(wq, xq).ravel().tolist() == g["block_sums"]
+    y = orc.gemm(wq, wd, xq, xd)
+    assert np.array_equal(y.view(np.uint32), from_hex(g["y_f32_hex"], (M, N)).view(np.uint32))

@@ -1,0 +1,470 @@
+"""Pins for the CPU oracle: closed forms, invariants, brute force and library routines.
+
+None of these checks recomputes the oracle's own formula: each compares it with
+something fixed independently (numpy's IEEE binary16 conversion, int64 / fp64
+brute force, libm's exp, exact special cases), chosen so that a dropped term, a
+wrong sign, a wrong block index or a transposed operand fails at least one test.
+"""
+
+import numpy as np
+import pytest
+
+U32 = 2.0 ** -24  # fp32 unit roundoff
+
+
+def rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ----------------------------------------------------------------------------
+# Scalar conversions against numpy (IEEE 754 binary16, round to nearest even).
+# ----------------------------------------------------------------------------
+
+def test_f16_to_f32_exhaustive(orc):
+    codes = np.arange(65536, dtype=np.uint16)
+    ours = orc.f16_bits_to_f32(codes)
+    ref = codes.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_f32_to_f16_ties_and_random(orc):
+    finite = np.arange(0x7C00, dtype=np.uint16)          # +0 .. max finite
+    hv = finite.view(np.float16).astype(np.float64)
+    mids = ((hv[:-1] + hv[1:]) / 2).astype(np.float32)  # exact ties between neighbours
+    assert np.array_equal(mids.astype(np.float64), (hv[:-1] + hv[1:]) / 2)
+    r = rng(1)
+    rand_bits = r.integers(0, 2 ** 32, size=40000, dtype=np.uint64).astype(np.uint32)
+    rand = rand_bits.view(np.float32)
+    rand = rand[np.isfinite(rand)]
+    logs = (r.uniform(-30, 17, size=20000)).astype(np.float64)
+    scaled = (np.sign(r.standard_normal(20000)) * 2.0 ** logs).astype(np.float32)
+    specials = np.array([0.0, -0.0, 65504.0, 65519.996, 65520.0, 70000.0, 2 ** -24, 2 ** -25,
+                         1.5 * 2 ** -25, 2 ** -14, np.inf, -np.inf, 1e-30, 3.0e38],
+                        dtype=np.float32)
+    vals = np.concatenate([mids, -mids, hv.astype(np.float32), rand, scaled, specials])
+    ours = orc.f32_to_f16_bits(vals)
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_bf16_to_f32_matches_torch(orc):
+    torch = pytest.importorskip("torch")
+    codes = np.arange(0, 65536, 7, dtype=np.uint16)
+    ours = orc.bf16_bits_to_f32(codes)
+    ref = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).float().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+# ----------------------------------------------------------------------------
+# Quantisers.
+# ----------------------------------------------------------------------------
+
+def _hand_block():
+    # amax = 127 gives d = 1 exactly for both quantisers (127/127 is exact and 1.0 is
+    # an fp16 number), so q is round-half-away of the value itself.
+    v = np.zeros(32, np.float32)
+    v[:10] = [127.0, 63.5, -63.5, 2.5, -2.5, 0.5, -0.5, 0.49, -126.6, 1.5]
+    q = np.zeros(32, np.int8)
+    q[:10] = [127, 64, -64, 3, -3, 1, -1, 0, -127, 2]
+    return v, q
+
+
+def test_quantizers_hand_worked_block(orc):
+    v, q = _hand_block()
+    wq, wd = orc.quantize_q8_0(v[None, :])
+    assert wd[0, 0] == 0x3C00  # fp16 1.0
+    assert np.array_equal(wq[0], q)
+    xq, xd = orc.quantize_q8_1(v[None, :])
+    assert xd[0, 0] == np.float32(1.0)
+    assert np.array_equal(xq[0], q)
+    # bf16 input: every value above is exactly representable in bf16 except 0.49 and -126.6
+    torch = pytest.importorskip("torch")
+    bits = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    xq_b, xd_b = orc.quantize_q8_1(bits[None, :])
+    assert xd_b[0, 0] == np.float32(1.0)
+    assert np.array_equal(xq_b[0], q)
+
+
+def test_zero_block_gives_zero_scale_and_quants(orc):
+    w = np.zeros((2, 64), np.float32)
+    w[1, 32:] = rng(2).standard_normal(32).astype(np.float32)
+    wq, wd = orc.quantize_q8_0(w)
+    assert wd[0, 0] == 0 and wd[0, 1] == 0 and wd[1, 0] == 0 and wd[1, 1] != 0
+    assert not wq[0].any() and not wq[1, :32].any()
+    xq, xd = orc.quantize_q8_1(w)
+    assert xd[0, 0] == 0 and xd[1, 0] == 0 and xd[1, 1] > 0
+    assert not xq[0].any() and not xq[1, :32].any()
+
+
+@pytest.mark.parametrize("std", [0.02, 1.0, 300.0])
+def test_weight_quant_invariants(orc, std):
+    r = rng(3)
+    w = (r.standard_normal((64, 256)) * std).astype(np.float32)
+    wq, wd = orc.quantize_q8_0(w)
+    d = wd.view(np.float16).astype(np.float64)
+    assert wq.min() >= -127 and wq.max() <= 127
+    deq = np.repeat(d, 32, axis=1) * wq
+    err = np.abs(w.astype(np.float64) - deq)
+    assert np.all(err <= np.repeat(d, 32, axis=1) / 2 * (1 + 1e-6))
+    # the largest |w| in a block maps to +-127 (fp16 rounding of d moves amax/d by
+    # at most 2^-11 * 127 < 0.5)
+    blocks = np.abs(w).reshape(64, 8, 32)
+    idx = blocks.argmax(axis=2)
+    qb = np.abs(wq.reshape(64, 8, 32))
+    assert np.all(np.take_along_axis(qb, idx[..., None], axis=2) == 127)
+    # the scale is the fp16 value nearest amax/127 (checked with numpy's conversion)
+    amax = blocks.max(axis=2).astype(np.float32)
+    ref_d = (amax / np.float32(127.0)).astype(np.float16).view(np.uint16)
+    assert np.array_equal(wd, ref_d)
+
+
+def test_weight_quant_subnormal_scale_clamps(orc):
+    # amax tiny enough that fp16(amax/127) is subnormal and rounds DOWN by a lot:
+    # amax/127 = 1.4 * 2^-24 rounds to 2^-24, so amax/d = 177.8 -> clamped to 127.
+    amax = np.float32(1.4 * 2 ** -24 * 127)
+    w = np.zeros((1, 32), np.float32)
+    w[0, 0] = amax
+    w[0, 1] = -amax / 2
+    w[0, 2] = amax / 200
+    wq, wd = orc.quantize_q8_0(w)
+    assert wd[0, 0] == 1  # smallest subnormal
+    assert wq[0, 0] == 127
+    d = 2.0 ** -24
+    assert wq[0, 1] == -round(float(amax) / 2 / d + 0.0)  # 88.9 -> -89
+    assert wq[0, 2] == round(float(amax) / 200 / d)       # 0.889 -> 1
+
+
+@pytest.mark.parametrize("std", [1.0, 1e-3, 1e4])
+def test_activation_quant_invariants(orc, std):
+    r = rng(4)
+    x = (r.standard_normal((8, 512)) * std).astype(np.float32)
+    x[0, :32] = 0.0
+    xq, xd = orc.quantize_q8_1(x)
+    assert xq.min() >= -127 and xq.max() <= 127
+    amax = np.abs(x).reshape(8, 16, 32).max(axis=2)
+    # d is the IEEE fp32 quotient amax / 127
+    assert np.array_equal(xd, (amax / np.float32(127.0)).astype(np.float32))
+    d = np.repeat(xd.astype(np.float64), 32, axis=1)
+    err = np.abs(x.astype(np.float64) - d * xq)
+    assert np.all(err <= d / 2 * (1 + 1e-6))
+    idx = np.abs(x).reshape(8, 16, 32).argmax(axis=2)
+    qb = np.abs(xq.reshape(8, 16, 32))
+    hit = np.take_along_axis(qb, idx[..., None], axis=2)[..., 0]
+    assert np.all(hit[amax > 0] == 127)
+
+
+def test_quant_power_of_two_scaling(orc):
+    r = rng(5)
+    x = r.standard_normal((4, 128)).astype(np.float32)
+    q1, d1 = orc.quantize_q8_1(x)
+    for k in (-5, 1, 7):
+        q2, d2 = orc.quantize_q8_1(x * np.float32(2.0 ** k))
+        assert np.array_equal(q1, q2)
+        assert np.array_equal(d2, d1 * np.float32(2.0 ** k))
+    w = (r.standard_normal((4, 128)) * 0.02).astype(np.float32)
+    wq1, wd1 = orc.quantize_q8_0(w)
+    wq2, wd2 = orc.quantize_q8_0(w * np.float32(4.0))
+    assert np.array_equal(wq1, wq2)
+    assert np.array_equal(wd2.view(np.float16).astype(np.float32),
+                          wd1.view(np.float16).astype(np.float32) * 4)
+
+
+def test_quant_sign_symmetry(orc):
+    r = rng(6)
+    x = r.standard_normal((3, 96)).astype(np.float32)
+    q1, d1 = orc.quantize_q8_1(x)
+    q2, d2 = orc.quantize_q8_1(-x)
+    assert np.array_equal(q2, -q1) and np.array_equal(d1, d2)
+
+
+# ----------------------------------------------------------------------------
+# Block dots and the GEMV / skinny GEMM.
+# ----------------------------------------------------------------------------
+
+def _rand_q(r, shape):
+    return r.integers(-127, 128, size=shape).astype(np.int8)
+
+
+def test_block_dots_int64_brute_force(orc):
+    r = rng(7)
+    N, K, M = 5, 160, 3
+    wq = _rand_q(r, (N, K))
+    xq = _rand_q(r, (M, K))
+    s = orc.block_dots(wq, xq)
+    ref = np.einsum("nbi,mbi->mnb", wq.reshape(N, K // 32, 32).astype(np.int64),
+                    xq.reshape(M, K // 32, 32).astype(np.int64))
+    assert np.array_equal(s.astype(np.int64), ref)
+    # extreme block: every product 127*127 (or -127*-127)
+    s2 = orc.block_dots(np.full((1, 32), -127, np.int8), np.full((1, 32), -127, np.int8))
+    assert s2[0, 0, 0] == 32 * 127 * 127
+
+
+def _case(seed, N, K, M, wstd=0.02):
+    r = rng(seed)
+    w = (r.standard_normal((N, K)) * wstd).astype(np.float32)
+    x = r.standard_normal((M, K)).astype(np.float32)
+    return w, x
+
+
+def _abs_terms(orc, wq, wd, xq, xd):
+    s = orc.block_dots(wq, xq).astype(np.float64)  # [M, N, nb]
+    c = wd.view(np.float16).astype(np.float64)[None, :, :] * xd.astype(np.float64)[:, None, :]
+    return np.abs(c * s).sum(axis=2)  # [M, N]
+
+
+@pytest.mark.parametrize("N,K,M", [(7, 32, 1), (33, 544, 1), (16, 5120, 2), (9, 768, 8)])
+def test_gemm_within_bound_of_fp64_brute_force(orc, N, K, M):
+    w, x = _case(8 + K, N, K, M)
+    wq, wd = orc.quantize_q8_0(w)
+    xq, xd = orc.quantize_q8_1(x)
+    y = orc.gemm(wq, wd, xq, xd)
+    # independent fp64 brute force in numpy (dequantise, then matmul)
+    Wd = wq.astype(np.float64) * np.repeat(wd.view(np.float16).astype(np.float64), 32, axis=1)
+    Xd = xq.astype(np.float64) * np.repeat(xd.astype(np.float64), 32, axis=1)
+    y64 = Xd @ Wd.T
+    # the C fp64 brute force agrees with numpy
+    assert np.allclose(orc.dequant_gemm_f64(wq, wd, xq, xd), y64, rtol=1e-12, atol=1e-300)
+    nb = K // 32
+    gamma = (nb + 2) * U32 / (1 - (nb + 2) * U32)  # sequential-sum rounding bound
+    bound = gamma * _abs_terms(orc, wq, wd, xq, xd)
+    assert np.all(np.abs(y.astype(np.float64) - y64) <= bound + 1e-30)
+    # and the stated parity tolerance holds a fortiori
+    assert np.all(np.abs(y - y64) <= 1e-4 * _abs_terms(orc, wq, wd, xq, xd) + 1e-6)
+
+
+def test_gemm_close_to_unquantized_product(orc):
+    N, K, M = 24, 1024, 2
+    w, x = _case(9, N, K, M)
+    wq, wd = orc.quantize_q8_0(w)
+    xq, xd = orc.quantize_q8_1(x)
+    y = orc.gemm(wq, wd, xq, xd).astype(np.float64)
+    exact = x.astype(np.float64) @ w.astype(np.float64).T
+    dw = np.repeat(wd.view(np.float16).astype(np.float64), 32, axis=1)
+    dx = np.repeat(xd.astype(np.float64), 32, axis=1)
+    Wd = wq * dw
+    Xd = xq * dx
+    # |wx - w'x'| <= |w'| dx/2 + |x'| dw/2 + dw dx/4 elementwise
+    qerr = (np.abs(Xd) @ (dw / 2).T + (dx / 2) @ np.abs(Wd).T + (dx / 2) @ (dw / 2).T)
+    fperr = 1e-4 * _abs_terms(orc, wq, wd, xq, xd) + 1e-6
+    assert np.all(np.abs(y - exact) <= qerr + fperr)
+
+
+def test_gemm_one_hot_activation_exact(orc):
+    r = rng(10)
+    N, K = 6, 96
+    w = (r.standard_normal((N, K)) * 0.02).astype(np.float32)
+    wq, wd = orc.quantize_q8_0(w)
+    for j in (0, 31, 32, 77, 95):
+        x = np.zeros((1, K), np.float32)
+        x[0, j] = 3.0
+        xq, xd = orc.quantize_q8_1(x)
+        assert xq[0, j] == 127 and np.count_nonzero(xq) == 1
+        y = orc.gemm(wq, wd, xq, xd)[0]
+        dw = wd[:, j // 32].view(np.float16).astype(np.float32)
+        # single nonzero block sum s = 127 * q_w: y = fl(fl(d_w * d_x) * s)
+        c = (dw * xd[0, j // 32]).astype(np.float32)
+        expect = c * (np.int32(127) * wq[:, j].astype(np.int32)).astype(np.float32)
+        assert np.array_equal(y, expect.astype(np.float32))
+
+
+def test_gemm_power_of_two_linearity_exact(orc):
+    w, x = _case(11, 12, 320, 2)
+    wq, wd = orc.quantize_q8_0(w)
+    xq, xd = orc.quantize_q8_1(x)
+    y1 = orc.gemm(wq, wd, xq, xd)
+    xq2, xd2 = orc.quantize_q8_1(x * np.float32(8.0))
+    y2 = orc.gemm(wq, wd, xq2, xd2)
+    assert np.array_equal(y2, y1 * np.float32(8.0))
+
+
+def test_gemm_additivity_within_quantization_bound(orc):
+    r = rng(12)
+    N, K = 10, 256
+    w = (r.standard_normal((N, K)) * 0.02).astype(np.float32)
+    x1 = r.standard_normal((1, K)).astype(np.float32)
+    x2 = r.standard_normal((1, K)).astype(np.float32)
+    wq, wd = orc.quantize_q8_0(w)
+    ys = []
+    for x in (x1, x2, x1 + x2):
+        xq, xd = orc.quantize_q8_1(x)
+        ys.append(orc.gemm(wq, wd, xq, xd)[0].astype(np.float64))
+    dw = np.repeat(wd.view(np.float16).astype(np.float64), 32, axis=1)
+    Wd = wq * dw
+
+    def qbound(x):
+        _, xd = orc.quantize_q8_1(x)
+        return np.abs(Wd) @ (np.repeat(xd.astype(np.float64), 32, axis=1)[0] / 2)
+
+    tol = qbound(x1) + qbound(x2) + qbound(x1 + x2) + 1e-5
+    assert np.all(np.abs(ys[2] - ys[0] - ys[1]) <= tol)
+
+
+def test_gemm_row_permutation_exact(orc):
+    w, x = _case(13, 20, 192, 1)
+    wq, wd = orc.quantize_q8_0(w)
+    xq, xd = orc.quantize_q8_1(x)
+    y = orc.gemm(wq, wd, xq, xd)
+    p = rng(14).permutation(20)
+    yp = orc.gemm(wq[p], wd[p], xq, xd)
+    assert np.array_equal(yp, y[:, p])
+
+
+def test_gemm_zero_blocks(orc):
+    w, x = _case(15, 8, 256, 1)
+    w[3, :] = 0.0
+    x[0, 64:96] = 0.0
+    wq, wd = orc.quantize_q8_0(w)
+    xq, xd = orc.quantize_q8_1(x)
+    y = orc.gemm(wq, wd, xq, xd)
+    assert y[0, 3] == 0.0
+    keep = np.r_[0:64, 96:256]
+    keep_b = np.r_[0:2, 3:8]
+    y_cut = orc.gemm(wq[:, keep], wd[:, keep_b], xq[:, keep], xd[:, keep_b])
+    assert np.array_equal(y, y_cut)
+
+
+def test_gemm_rows_independent_of_m_and_threads(orc):
+    w, x = _case(16, 40, 640, 8)
+    wq, wd = orc.quantize_q8_0(w)
+    xq, xd = orc.quantize_q8_1(x)
+    y8 = orc.gemm(wq, wd, xq, xd)
+    for m in range(8):
+        y1 = orc.gemm(wq, wd, xq[m:m + 1], xd[m:m + 1])
+        assert np.array_equal(y1[0], y8[m])
+    assert np.array_equal(orc.gemm(wq, wd, xq, xd, threads=4), y8)
+
+
+# ----------------------------------------------------------------------------
+# exp, SwiGLU and the routed-expert GEMV.
+# ----------------------------------------------------------------------------
+
+def test_exp_cw_against_libm(orc):
+    xs = np.concatenate([np.linspace(-87.0, 88.0, 20001, dtype=np.float32),
+                         np.array([0.0, -0.0, 1e-8, -1e-8, 0.5, -0.5, 1.0], np.float32)])
+    ours = orc.exp_cw(xs).astype(np.float64)
+    ref = np.exp(xs.astype(np.float64))
+    rel = np.abs(ours - ref) / ref
+    assert rel.max() < 4 * U32 * 2  # within a few fp32 ulp
+    assert orc.exp_cw(np.array([0.0], np.float32))[0] == 1.0
+    # clamped outside [-87, 88]
+    assert orc.exp_cw(np.array([200.0], np.float32))[0] == orc.exp_cw(np.array([88.0],
+                                                                              np.float32))[0]
+
+
+def test_swiglu_against_fp64(orc):
+    r = rng(17)
+    R, F = 3, 96
+    gu = (r.standard_normal((R, 2 * F)) * 4).astype(np.float32)
+    gu[0, :5] = [0.0, -30.0, 30.0, -90.0, 1e-3]
+    h = orc.swiglu(gu).astype(np.float64)
+    g = gu[:, :F].astype(np.float64)
+    u = gu[:, F:].astype(np.float64)
+    ref = g / (1 + np.exp(-g)) * u
+    assert np.all(np.abs(h - ref) <= 1e-6 * np.abs(ref) + 1e-30 + 1e-36 * np.abs(u))
+    # gate half really is the first half: silu(g)*u is not symmetric in (g, u)
+    swapped = u / (1 + np.exp(-u)) * g
+    assert not np.allclose(h, swapped)
+
+
+def test_swiglu_quantize_is_quantize_of_swiglu(orc):
+    r = rng(18)
+    gu = r.standard_normal((4, 2 * 64)).astype(np.float32)
+    hq, hd = orc.swiglu_quantize_q8_1(gu)
+    q2, d2 = orc.quantize_q8_1(orc.swiglu(gu))
+    assert np.array_equal(hq, q2) and np.array_equal(hd, d2)
+
+
+def _bank(seed, E, N, K):
+    r = rng(seed)
+    w = (r.standard_normal((E, N, K)) * 0.02).astype(np.float32)
+    wq = np.empty((E, N, K), np.int8)
+    wd = np.empty((E, N, K // 32), np.uint16)
+    return w, wq, wd
+
+
+def test_moe_gemv_reduces_to_plain_gemv(orc):
+    E, N, K = 5, 24, 128
+    w, wq, wd = _bank(19, E, N, K)
+    for e in range(E):
+        wq[e], wd[e] = orc.quantize_q8_0(w[e])
+    r = rng(20)
+    x = r.standard_normal((3, K)).astype(np.float32)
+    xq, xd = orc.quantize_q8_1(x)
+    ids = np.array([4, 0, 2], np.int32)
+    # ungated, per-expert activations: row k is the plain GEMV of expert ids[k]
+    y, bad = orc.moe_gemv(wq, wd, ids, None, xq, xd, 1)
+    assert bad == 0
+    for k, e in enumerate(ids):
+        assert np.array_equal(y[k], orc.gemm(wq[e], wd[e], xq[k:k + 1], xd[k:k + 1])[0])
+    # ungated, shared activation
+    y, _ = orc.moe_gemv(wq, wd, ids, None, xq[:1], xd[:1], 0)
+    for k, e in enumerate(ids):
+        assert np.array_equal(y[k], orc.gemm(wq[e], wd[e], xq[:1], xd[:1])[0])
+    # top-1 with weight 1: the gated sum is that expert's GEMV exactly
+    y1, _ = orc.moe_gemv(wq, wd, ids[:1], np.ones(1, np.float32), xq[:1], xd[:1], 0)
+    assert np.array_equal(y1, orc.gemm(wq[4], wd[4], xq[:1], xd[:1])[0])
+
+
+def test_moe_gemv_gated_sum_against_fp64(orc):
+    E, N, K = 6, 16, 96
+    w, wq, wd = _bank(21, E, N, K)
+    for e in range(E):
+        wq[e], wd[e] = orc.quantize_q8_0(w[e])
+    r = rng(22)
+    x = r.standard_normal((4, K)).astype(np.float32)
+    xq, xd = orc.quantize_q8_1(x)
+    ids = np.array([5, 1, 3, 1], np.int32)
+    gw = np.array([0.4, 0.3, 0.2, 0.1], np.float32)
+    y, bad = orc.moe_gemv(wq, wd, ids, gw, xq, xd, 1)
+    assert bad == 0
+    ref = np.zeros(N)
+    tol = np.zeros(N)
+    for k, e in enumerate(ids):
+        ref += gw[k] * orc.dequant_gemm_f64(wq[e], wd[e], xq[k:k + 1], xd[k:k + 1])[0]
+        tol += abs(gw[k]) * _abs_terms(orc, wq[e], wd[e], xq[k:k + 1], xd[k:k + 1])[0]
+    assert np.all(np.abs(y - ref) <= 1e-4 * tol + 1e-6)
+
+
+def test_moe_gemv_out_of_range_ids(orc):
+    E, N, K = 3, 8, 64
+    w, wq, wd = _bank(23, E, N, K)
+    for e in range(E):
+        wq[e], wd[e] = orc.quantize_q8_0(w[e])
+    xq, xd = orc.quantize_q8_1(rng(24).standard_normal((1, K)).astype(np.float32))
+    ids = np.array([1, 3, -1], np.int32)
+    y, bad = orc.moe_gemv(wq, wd, ids, None, xq, xd, 0)
+    assert bad == 2
+    assert not y[1].any() and not y[2].any()
+    assert np.array_equal(y[0], orc.gemm(wq[1], wd[1], xq, xd)[0])
+    yg, bad = orc.moe_gemv(wq, wd, ids, np.array([1.0, 5.0, 7.0], np.float32), xq, xd, 0)
+    assert bad == 2 and np.array_equal(yg, y[0])
+
+
+def test_moe_ffn_single_expert_is_dense_ffn(orc):
+    # E = 1, top_k = 1, weight 1: the layer is a dense SwiGLU FFN with Q8_0 weights.
+    K, F, N_out = 64, 32, 64
+    r = rng(25)
+    wgu = (r.standard_normal((1, 2 * F, K)) * 0.05).astype(np.float32)
+    wdn = (r.standard_normal((1, N_out, F)) * 0.05).astype(np.float32)
+    gq, gd = orc.quantize_q8_0(wgu[0])
+    dq, dd = orc.quantize_q8_0(wdn[0])
+    x = r.standard_normal(K).astype(np.float32)
+    y, bad = orc.moe_ffn(x, gq[None], gd[None], dq[None], dd[None], np.zeros(1, np.int32),
+                         np.ones(1, np.float32))
+    assert bad == 0
+    xq, xd = orc.quantize_q8_1(x[None])
+    hgu = orc.gemm(gq, gd, xq, xd)
+    hq, hd = orc.swiglu_quantize_q8_1(hgu)
+    ref = orc.gemm(dq, dd, hq, hd)[0]
+    assert np.array_equal(y, ref)
+    # and it tracks the unquantised fp64 FFN to within quantisation-level error
+    xf = x.astype(np.float64)
+    g_u = wgu[0].astype(np.float64) @ xf
+    h = g_u[:F] / (1 + np.exp(-g_u[:F])) * g_u[F:]
+    y64 = wdn[0].astype(np.float64) @ h
+    assert np.max(np.abs(y - y64)) < 0.05 * np.max(np.abs(y64)) + 1e-6
