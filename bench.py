@@ -1,0 +1,626 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q8_0 decode hot path on GB300.
+
+Default workload (one "step" = one decode token): a dense ~27B decode sweep, M = 1,
+64 layers of distinct seeded weights, each layer = 4 x (q8_1 quantise of a bf16
+activation, Q8_0 GEMV): fused QKV 5120->7168, O 5120->5120, gate+up 5120->34816,
+down 17408->5120.  22.46 GB of Q8_0 weights stream from HBM per step (far above the
+129 MB L2, so no flush is needed between steps).
+
+Prints ONE JSON line.  ``value`` is weight-stream GB/s over the whole job (all
+ranks); ``e2e`` repeats the measurement through the public API with the step's
+activations copied in from pinned host memory and every output copied back;
+``roofline`` is the GEMV kernel's achieved HBM bandwidth against the measured copy
+peak; ``cpu_baseline`` is the CPU oracle on the host cores over a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl memra|reference]
+                  [--workload dense27b_sweep|gemv_4096|verify_m2|verify_m4|verify_m8|
+                              moe_top8|stress_lm_head]
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = ("Q8_0 decode GEMV weight-stream GB/s (% of GB300 HBM peak); "
+          "µs per 27B layer sweep")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8", "moe_top8",
+             "stress_lm_head")
+
+
+# ----------------------------------------------------------------------------
+# Workload construction (inputs from synth, weights quantised by the library).
+# ----------------------------------------------------------------------------
+
+class Gemv:
+    """One Q8_0 product of a step: weights, its bf16 activation(s), q8_1 buffers, y."""
+
+    def __init__(self, wq, wd, x, name):
+        self.wq, self.wd, self.x, self.name = wq, wd, x, name
+        M, K = x.shape
+        N = wq.shape[0]
+        dev = wq.device
+        self.xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+        self.xd = torch.empty((M, K // 32), dtype=torch.float32, device=dev)
+        self.y = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+    @property
+    def weight_bytes(self):
+        return synth.q8_0_bytes(*self.wq.shape)
+
+
+def quantized_weights(mem, N, K, *keys, device, perturb=None):
+    w = synth.weights_fp32(N, K, *keys, device=device)
+    if perturb:
+        synth.perturb_blocks(w, *keys, **perturb)
+    wq, wd = mem.memra_quantize_q8_0(w)
+    del w
+    return wq, wd
+
+
+def build_dense_sweep(mem, device, M=1, layers=None, workload_id=1):
+    """The dense 27B-class sweep: per layer QKV, O, gate+up, down."""
+    cfg = synth.DENSE27B
+    L = cfg["layers"] if layers is None else layers
+    ops = []
+    for layer in range(L):
+        for t, (name, N, K) in enumerate(cfg["gemvs"]):
+            wq, wd = quantized_weights(mem, N, K, workload_id, layer, t, device=device)
+            x = synth.activations_bf16(M, K, workload_id, layer, t, 1000 + M,
+                                       outlier_frac=cfg["outlier_frac"],
+                                       outlier_scale=cfg["outlier_scale"], device=device)
+            ops.append(Gemv(wq, wd, x, "L%d.%s" % (layer, name)))
+    return ops
+
+
+def build_gemv_4096(mem, device, copies=32):
+    """One 4096x4096 GEMV (seed 0); `copies` distinct weight copies rotate so that the
+    weights of consecutive calls are not L2 resident (32 x 17.8 MB >> 129 MB L2)."""
+    c = synth.GEMV_4096
+    wq, wd = quantized_weights(mem, c["N"], c["K"], c["seed"], device=device)
+    x = synth.activations_bf16(1, c["K"], c["seed"], 1, device=device)
+    ops = []
+    for i in range(copies):
+        ops.append(Gemv(wq.clone() if i else wq, wd.clone() if i else wd, x, "copy%d" % i))
+    return ops
+
+
+def build_stress(mem, device, M):
+    s = synth.STRESS
+    ops = []
+    for t, (name, N, K) in enumerate(s["shapes"]):
+        wq, wd = quantized_weights(mem, N, K, 4, t, device=device,
+                                   perturb=dict(zero_frac=s["zero_frac"],
+                                                scale_frac=s["scale_frac"], scale=s["scale"]))
+        x = synth.activations_bf16(M, K, 4, t, 1000 + M, device=device)
+        ops.append(Gemv(wq, wd, x, name))
+    return ops
+
+
+class MoeLayer:
+    def __init__(self, mem, layer, device):
+        c = synth.MOE
+        E, H, F, k = c["experts"], c["hidden"], c["ffn"], c["top_k"]
+        gq, gd = quantized_weights(mem, E * 2 * F, H, 3, layer, 0, device=device)
+        dq, dd = quantized_weights(mem, E * H, F, 3, layer, 1, device=device)
+        self.gq, self.gd = gq.view(E, 2 * F, H), gd.view(E, 2 * F, H // 32)
+        self.dq, self.dd = dq.view(E, H, F), dd.view(E, H, F // 32)
+        self.ids, self.gw = synth.routing(E, k, 3, layer, 2, device=device)
+        self.x = synth.activations_bf16(1, H, 3, layer, 3, device=device)
+        self.xq = torch.empty((1, H), dtype=torch.int8, device=device)
+        self.xd = torch.empty((1, H // 32), dtype=torch.float32, device=device)
+        self.ygu = torch.empty((k, 2 * F), dtype=torch.float32, device=device)
+        self.hq = torch.empty((k, F), dtype=torch.int8, device=device)
+        self.hd = torch.empty((k, F // 32), dtype=torch.float32, device=device)
+        self.y = torch.empty((H,), dtype=torch.float32, device=device)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=device)
+        self.weight_bytes = k * (synth.q8_0_bytes(2 * F, H) + synth.q8_0_bytes(H, F))
+
+    def run(self, mem):
+        mem.memra_quantize_q8_1(self.x, self.xq, self.xd)
+        mem.memra_q8_0_moe_gemv(self.gq, self.gd, self.ids, None, self.xq[0], self.xd[0], False,
+                                y=self.ygu, dev_status=self.status)
+        mem.memra_swiglu_quantize_q8_1(self.ygu, self.hq, self.hd)
+        mem.memra_q8_0_moe_gemv(self.dq, self.dd, self.ids, self.gw, self.hq, self.hd, True,
+                                y=self.y, dev_status=self.status)
+
+
+def run_gemv_op(mem, op, quantize=True):
+    if quantize:
+        mem.memra_quantize_q8_1(op.x, op.xq, op.xd)
+    if op.xq.shape[0] == 1:
+        mem.memra_q8_0_gemv(op.wq, op.wd, op.xq[0], op.xd[0], y=op.y[0])
+    else:
+        mem.memra_q8_0_gemm_small_m(op.wq, op.wd, op.xq, op.xd, y=op.y)
+
+
+class Workload:
+    """A step = a fixed list of library calls; captured once into a CUDA graph."""
+
+    def __init__(self, name, mem, device):
+        self.name = name
+        self.mem = mem
+        self.device = device
+        self.moe = None
+        self.ops = []
+        if name == "dense27b_sweep":
+            self.ops = build_dense_sweep(mem, device, M=1)
+        elif name.startswith("verify_m"):
+            self.ops = build_dense_sweep(mem, device, M=int(name[len("verify_m"):]),
+                                         workload_id=2)
+        elif name == "gemv_4096":
+            self.ops = build_gemv_4096(mem, device)
+        elif name == "stress_lm_head":
+            self.ops = build_stress(mem, device, M=1) + build_stress(mem, device, M=8)
+        elif name == "moe_top8":
+            self.moe = [MoeLayer(mem, layer, device) for layer in range(synth.MOE["layers"])]
+        else:
+            raise ValueError(name)
+        torch.cuda.synchronize(device)
+
+    @property
+    def weight_bytes(self):
+        if self.moe is not None:
+            return sum(m.weight_bytes for m in self.moe)
+        return sum(op.weight_bytes for op in self.ops)
+
+    @property
+    def launches_per_step(self):
+        if self.moe is not None:
+            return 4 * len(self.moe)
+        return 2 * len(self.ops)
+
+    @property
+    def gemv_launches_per_step(self):
+        if self.moe is not None:
+            return 2 * len(self.moe)
+        return len(self.ops)
+
+    def step(self):
+        if self.moe is not None:
+            for m in self.moe:
+                m.run(self.mem)
+        else:
+            for op in self.ops:
+                run_gemv_op(self.mem, op)
+
+    def gemv_only(self):
+        """The step's weight-streaming kernels alone (activations already quantised)."""
+        if self.moe is not None:
+            for m in self.moe:
+                self.mem.memra_q8_0_moe_gemv(m.gq, m.gd, m.ids, None, m.xq[0], m.xd[0], False,
+                                             y=m.ygu, dev_status=m.status)
+                self.mem.memra_q8_0_moe_gemv(m.dq, m.dd, m.ids, m.gw, m.hq, m.hd, True,
+                                             y=m.y, dev_status=m.status)
+        else:
+            for op in self.ops:
+                run_gemv_op(self.mem, op, quantize=False)
+
+    def inputs(self):
+        if self.moe is not None:
+            return [m.x for m in self.moe]
+        seen, out = set(), []
+        for op in self.ops:
+            if id(op.x) not in seen:
+                seen.add(id(op.x))
+                out.append(op.x)
+        return out
+
+    def outputs(self):
+        if self.moe is not None:
+            return [m.y for m in self.moe]
+        return [op.y for op in self.ops]
+
+    def capture(self, fn):
+        stream = torch.cuda.Stream(self.device)
+        stream.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(stream):
+            fn()  # warm-up outside the graph (sets kernel attributes)
+        torch.cuda.synchronize(self.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        torch.cuda.synchronize(self.device)
+        return g
+
+
+# ----------------------------------------------------------------------------
+# Timing helpers.
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.lines = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            if not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", uuid, "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+                power.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value, world_size, device=None, backend_device="cpu"):
+    """Max of a float over all ranks (identity for one rank)."""
+    if world_size <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=backend_device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world_size):
+    if world_size > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(kernel_source_hash):
+    """DRAM bytes per launch of the GEMV kernel from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "gemv_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_source_sha256") == kernel_source_hash:
+            return d
+    except Exception:
+        pass
+    return None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "block_quantized_decode_quantize_gb300", "csrc",
+                               name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def time_graph(graph, reps, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1000.0
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle sample (the reported CPU baseline and the reference arm).
+# ----------------------------------------------------------------------------
+
+class CpuOracleSample:
+    """The CPU oracle (quantise x + GEMV, all host threads) on layer 0's four products
+    of the dense sweep.  Weight ingest is done once, untimed, like the GPU's."""
+
+    def __init__(self):
+        import numpy as np
+
+        import oracle
+        self.oracle = oracle
+        self.threads = os.cpu_count() or 1
+        cfg = synth.DENSE27B
+        self.items = []
+        for t, (name, N, K) in enumerate(cfg["gemvs"]):
+            w = synth.weights_fp32(N, K, 1, 0, t, device="cpu").numpy()
+            wq, wd = oracle.quantize_q8_0(w)
+            del w
+            x = synth.activations_bf16(1, K, 1, 0, t, 1001, outlier_frac=cfg["outlier_frac"],
+                                       outlier_scale=cfg["outlier_scale"])
+            xb = x.view(torch.int16).numpy().view(np.uint16)
+            self.items.append((name, wq, wd, xb, synth.q8_0_bytes(N, K)))
+        self.done = 0
+
+    def run_one(self):
+        """Run the next product; returns (seconds, weight bytes)."""
+        name, wq, wd, xb, b = self.items[self.done % len(self.items)]
+        t0 = time.perf_counter()
+        xq, xd = self.oracle.quantize_q8_1(xb)
+        self.oracle.gemm(wq, wd, xq, xd, threads=self.threads)
+        dt = time.perf_counter() - t0
+        self.done += 1
+        return dt, b
+
+    def run_for(self, budget_s):
+        """Run products until `budget_s` seconds of oracle time; returns (GB/s, seconds,
+        products)."""
+        spent, nbytes, n = 0.0, 0, 0
+        while spent < budget_s or n < len(self.items):
+            dt, b = self.run_one()
+            spent += dt
+            nbytes += b
+            n += 1
+        return nbytes / spent / 1e9, spent, n
+
+    def describe(self, n):
+        return ("%d Q8_0 products (q8_1 quantise of x + GEMV) cycling through layer 0's QKV, "
+                "O, gate+up and down of the dense sweep; %d OpenMP threads"
+                % (n, self.threads))
+
+
+# ----------------------------------------------------------------------------
+# Arms.
+# ----------------------------------------------------------------------------
+
+def workload_config(name, wl):
+    cfg = {"workload": name}
+    if name == "dense27b_sweep" or name.startswith("verify_m"):
+        cfg.update({"layers": synth.DENSE27B["layers"], "hidden": synth.DENSE27B["hidden"],
+                    "gemvs_per_layer": [[n, N, K] for n, N, K in synth.DENSE27B["gemvs"]],
+                    "M": 1 if name == "dense27b_sweep" else int(name[len("verify_m"):]),
+                    "activations": "bf16 N(0,1), 0.1% of entries x20"})
+    elif name == "gemv_4096":
+        cfg.update({"N": 4096, "K": 4096, "M": 1, "weight_copies": len(wl.ops)})
+    elif name == "moe_top8":
+        cfg.update(dict(synth.MOE))
+    elif name == "stress_lm_head":
+        cfg.update({"shapes": [[n, N, K] for n, N, K in synth.STRESS["shapes"]], "M": [1, 8]})
+    cfg["weights"] = "N(0,0.02) fp32 quantised to Q8_0 (32 int8 + fp16 scale per block)"
+    cfg["weight_bytes_per_step"] = wl.weight_bytes
+    cfg["l2"] = ("inputs larger than L2: %.2f GB of distinct weights per step vs 129 MB L2"
+                 % (wl.weight_bytes / 1e9))
+    return cfg
+
+
+def run_memra(args):
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import block_quantized_decode_quantize_gb300 as mem
+    from block_quantized_decode_quantize_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    barrier(world)
+    mem.lib()
+
+    wl = Workload(args.workload, mem, device)
+    stream = torch.cuda.Stream(device)
+    step_graph = wl.capture(wl.step)
+    gemv_graph = wl.capture(wl.gemv_only)
+
+    # Warm-up, then the timed region: K graph replays of the whole step.
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            step_graph.replay()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(device)
+    time.sleep(0.2)
+    elapsed = time_graph(step_graph, args.steps, stream)
+    torch.cuda.synchronize(device)
+    clock_info = clocks.stop()
+    barrier(world)
+    elapsed_max = max_over_ranks(elapsed, world, backend_device=device)
+
+    bytes_step = wl.weight_bytes
+    value = world * bytes_step * args.steps / elapsed_max / 1e9
+    ms_per_step = elapsed_max / args.steps * 1e3
+
+    # Dominant kernel: the weight-streaming GEMV alone, same buffers and launch shapes.
+    g_elapsed = time_graph(gemv_graph, args.steps, stream)
+    n_gemv = wl.gemv_launches_per_step * args.steps
+    gemv_avg_s = g_elapsed / n_gemv
+    bytes_per_launch = bytes_step / wl.gemv_launches_per_step
+    achieved = bytes_per_launch / gemv_avg_s / 1e9
+    peak, peak_kind = measured_peaks()
+    prof = profile_traffic(kernel_source_hash())
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": (round(prof["dram_bytes_per_launch"] * bytes_per_launch /
+                                  prof["weight_bytes_per_launch"])
+                            if prof else None),
+                "peak_kind": peak_kind + " copy bandwidth (MEASURED_PEAKS hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "kernel": "q8_gemm_kernel (Q8_0 GEMV, M=%s)" % (
+                    1 if wl.moe is not None else wl.ops[0].xq.shape[0]),
+                "avg_launch_us": round(gemv_avg_s * 1e6, 3),
+                "bytes_per_launch": int(bytes_per_launch),
+                "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
+
+    # End to end through the public API: pinned host activations in, every output out.
+    ins = wl.inputs()
+    outs = wl.outputs()
+    h_in = [t.detach().cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    e2e_steps = max(3, min(args.steps, 50))
+    torch.cuda.synchronize(device)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            for d, h in zip(ins, h_in):
+                d.copy_(h, non_blocking=True)
+            step_graph.replay()
+            for h, d in zip(h_out, outs):
+                h.copy_(d, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, world, backend_device=device)
+    e2e_value = world * bytes_step * e2e_steps / e2e_s / 1e9
+
+    status_bad = 0
+    if wl.moe is not None:
+        status_bad = int(sum(int(m.status.item()) for m in wl.moe))
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cs = CpuOracleSample()
+        v, spent, n = cs.run_for(args.cpu_budget)
+        cpu = {"value": round(v, 3), "unit": "GB/s", "cores": cs.threads, "kind": "oracle",
+               "sample": cs.describe(n), "seconds": round(spent, 2)}
+
+    if rank == 0:
+        cfg = workload_config(args.workload, wl)
+        cfg["parallelism"] = "replicas x%d (no data-path collective)" % world
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8 (dp4a int32 block sums, fp32 scale-accumulate)",
+            "data": "synthetic (seeded N(0,0.02) weights, bf16 N(0,1) activations)",
+            "config": cfg,
+            "us_per_step": round(ms_per_step * 1e3, 2),
+            "tok_per_s": round(1e3 / ms_per_step, 2) if args.workload in (
+                "dense27b_sweep", "moe_top8") or args.workload.startswith("verify_m") else None,
+            "hbm_frac_of_measured": round(value / world / peak, 4),
+            "hbm_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "pinned H2D of the step's activations, CUDA-graph replay of the "
+                            "step's C-ABI calls, D2H of every output, host sync per step",
+                    "steps": e2e_steps},
+            "gpu_launches": wl.launches_per_step * args.steps,
+            "clocks": clock_info,
+        }
+        if status_bad:
+            line["moe_status_flags"] = status_bad
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    cs = CpuOracleSample()
+    for _ in range(args.warmup):
+        cs.run_one()
+    spent, nbytes = 0.0, 0
+    for _ in range(args.steps):
+        dt, b = cs.run_one()
+        spent += dt
+        nbytes += b
+    value = nbytes / spent / 1e9
+    sample = ("each step one Q8_0 product (q8_1 quantise of x + GEMV) of layer 0 of the dense "
+              "sweep, cycling QKV, O, gate+up, down; %d OpenMP threads" % cs.threads)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(spent / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "impl": "reference",
+        "dtype": "int8 (int32 block sums, fp32 scale-accumulate)",
+        "data": "synthetic (seeded N(0,0.02) weights, bf16 N(0,1) activations)",
+        "config": {"workload": "dense27b_sweep", "layers_sampled": 1, "M": 1},
+        "cpu_baseline": {"value": round(value, 3), "kind": "oracle", "cores": cs.threads,
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("memra", "reference"), default="memra")
+    ap.add_argument("--workload", choices=WORKLOADS, default="dense27b_sweep")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_memra(args)
+
+
+if __name__ == "__main__":
+    main()

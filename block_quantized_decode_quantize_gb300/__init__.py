@@ -1,0 +1,260 @@
+"""memra-gb300: Q8_0 decode GEMV / verify GEMM / routed-expert GEMV for GB300.
+
+A thin Python binding over the C ABI in ``include/memra.h`` (``libmemra.so``).
+The binding only marshals arguments: it checks tensor devices, dtypes, shapes and
+contiguity, allocates outputs with torch when the caller passes none, and calls the
+library on the current torch CUDA stream.  Every step of the computation runs in the
+library's sm_103a kernels; there is no fallback.  If the library has not been built
+(``block_quantized_decode_quantize_gb300.build.build()``) loading it raises.
+
+Tensor conventions (all on one CUDA device, contiguous):
+  wq  int8 [N, K]          Q8_0 quants            wd  float16 [N, K/32]  Q8_0 scales
+  xq  int8 [M, K]          q8_1 quants            xd  float32 [M, K/32]  q8_1 scales
+  y   float32 [M, N]       (the GEMV takes and returns 1-D x / y)
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MEMRA_OK = 0
+MEMRA_BF16 = 0
+MEMRA_F32 = 1
+MAX_M = 8
+MAX_TOP_K = 64
+
+_STATUS = {0: "MEMRA_OK", 1: "MEMRA_ERR_INVALID_ARG", 2: "MEMRA_ERR_ALIGNMENT",
+           3: "MEMRA_ERR_UNSUPPORTED", 4: "MEMRA_ERR_CUDA"}
+
+
+class MemraError(RuntimeError):
+    def __init__(self, fn, status, cuda_error=0):
+        self.status = status
+        self.cuda_error = cuda_error
+        msg = "%s returned %s" % (fn, _STATUS.get(status, status))
+        if cuda_error:
+            msg += " (cudaError %d)" % cuda_error
+        super().__init__(msg)
+
+
+_lib = None
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+
+_SIGS = {
+    "memra_quantize_q8_0": [_p, _i64, _i64, _p, _p, _p],
+    "memra_quantize_q8_1": [_p, _i32, _i64, _i64, _p, _p, _p],
+    "memra_q8_0_gemv": [_p, _p, _i64, _i64, _p, _p, _p, _p],
+    "memra_q8_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
+    "memra_q8_0_moe_gemv": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p, _p],
+    "memra_swiglu_quantize_q8_1": [_p, _i64, _i64, _p, _p, _p],
+    "memra_q8_0_block_dots": [_p, _i64, _i64, _p, _i64, _p, _p],
+}
+
+
+def library_path():
+    return _build.LIB
+
+
+def lib():
+    """The loaded C library (ctypes), with argument types set for every entry point."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError("libmemra.so is not built (expected at %s); run "
+                               "block_quantized_decode_quantize_gb300.build.build()" % path)
+        L = ctypes.CDLL(path)
+        for name, args in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.memra_status_string.argtypes = [ctypes.c_int]
+        L.memra_status_string.restype = ctypes.c_char_p
+        L.memra_last_cuda_error.restype = ctypes.c_int32
+        L.memra_version.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(name, status):
+    if status != MEMRA_OK:
+        L = lib()
+        raise MemraError(name, status, L.memra_last_cuda_error() if status == 4 else 0)
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, name, dtype, device=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must have dtype %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+def memra_quantize_q8_0(w, wq=None, wd=None):
+    """fp32 weights [N, K] -> (wq int8 [N, K], wd float16 [N, K/32])."""
+    _need(w, "w", torch.float32)
+    N, K = w.shape
+    if wq is None:
+        wq = torch.empty((N, K), dtype=torch.int8, device=w.device)
+    if wd is None:
+        wd = torch.empty((N, K // 32), dtype=torch.float16, device=w.device)
+    _need(wq, "wq", torch.int8, w.device, (N, K))
+    _need(wd, "wd", torch.float16, w.device, (N, K // 32))
+    with torch.cuda.device(w.device):
+        _check("memra_quantize_q8_0",
+               lib().memra_quantize_q8_0(_ptr(w), N, K, _ptr(wq), _ptr(wd), _stream(w)))
+    return wq, wd
+
+
+def memra_quantize_q8_1(x, xq=None, xd=None):
+    """Activations [M, K] (bf16 or fp32) -> (xq int8 [M, K], xd float32 [M, K/32])."""
+    if x.dtype == torch.bfloat16:
+        dt = MEMRA_BF16
+    elif x.dtype == torch.float32:
+        dt = MEMRA_F32
+    else:
+        raise TypeError("x must be bfloat16 or float32")
+    _need(x, "x", x.dtype)
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if xd is None:
+        xd = torch.empty((M, K // 32), dtype=torch.float32, device=x.device)
+    _need(xq, "xq", torch.int8, x.device, (M, K))
+    _need(xd, "xd", torch.float32, x.device, (M, K // 32))
+    with torch.cuda.device(x.device):
+        _check("memra_quantize_q8_1",
+               lib().memra_quantize_q8_1(_ptr(x), dt, M, K, _ptr(xq), _ptr(xd), _stream(x)))
+    return xq, xd
+
+
+def memra_q8_0_gemm_small_m(wq, wd, xq, xd, y=None):
+    """y [M, N] = W (Q8_0) x (q8_1) for M <= 8 activation rows."""
+    _need(wq, "wq", torch.int8)
+    N, K = wq.shape
+    dev = wq.device
+    _need(wd, "wd", torch.float16, dev, (N, K // 32))
+    _need(xq, "xq", torch.int8, dev)
+    M = xq.shape[0]
+    _need(xq, "xq", torch.int8, dev, (M, K))
+    _need(xd, "xd", torch.float32, dev, (M, K // 32))
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, (M, N))
+    with torch.cuda.device(dev):
+        _check("memra_q8_0_gemm_small_m",
+               lib().memra_q8_0_gemm_small_m(_ptr(wq), _ptr(wd), N, K, M, _ptr(xq), _ptr(xd),
+                                             _ptr(y), _stream(wq)))
+    return y
+
+
+def memra_q8_0_gemv(wq, wd, xq, xd, y=None):
+    """y [N] = W (Q8_0) x (q8_1) for one activation row (xq [K], xd [K/32])."""
+    _need(wq, "wq", torch.int8)
+    N, K = wq.shape
+    dev = wq.device
+    _need(wd, "wd", torch.float16, dev, (N, K // 32))
+    _need(xq, "xq", torch.int8, dev, (K,))
+    _need(xd, "xd", torch.float32, dev, (K // 32,))
+    if y is None:
+        y = torch.empty((N,), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, (N,))
+    with torch.cuda.device(dev):
+        _check("memra_q8_0_gemv",
+               lib().memra_q8_0_gemv(_ptr(wq), _ptr(wd), N, K, _ptr(xq), _ptr(xd), _ptr(y),
+                                     _stream(wq)))
+    return y
+
+
+def memra_q8_0_moe_gemv(wq_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert, y=None,
+                        dev_status=None):
+    """Routed-expert GEMV.  wq_bank int8 [E, N, K], wd_bank float16 [E, N, K/32],
+    ids int32 [top_k], gate_w float32 [top_k] or None.  x_per_expert=False: xq [K],
+    xd [K/32]; True: xq [top_k, K], xd [top_k, K/32].  Returns y [top_k, N] without
+    gate weights, [N] with them."""
+    _need(wq_bank, "wq_bank", torch.int8)
+    E, N, K = wq_bank.shape
+    dev = wq_bank.device
+    _need(wd_bank, "wd_bank", torch.float16, dev, (E, N, K // 32))
+    _need(ids, "ids", torch.int32, dev)
+    top_k = ids.shape[0]
+    if gate_w is not None:
+        _need(gate_w, "gate_w", torch.float32, dev, (top_k,))
+    xpe = 1 if x_per_expert else 0
+    if xpe:
+        _need(xq, "xq", torch.int8, dev, (top_k, K))
+        _need(xd, "xd", torch.float32, dev, (top_k, K // 32))
+    else:
+        _need(xq, "xq", torch.int8, dev, (K,))
+        _need(xd, "xd", torch.float32, dev, (K // 32,))
+    yshape = (N,) if gate_w is not None else (top_k, N)
+    if y is None:
+        y = torch.empty(yshape, dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, yshape)
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    with torch.cuda.device(dev):
+        _check("memra_q8_0_moe_gemv",
+               lib().memra_q8_0_moe_gemv(_ptr(wq_bank), _ptr(wd_bank), E, N, K, _ptr(ids),
+                                         _ptr(gate_w), top_k, _ptr(xq), _ptr(xd), xpe, _ptr(y),
+                                         _ptr(dev_status), _stream(wq_bank)))
+    return y
+
+
+def memra_swiglu_quantize_q8_1(gu, hq=None, hd=None):
+    """gu float32 [R, 2F] (gate | up) -> (hq int8 [R, F], hd float32 [R, F/32])."""
+    _need(gu, "gu", torch.float32)
+    R, F2 = gu.shape
+    F = F2 // 2
+    if hq is None:
+        hq = torch.empty((R, F), dtype=torch.int8, device=gu.device)
+    if hd is None:
+        hd = torch.empty((R, F // 32), dtype=torch.float32, device=gu.device)
+    _need(hq, "hq", torch.int8, gu.device, (R, F))
+    _need(hd, "hd", torch.float32, gu.device, (R, F // 32))
+    with torch.cuda.device(gu.device):
+        _check("memra_swiglu_quantize_q8_1",
+               lib().memra_swiglu_quantize_q8_1(_ptr(gu), R, F, _ptr(hq), _ptr(hd),
+                                                _stream(gu)))
+    return hq, hd
+
+
+def memra_q8_0_block_dots(wq, xq, s=None):
+    """Exact int32 block sums s [M, N, K/32]."""
+    _need(wq, "wq", torch.int8)
+    N, K = wq.shape
+    dev = wq.device
+    _need(xq, "xq", torch.int8, dev)
+    M = xq.shape[0]
+    _need(xq, "xq", torch.int8, dev, (M, K))
+    if s is None:
+        s = torch.empty((M, N, K // 32), dtype=torch.int32, device=dev)
+    _need(s, "s", torch.int32, dev, (M, N, K // 32))
+    with torch.cuda.device(dev):
+        _check("memra_q8_0_block_dots",
+               lib().memra_q8_0_block_dots(_ptr(wq), N, K, _ptr(xq), M, _ptr(s), _stream(wq)))
+    return s
+
+
+def version():
+    return lib().memra_version().decode()

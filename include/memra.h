@@ -1,0 +1,167 @@
+/*
+ * memra.h -- C ABI of the GB300 (sm_103a) Q8_0 decode library.
+ *
+ * The single-user decode step of an LLM streams block-quantised weights through
+ * a fused dequantise matrix-vector (M = 1) or skinny matrix (M <= 8, speculative
+ * verify) product, plus a routed-expert (MoE) variant.  The memra pages name this
+ * path: Q8_0 decode through split-plane repacked matvecs with warp-level dp4a and
+ * per-shape dispatch (memra wiki, github.com/avifenesh/memra/wiki, feature list);
+ * one batched K+1 verify for MTP speculative decoding (same list); routed MoE
+ * experts (same list); Q8_0 27B plain decode as a measured cell ("memra
+ * performance", docs/PERFORMANCE.md, historical 27B board).  They print no block
+ * layout or formula; the arithmetic stated here is GGUF's Q8_0 format as the
+ * workloads define it.
+ *
+ * Formats (all row-major, "split-plane": quants and scales in separate arrays):
+ *   Q8_0 weights   wq int8 [N][K] and wd fp16 (IEEE binary16 bits) [N][K/32].
+ *                  Block b of row n covers k in [32b, 32b+32):
+ *                  w[n][k] ~= float(wd[n][b]) * wq[n][k].
+ *   q8_1 activation xq int8 [M][K] and xd fp32 [M][K/32]:
+ *                  x[m][k] ~= xd[m][b] * xq[m][k].
+ *   Quantisation of a block: amax = max|v|; weights d = fp16_rne(amax/127) and
+ *   q = clamp(round_half_away(v / float(d)), -127, 127); activations d = amax/127
+ *   in fp32 and q = clamp(round_half_away(v / d), -127, 127); amax = 0 gives
+ *   d = 0 and q = 0.  Division is IEEE fp32 division.
+ *   Product:       s_b = sum_{i<32} wq*xq (exact int32, |s_b| <= 516128) and
+ *                  y[m][n] = sum_b (float(wd[n][b]) * xd[m][b]) * float(s_b) in fp32.
+ *                  The int32 block sums are exact; the fp32 sum order is fixed by
+ *                  the kernel (deterministic, no atomics) and a row's result does
+ *                  not depend on M or on the other rows in the call.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers, allocated and owned by the caller.
+ *     The library allocates nothing and keeps no state beyond a per-device cache
+ *     of the SM count and shared-memory limit.
+ *   - Work is enqueued on `stream` (0 = legacy default stream); no call
+ *     synchronises.  Kernels may be launched with programmatic dependent launch,
+ *     so a kernel may start streaming weights before the preceding kernel on the
+ *     stream has finished; it reads activations, ids and gate weights and writes
+ *     its outputs only after that kernel has completed.  Weights must therefore
+ *     not be written by the immediately preceding kernel on the same stream.
+ *   - Sizes are int64_t.  K must be a multiple of 32.  N, M, K may be 0 (an empty
+ *     product writes zeros where an output row exists, nothing otherwise).
+ *   - A violated precondition returns an error status and launches nothing.  A
+ *     launch failure returns MEMRA_ERR_CUDA; memra_last_cuda_error() gives the
+ *     cudaError_t of the calling thread's last failure.
+ *   - Alignment: wq and wq_bank 32 bytes; xq, hq (outputs of the quantisers) and
+ *     the quantiser inputs 16 bytes; wd 2 bytes; xd, y, ids, gate_w 4 bytes.
+ *   - Inputs must be finite.
+ */
+#ifndef MEMRA_H
+#define MEMRA_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum memra_status {
+  MEMRA_OK = 0,
+  MEMRA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, K % 32 != 0, bad enum */
+  MEMRA_ERR_ALIGNMENT = 2,     /* a pointer violates the alignment above */
+  MEMRA_ERR_UNSUPPORTED = 3,   /* a size beyond the documented limits (M > 8, ...) */
+  MEMRA_ERR_CUDA = 4           /* the CUDA runtime reported an error */
+} memra_status;
+
+typedef enum memra_dtype { MEMRA_BF16 = 0, MEMRA_F32 = 1 } memra_dtype;
+
+/* Limits. */
+#define MEMRA_MAX_M 8            /* activation rows per small-M call */
+#define MEMRA_MAX_TOP_K 64       /* experts per routed call */
+#define MEMRA_MAX_X_BYTES 196608 /* M*K*(1 + 4/32) bytes of q8_1 activation per call */
+
+/*
+ * Weight ingest: fp32 W [N][K] -> Q8_0 planes wq [N][K], wd [N][K/32].
+ * The pages have memra repack checkpoints into its own internal layout (agentlens
+ * summary of memra, "Design boundaries"); this is that repack for Q8_0 from fp32.
+ * w: 16-byte aligned.  Bit-exact with the block definition above.
+ */
+memra_status memra_quantize_q8_0(const float* w, int64_t N, int64_t K, int8_t* wq, uint16_t* wd,
+                                 cudaStream_t stream);
+
+/*
+ * Activation quantisation to int8 blocks with fp32 scales, the operand of the
+ * dp4a block dot (memra wiki, feature list: warp-level dp4a).
+ * x: [M][K] of `dtype` (MEMRA_BF16: uint16 bf16 bits, MEMRA_F32: float), 16-byte
+ * aligned.  Outputs xq [M][K] (16-byte aligned), xd [M][K/32].
+ * The block carries an fp32 scale and no sum term (Q8_0 weights have no offset).
+ */
+memra_status memra_quantize_q8_1(const void* x, int32_t dtype, int64_t M, int64_t K, int8_t* xq,
+                                 float* xd, cudaStream_t stream);
+
+/*
+ * Plain decode GEMV (M = 1): y[n] = sum_b d_w[n][b] d_x[b] s_b[n].
+ * memra wiki, feature list (Q8_0 split-plane dp4a matvec); memra performance,
+ * historical 27B board (Q8_0 plain decode).  y: fp32 [N].
+ */
+memra_status memra_q8_0_gemv(const int8_t* wq, const uint16_t* wd, int64_t N, int64_t K,
+                             const int8_t* xq, const float* xd, float* y, cudaStream_t stream);
+
+/*
+ * Speculative / MTP verify skinny GEMM: M in [0, 8] activation rows share one
+ * pass over the weights (memra wiki, feature list: one batched K+1 verify).
+ * xq [M][K], xd [M][K/32], y fp32 [M][N].  Row m of y equals, bit for bit, the
+ * memra_q8_0_gemv result for activation row m.
+ */
+memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t* wd, int64_t N, int64_t K,
+                                     int64_t M, const int8_t* xq, const float* xd, float* y,
+                                     cudaStream_t stream);
+
+/*
+ * Routed-expert GEMV for one token (memra wiki, feature list: MoE routed experts).
+ * Bank: wq_bank [E][N][K], wd_bank [E][N][K/32] (expert e's planes are the slices
+ * at e*N*K and e*N*(K/32)).  ids: device int32 [top_k]; gate_w: device fp32
+ * [top_k] or NULL.  x_per_expert = 0: one shared activation xq [K], xd [K/32];
+ * x_per_expert = 1: row k of xq [top_k][K], xd [top_k][K/32] feeds expert k.
+ *   gate_w == NULL: y fp32 [top_k][N], row k = W_{ids[k]} x_k.
+ *   gate_w != NULL: y fp32 [N] = sum_k gate_w[k] * (W_{ids[k]} x_k), k ascending.
+ * An id outside [0, E) is detected on the device: that expert is skipped (its
+ * ungated row is written as zeros; it adds nothing to the gated sum) and, if
+ * dev_status is not NULL, the int32 word *dev_status is OR-ed with 1.  The word is
+ * never cleared by the library.  E >= 1 and 1 <= top_k <= MEMRA_MAX_TOP_K.  With
+ * K = 0 the outputs are zero-filled and the ids are not examined.
+ */
+memra_status memra_q8_0_moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank, int64_t E,
+                                 int64_t N, int64_t K, const int32_t* ids, const float* gate_w,
+                                 int64_t top_k, const int8_t* xq, const float* xd,
+                                 int32_t x_per_expert, float* y, int32_t* dev_status,
+                                 cudaStream_t stream);
+
+/*
+ * SwiGLU between the routed gate/up and down projections, followed by q8_1
+ * quantisation (the MoE FFN's activation; the pages put the routed experts in the
+ * qwen/silu MoE class: memra performance, "Shipped on the sm_90a build").  The
+ * gate/up split below is this library's reading.  gu: fp32 [R][2F], gate in
+ * columns [0, F), up in [F, 2F); F % 32 == 0.  h = (g / (1 + exp(-g))) * u with
+ * each fp32 operation rounded once in that order and exp computed by Cody-Waite
+ * reduction (ln 2 = 0.693359375 + -2.12194440e-4, k = rint(x*log2(e)), argument
+ * clamped to [-87, 88]) and the degree-7 Taylor polynomial in Horner form; then
+ * hq [R][F], hd [R][F/32] as memra_quantize_q8_1.
+ */
+memra_status memra_swiglu_quantize_q8_1(const float* gu, int64_t R, int64_t F, int8_t* hq,
+                                        float* hd, cudaStream_t stream);
+
+/*
+ * Exact int32 block sums s[m][n][b] = sum_{i<32} wq[n][32b+i] * xq[m][32b+i],
+ * computed with the same dp4a block-dot routine as the product kernels.  For
+ * verification of the integer stage.  s: int32 [M][N][K/32], 4-byte aligned.
+ */
+memra_status memra_q8_0_block_dots(const int8_t* wq, int64_t N, int64_t K, const int8_t* xq,
+                                   int64_t M, int32_t* s, cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* memra_status_string(memra_status status);
+
+/* The cudaError_t (as int) of the calling thread's last MEMRA_ERR_CUDA, else 0. */
+int32_t memra_last_cuda_error(void);
+
+/* Library version string. */
+const char* memra_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEMRA_H */

@@ -1,0 +1,67 @@
+"""Host-side logic of bench.py: argument rules, rank aggregation over gloo (world
+size 2 on CPU), workload byte counts."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+import synth
+
+
+def test_dense_sweep_bytes_match_the_shapes():
+    per_layer = (7168 * 5120 + 5120 * 5120 + 34816 * 5120 + 5120 * 17408) * 34 // 32
+    assert synth.dense27b_bytes_per_token() == 64 * per_layer
+    assert abs(synth.dense27b_bytes_per_token() / 1e9 - 22.46) < 0.01
+
+
+def test_warmup_must_be_at_least_three():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2", "--steps", "1"])
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, values, out):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        m = bench.max_over_ranks(values[rank], world, backend_device="cpu")
+        bench.barrier(world)
+        out[rank] = m
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_size_2():
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    port = _free_port()
+    values = [1.25, 3.5]
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, values, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] == 3.5 and out[1] == 3.5
+
+
+def test_single_rank_aggregation_is_identity():
+    assert bench.max_over_ranks(2.5, 1) == 2.5
+
+
+def test_dist_info_defaults(monkeypatch):
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_info() == (1, 0, 0)

@@ -1,0 +1,320 @@
+"""GPU parity: the sm_103a library against the CPU oracle, through the C ABI.
+
+Integer stages (quantised weights and activations, block sums) must match bit for
+bit; fp32 outputs within |y - y_ref| <= 1e-4 * sum_b |d_w d_x s_b| + 1e-6.  Each
+side runs its own pipeline from the same seeded fp32/bf16 inputs: the oracle never
+sees a value the GPU produced.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from _util import Guarded, abs_terms, assert_within, bf16_bits_np, np_, wd_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mem():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_quantized_decode_quantize_gb300 as m
+    from block_quantized_decode_quantize_gb300 import build
+    build.build()
+    m.lib()
+    return m
+
+
+def gpu_weights(mem, w_cpu):
+    wq, wd = mem.memra_quantize_q8_0(w_cpu.cuda())
+    return wq, wd
+
+
+def check_weights(orc, w_cpu, wq, wd):
+    oq, od = orc.quantize_q8_0(np_(w_cpu))
+    assert np.array_equal(np_(wq), oq)
+    assert np.array_equal(wd_bits(wd), od)
+    return oq, od
+
+
+def check_acts(orc, x_cpu, xq, xd):
+    if x_cpu.dtype == torch.bfloat16:
+        oq, od = orc.quantize_q8_1(bf16_bits_np(x_cpu))
+    else:
+        oq, od = orc.quantize_q8_1(np_(x_cpu))
+    assert np.array_equal(np_(xq), oq)
+    assert np.array_equal(np_(xd).view(np.uint32), od.view(np.uint32))
+    return oq, od
+
+
+# ----------------------------------------------------------------------------
+# Quantisers and block sums: bit-exact.
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K,seed", [(37, 96, 1), (4096, 4096, 0), (3, 17408, 2)])
+def test_quantize_q8_0_bit_exact(mem, orc, N, K, seed):
+    w = synth.weights_fp32(N, K, seed, 0)
+    wq, wd = gpu_weights(mem, w)
+    check_weights(orc, w, wq, wd)
+
+
+def test_quantize_q8_0_special_blocks(mem, orc):
+    w = synth.weights_fp32(64, 512, 7, 1)
+    synth.perturb_blocks(w, 7, 2, zero_frac=0.05, scale_frac=0.05, scale=50.0)
+    w[3, :32] = torch.tensor(1.4 * 2 ** -24 * 127)       # subnormal fp16 scale, clamped quants
+    w[3, 1] = -w[3, 0] / 2
+    w[4, :32] = 0.0
+    w[5, 32:64] = torch.linspace(-127.0, 127.0, 32)       # d = 1 exactly, ties at .5 steps
+    w[6, 64:96] = 300.0 * torch.randn(32)                # scale far above the others
+    wq, wd = gpu_weights(mem, w)
+    check_weights(orc, w, wq, wd)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 96), (8, 17408), (5, 5120)])
+def test_quantize_q8_1_bit_exact(mem, orc, dtype, M, K):
+    x = synth.activations_fp32(M, K, 11, M, K, outlier_frac=0.001).to(dtype)
+    if K >= 64:
+        x[0, 32:64] = 0.0                                # all-zero block
+        x[0, :32] = torch.tensor([127.0, 63.5, -63.5, 2.5, -2.5, 0.5, -0.5, 1.5] * 4)
+    xq, xd = mem.memra_quantize_q8_1(x.cuda())
+    check_acts(orc, x, xq, xd)
+
+
+def test_block_dots_bit_exact(mem, orc):
+    g = torch.Generator().manual_seed(5)
+    N, K, M = 50, 1184, 3
+    wq = torch.randint(-127, 128, (N, K), generator=g, dtype=torch.int8)
+    xq = torch.randint(-127, 128, (M, K), generator=g, dtype=torch.int8)
+    wq[0, :32] = -127
+    xq[0, :32] = -127
+    s = mem.memra_q8_0_block_dots(wq.cuda(), xq.cuda())
+    ref = orc.block_dots(np_(wq), np_(xq))
+    assert np.array_equal(np_(s), ref)
+    assert int(ref[0, 0, 0]) == 32 * 127 * 127
+
+
+# ----------------------------------------------------------------------------
+# GEMV and the verify skinny GEMM.
+# ----------------------------------------------------------------------------
+
+def run_pair(mem, orc, N, K, M, seed, x_dtype=torch.bfloat16, outliers=0.001):
+    w = synth.weights_fp32(N, K, seed, 100)
+    x = synth.activations_fp32(M, K, seed, 200, outlier_frac=outliers).to(x_dtype)
+    wq, wd = gpu_weights(mem, w)
+    xq, xd = mem.memra_quantize_q8_1(x.cuda())
+    oq, od = check_weights(orc, w, wq, wd)
+    oxq, oxd = check_acts(orc, x, xq, xd)
+    return (wq, wd, xq, xd), (oq, od, oxq, oxd)
+
+
+@pytest.mark.parametrize("N,K", [(1003, 1184), (257, 17408), (4096, 4096), (64, 32),
+                                 (130, 768), (1, 5120)])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_gemm_parity(mem, orc, N, K, M):
+    (wq, wd, xq, xd), (oq, od, oxq, oxd) = run_pair(mem, orc, N, K, M, seed=N * 31 + K + M)
+    y = Guarded((M, N), torch.float32)
+    if M == 1:
+        mem.memra_q8_0_gemv(wq, wd, xq[0], xd[0], y=y.view[0])
+    else:
+        mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd, y=y.view)
+    torch.cuda.synchronize()
+    assert y.intact()
+    y_ref = orc.gemm(oq, od, oxq, oxd)
+    terms = abs_terms(orc.block_dots(oq, oxq), od, oxd)
+    assert_within(np_(y.view), y_ref, terms, "gemm N=%d K=%d M=%d" % (N, K, M))
+
+
+def test_rows_do_not_depend_on_m(mem, orc):
+    N, K = 777, 5120
+    (wq, wd, xq, xd), _ = run_pair(mem, orc, N, K, 8, seed=9)
+    y8 = mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd)
+    for m in range(8):
+        y1 = mem.memra_q8_0_gemv(wq, wd, xq[m], xd[m])
+        assert torch.equal(y1.view(torch.int32), y8[m].view(torch.int32)), m
+    for M in (2, 3, 5):
+        yM = mem.memra_q8_0_gemm_small_m(wq, wd, xq[:M].contiguous(), xd[:M].contiguous())
+        assert torch.equal(yM.view(torch.int32), y8[:M].view(torch.int32)), M
+
+
+def test_deterministic_repeat(mem, orc):
+    (wq, wd, xq, xd), _ = run_pair(mem, orc, 2048, 5120, 4, seed=3)
+    a = mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd)
+    b = mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_zero_and_scaled_blocks(mem, orc):
+    N, K = 300, 2048
+    w = synth.weights_fp32(N, K, 4, 4)
+    synth.perturb_blocks(w, 4, 5, zero_frac=0.01, scale_frac=0.01, scale=50.0)
+    w[17] = 0.0
+    x = synth.activations_bf16(8, K, 4, 6)
+    wq, wd = gpu_weights(mem, w)
+    xq, xd = mem.memra_quantize_q8_1(x.cuda())
+    oq, od = check_weights(orc, w, wq, wd)
+    oxq, oxd = check_acts(orc, x, xq, xd)
+    y = mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd)
+    y_ref = orc.gemm(oq, od, oxq, oxd)
+    assert_within(np_(y), y_ref, abs_terms(orc.block_dots(oq, oxq), od, oxd), "perturbed")
+    assert torch.all(y[:, 17] == 0)
+
+
+# ----------------------------------------------------------------------------
+# Routed experts.
+# ----------------------------------------------------------------------------
+
+def make_bank(mem, E, N, K, seed):
+    w = torch.stack([synth.weights_fp32(N, K, seed, 300, e) for e in range(E)])
+    wq, wd = mem.memra_quantize_q8_0(w.view(E * N, K).cuda())
+    return w, wq.view(E, N, K), wd.view(E, N, K // 32)
+
+
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("per_expert", [False, True])
+def test_moe_gemv_parity(mem, orc, gated, per_expert):
+    E, N, K, top_k = 12, 200, 768, 8
+    w, wq, wd = make_bank(mem, E, N, K, 21)
+    oq, od = orc.quantize_q8_0(np_(w).reshape(E * N, K))
+    assert np.array_equal(np_(wq).reshape(E * N, K), oq)
+    oq = oq.reshape(E, N, K)
+    od = od.reshape(E, N, K // 32)
+    ids, gw = synth.routing(E, top_k, 22, int(gated), int(per_expert))
+    x = synth.activations_bf16(top_k if per_expert else 1, K, 23)
+    xq, xd = mem.memra_quantize_q8_1(x.cuda())
+    oxq, oxd = check_acts(orc, x, xq, xd)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    xq_in, xd_in = (xq, xd) if per_expert else (xq[0], xd[0])
+    y = mem.memra_q8_0_moe_gemv(wq, wd, ids.cuda(), gw.cuda() if gated else None, xq_in, xd_in,
+                                per_expert, dev_status=status)
+    y_ref, bad = orc.moe_gemv(oq, od, np_(ids), np_(gw) if gated else None,
+                              oxq if per_expert else oxq[:1], oxd if per_expert else oxd[:1],
+                              int(per_expert))
+    assert bad == 0 and int(status.item()) == 0
+    terms = np.zeros((top_k, N))
+    for k, e in enumerate(np_(ids)):
+        xr = k if per_expert else 0
+        terms[k] = abs_terms(orc.block_dots(oq[e], oxq[xr:xr + 1]), od[e], oxd[xr:xr + 1])[0]
+    if gated:
+        terms = (np.abs(np_(gw))[:, None] * terms).sum(axis=0)
+    assert_within(np_(y), y_ref, terms, "moe gated=%s per_expert=%s" % (gated, per_expert))
+
+
+def test_moe_bad_ids_flagged_and_skipped(mem, orc):
+    E, N, K = 4, 64, 256
+    w, wq, wd = make_bank(mem, E, N, K, 31)
+    oq, od = orc.quantize_q8_0(np_(w).reshape(E * N, K))
+    oq = oq.reshape(E, N, K)
+    od = od.reshape(E, N, K // 32)
+    x = synth.activations_bf16(1, K, 32)
+    xq, xd = mem.memra_quantize_q8_1(x.cuda())
+    oxq, oxd = check_acts(orc, x, xq, xd)
+    ids = torch.tensor([2, 7, -3], dtype=torch.int32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = mem.memra_q8_0_moe_gemv(wq, wd, ids.cuda(), None, xq[0], xd[0], False, dev_status=status)
+    assert int(status.item()) == 1
+    assert torch.all(y[1] == 0) and torch.all(y[2] == 0)
+    y_ref, bad = orc.moe_gemv(oq, od, np_(ids), None, oxq, oxd, 0)
+    assert bad == 2
+    terms = abs_terms(orc.block_dots(oq[2], oxq), od[2], oxd)[0]
+    assert_within(np_(y[0]), y_ref[0], terms, "moe bad ids")
+    status.zero_()
+    gw = torch.tensor([0.5, 0.25, 0.25], dtype=torch.float32)
+    yg = mem.memra_q8_0_moe_gemv(wq, wd, ids.cuda(), gw.cuda(), xq[0], xd[0], False,
+                                 dev_status=status)
+    assert int(status.item()) == 1
+    yg_ref, _ = orc.moe_gemv(oq, od, np_(ids), np_(gw), oxq, oxd, 0)
+    assert_within(np_(yg), yg_ref, 0.5 * terms, "moe bad ids gated")
+
+
+@pytest.mark.parametrize("R,F", [(8, 768), (1, 32), (3, 2048)])
+def test_swiglu_quantize_bit_exact(mem, orc, R, F):
+    gu = synth.normal((R, 2 * F), 41, R, F, std=3.0)
+    gu[0, :6] = torch.tensor([0.0, -30.0, 30.0, -95.0, 95.0, 1e-3])
+    hq, hd = mem.memra_swiglu_quantize_q8_1(gu.cuda())
+    oq, od = orc.swiglu_quantize_q8_1(np_(gu))
+    assert np.array_equal(np_(hq), oq)
+    assert np.array_equal(np_(hd).view(np.uint32), od.view(np.uint32))
+
+
+def test_moe_ffn_layer_composition(mem, orc):
+    """One routed FFN layer: quantise x, gate/up experts, SwiGLU + quantise, down experts
+    with gate weights.  The GPU's fp32 gate/up outputs differ from the oracle's in the
+    last bits, so h may quantise one step differently; the bound allows one h quantum
+    per element on top of the stated product tolerance."""
+    E, H, F, top_k = 16, 2048, 768, 8
+    wgu, gq, gd = make_bank(mem, E, 2 * F, H, 51)
+    wdn, dq, dd = make_bank(mem, E, H, F, 52)
+    ogq, ogd = orc.quantize_q8_0(np_(wgu).reshape(-1, H))
+    odq, odd = orc.quantize_q8_0(np_(wdn).reshape(-1, F))
+    ogq, ogd = ogq.reshape(E, 2 * F, H), ogd.reshape(E, 2 * F, H // 32)
+    odq, odd = odq.reshape(E, H, F), odd.reshape(E, H, F // 32)
+    ids, gw = synth.routing(E, top_k, 53)
+    x = synth.normal((H,), 54)
+    xq, xd = mem.memra_quantize_q8_1(x.cuda()[None])
+    ygu = mem.memra_q8_0_moe_gemv(gq, gd, ids.cuda(), None, xq[0], xd[0], False)
+    hq, hd = mem.memra_swiglu_quantize_q8_1(ygu)
+    y = mem.memra_q8_0_moe_gemv(dq, dd, ids.cuda(), gw.cuda(), hq, hd, True)
+    y_ref, bad = orc.moe_ffn(np_(x), ogq, ogd, odq, odd, np_(ids), np_(gw))
+    assert bad == 0
+    # one quantum of h per element: sum_k w_k sum_f |W_dn[n, f]| * hd_k[f/32]
+    _, ohd = orc.swiglu_quantize_q8_1(orc.moe_gemv(ogq, ogd, np_(ids), None,
+                                                   *orc.quantize_q8_1(np_(x)[None]), 0)[0])
+    bound = np.zeros(H)
+    for k, e in enumerate(np_(ids)):
+        wabs = np.abs(odq[e].astype(np.float64) *
+                      np.repeat(odd[e].view(np.float16).astype(np.float64), 32, axis=1))
+        bound += gw[k].item() * (wabs @ np.repeat(2.0 * ohd[k].astype(np.float64), 32))
+    err = np.abs(np_(y).astype(np.float64) - y_ref)
+    assert np.all(err <= bound + 1e-4 * np.abs(y_ref).max() + 1e-6)
+
+
+# ----------------------------------------------------------------------------
+# Edge cases and errors.
+# ----------------------------------------------------------------------------
+
+def test_empty_and_degenerate_sizes(mem, orc):
+    dev = "cuda"
+    wq = torch.zeros((5, 0), dtype=torch.int8, device=dev)
+    wd = torch.zeros((5, 0), dtype=torch.float16, device=dev)
+    xq = torch.zeros((2, 0), dtype=torch.int8, device=dev)
+    xd = torch.zeros((2, 0), dtype=torch.float32, device=dev)
+    y = torch.full((2, 5), 7.0, device=dev)
+    mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd, y=y)       # K = 0: empty sums
+    assert torch.all(y == 0)
+    y0 = mem.memra_q8_0_gemm_small_m(torch.zeros((0, 64), dtype=torch.int8, device=dev),
+                                     torch.zeros((0, 2), dtype=torch.float16, device=dev),
+                                     torch.zeros((3, 64), dtype=torch.int8, device=dev),
+                                     torch.zeros((3, 2), dtype=torch.float32, device=dev))
+    assert y0.shape == (3, 0)
+    # N = 1, K = 32: one block
+    (wq, wd, xq, xd), (oq, od, oxq, oxd) = run_pair(mem, orc, 1, 32, 1, seed=61)
+    y = mem.memra_q8_0_gemv(wq, wd, xq[0], xd[0])
+    assert_within(np_(y)[None], orc.gemm(oq, od, oxq, oxd),
+                  abs_terms(orc.block_dots(oq, oxq), od, oxd), "1x32")
+    # all-zero activation: every output exactly zero
+    z = torch.zeros((1, 4096), dtype=torch.bfloat16, device=dev)
+    zq, zd = mem.memra_quantize_q8_1(z)
+    assert torch.all(zd == 0) and torch.all(zq == 0)
+
+
+def test_misaligned_views_are_rejected(mem):
+    dev = "cuda"
+    N, K = 64, 256
+    base = torch.zeros(N * K + 16, dtype=torch.int8, device=dev)
+    wq_bad = base[16:16 + N * K].view(N, K)             # 16-byte aligned, not 32
+    wd = torch.zeros((N, K // 32), dtype=torch.float16, device=dev)
+    xq = torch.zeros((1, K), dtype=torch.int8, device=dev)
+    xd = torch.zeros((1, K // 32), dtype=torch.float32, device=dev)
+    y = torch.full((1, N), 3.0, device=dev)
+    with pytest.raises(mem.MemraError) as ei:
+        mem.memra_q8_0_gemm_small_m(wq_bad, wd, xq, xd, y=y)
+    assert ei.value.status == 2
+    torch.cuda.synchronize()
+    assert torch.all(y == 3.0)                          # nothing launched
+    with pytest.raises(mem.MemraError) as ei:
+        mem.memra_q8_0_gemm_small_m(torch.zeros((N, K), dtype=torch.int8, device=dev), wd,
+                                    torch.zeros((9, K), dtype=torch.int8, device=dev),
+                                    torch.zeros((9, K // 32), dtype=torch.float32, device=dev))
+    assert ei.value.status == 3
