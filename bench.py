@@ -151,23 +151,24 @@ def run_gemv_op(mem, op, quantize=True):
 class Workload:
     """A step = a fixed list of library calls; captured once into a CUDA graph."""
 
-    def __init__(self, name, mem, device):
+    def __init__(self, name, mem, device, layers=None):
         self.name = name
         self.mem = mem
         self.device = device
         self.moe = None
         self.ops = []
         if name == "dense27b_sweep":
-            self.ops = build_dense_sweep(mem, device, M=1)
+            self.ops = build_dense_sweep(mem, device, M=1, layers=layers)
         elif name.startswith("verify_m"):
             self.ops = build_dense_sweep(mem, device, M=int(name[len("verify_m"):]),
-                                         workload_id=2)
+                                         layers=layers, workload_id=2)
         elif name == "gemv_4096":
             self.ops = build_gemv_4096(mem, device)
         elif name == "stress_lm_head":
             self.ops = build_stress(mem, device, M=1) + build_stress(mem, device, M=8)
         elif name == "moe_top8":
-            self.moe = [MoeLayer(mem, layer, device) for layer in range(synth.MOE["layers"])]
+            n = synth.MOE["layers"] if layers is None else layers
+            self.moe = [MoeLayer(mem, layer, device) for layer in range(n)]
         else:
             raise ValueError(name)
         torch.cuda.synchronize(device)
@@ -428,7 +429,7 @@ class CpuOracleSample:
 def workload_config(name, wl):
     cfg = {"workload": name}
     if name == "dense27b_sweep" or name.startswith("verify_m"):
-        cfg.update({"layers": synth.DENSE27B["layers"], "hidden": synth.DENSE27B["hidden"],
+        cfg.update({"layers": len(wl.ops) // 4, "hidden": synth.DENSE27B["hidden"],
                     "gemvs_per_layer": [[n, N, K] for n, N, K in synth.DENSE27B["gemvs"]],
                     "M": 1 if name == "dense27b_sweep" else int(name[len("verify_m"):]),
                     "activations": "bf16 N(0,1), 0.1% of entries x20"})
@@ -460,7 +461,7 @@ def run_memra(args):
     barrier(world)
     mem.lib()
 
-    wl = Workload(args.workload, mem, device)
+    wl = Workload(args.workload, mem, device, layers=args.layers)
     stream = torch.cuda.Stream(device)
     step_graph = wl.capture(wl.step)
     gemv_graph = wl.capture(wl.gemv_only)
@@ -613,6 +614,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=WORKLOADS, default="dense27b_sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="fewer layers than the workload's own (profiling captures only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

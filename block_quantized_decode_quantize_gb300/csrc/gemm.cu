@@ -1,79 +1,66 @@
 // Q8_0 x q8_1 products: the M = 1 decode GEMV, the M <= 8 verify skinny GEMM and
-// the routed-expert (MoE) GEMV, all from one weight-streaming kernel template.
+// the routed-expert (MoE) GEMV.
 //
-// Work decomposition.  A "virtual row" is one weight row paired with the
-// activation row(s) it multiplies: row n of W for the dense product, (expert k,
-// row n) for the routed product.  Each CTA owns a contiguous range of virtual rows
-// (balanced to within one row, or one group of top_k rows for the gated MoE), and
-// splits it into chunks of R rows x 32 blocks: lane l of the warp that takes a
-// chunk streams block 32p + l of each of the R rows (one 32-byte load per row),
-// so a chunk is R contiguous 1-KB runs of the weight plane.  Chunks are dealt
-// round-robin to the CTA's warps and each warp keeps U chunks of loads in flight
-// in a register ring, so a CTA's share of HBM bandwidth does not depend on how
-// its rows divide among warps.
+// Arithmetic (one definition for every kernel below, so that a row's result is
+// the same bit for bit whichever kernel, M, grid or batch produced it):
+//   nb = K/32 blocks, cpr = ceil(nb/32) parts of 32 blocks, S = ceil(cpr/4)
+//   slices; slice s covers parts [s*cpr/S, (s+1)*cpr/S).
+//   Within a slice, lane l owns blocks b = 32p + l and accumulates, in ascending
+//   p:  acc = fma(fl(float(d_w[b]) * d_x[b]), float(s_b), acc), from acc = 0,
+//   where s_b is the exact int32 block dot (8 dp4a).
+//   part[s] = xor-butterfly sum over the 32 lanes (masks 16, 8, 4, 2, 1).
+//   y = part[0] + part[1] + ... + part[S-1], sequentially.
 //
-// Arithmetic (fixed order, deterministic):
-//   term  = (float(d_w) * d_x) * float(s_b)   s_b from 8 dp4a, exact int32
-//   part  = xor-butterfly sum of the 32 lanes' terms (masks 16, 8, 4, 2, 1)
-//   y     = sum over the parts of the row, sequential in part index.
-// A row's value depends only on K, never on M, R, U, the grid or the other rows,
-// so the M-row verify result equals the M = 1 GEMV bit for bit.
+// Two kernels implement it.
 //
-// Activations are staged once per CTA in shared memory in a half-block-split
-// layout (xs[row][half][block] of 16 bytes) so that lane-consecutive blocks read
-// consecutive 16-byte words without bank conflicts.  The weights never touch
-// shared memory.  With programmatic dependent launch the weight loads of the
-// first U chunks are issued before the wait on the preceding kernel.
+// q8_tma_kernel (the GB300 path; K % 256 == 0 and 16-byte aligned planes): one
+//   CTA per SM owns a contiguous range of weight rows (or, for the routed product,
+//   a few contiguous row ranges, one per selected expert).  Warp 0 is the
+//   producer: one lane streams whole rows of the quant and scale planes into a ring
+//   of shared-memory stages with cp.async.bulk, completing on per-stage mbarriers,
+//   and the warp reduces each finished stage's slice partials into y.  Warps 1..8
+//   consume stages: each task is (R rows, one slice), read from shared memory with
+//   128-bit loads whose half-block order alternates between lane quads so that no
+//   two lanes of a phase hit the same banks.  The HBM stream is set by the ring
+//   (tens of KB in flight per SM), not by how tasks divide among warps.  With
+//   programmatic dependent launch the producer fills the ring before waiting for the
+//   preceding kernel; the CTA is sized so that the next kernel's CTA fits beside it
+//   on the SM and starts its own stream while this one drains.
+//
+// q8_reg_kernel (everything else): the same tasks with weights loaded straight
+//   into registers (256-bit loads, a slice's blocks issued together), activations
+//   staged in shared memory.
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 
 namespace memra {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kPartFloats = 8192;  // 32 KB of per-part partial sums per tile
+#ifndef MEMRA_SLICE_PARTS
+#define MEMRA_SLICE_PARTS 4
+#endif
+constexpr int kSlicePartsMax = MEMRA_SLICE_PARTS;
 constexpr int kMaxTopK = MEMRA_MAX_TOP_K;
 
 enum Mode { kDense = 0, kMoeUngated = 1, kMoeGated = 2 };
 
-struct Params {
-  const int8_t* wq;       // dense weights or the expert bank
-  const uint16_t* wd;
-  int64_t N;              // rows of one weight matrix
-  int64_t K;
-  int nb;                 // blocks per row (K / 32)
-  int cpr;                // parts (32-block runs) per row
-  const int8_t* xq;
-  const float* xd;
-  int xrows;              // activation rows staged in shared memory
-  float* y;
-  int64_t vrows;          // virtual rows
-  int unit;               // CTA ranges are multiples of this many virtual rows
-  int tile_rows;          // virtual rows per partial-sum tile (multiple of unit and R)
-  // routed experts
-  const int32_t* ids;
-  const float* gate_w;
-  int top_k;
-  int64_t E;
-  int x_per_expert;
-  int32_t* status;
-};
-
-template <int R>
-struct ChunkRegs {
-  Quants32 w[R];
-  uint16_t d[R];
-};
-
 __host__ __device__ constexpr int next_pow2(int v) { return v <= 1 ? 1 : 2 * next_pow2((v + 1) / 2); }
 __host__ __device__ constexpr int log2i(int v) { return v <= 1 ? 0 : 1 + log2i(v / 2); }
 
+__host__ __device__ inline int slices_for(int cpr) {
+  return (cpr + kSlicePartsMax - 1) / kSlicePartsMax;
+}
+__host__ __device__ inline int slice_begin(int s, int cpr, int S) {
+  return (int)(((long long)s * cpr) / S);
+}
+
 // Sum V = 2^t values across the warp with the xor-butterfly tree (masks 16, 8, 4,
 // 2, 1), exchanging half of the remaining values at each of the first t stages.
-// Every value goes through the same tree of pairwise sums as a plain butterfly.
-// Afterwards lane l holds the total of value (l >> (5 - t)).
+// Every value goes through the same tree of pairwise sums as a plain butterfly
+// (fp32 addition is commutative).  Afterwards lane l holds value (l >> (5 - t)).
 template <int V>
 __device__ __forceinline__ void warp_sum_transposed(float (&v)[V], int lane) {
   constexpr int t = log2i(V);
@@ -86,204 +73,539 @@ __device__ __forceinline__ void warp_sum_transposed(float (&v)[V], int lane) {
     for (int i = 0; i < half; ++i) {
       const float send = upper ? v[i] : v[i + half];
       const float keep = upper ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(kFullMask, send, mask);
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(kFullMask, send, mask));
     }
   }
 #pragma unroll
-  for (int s = t; s < 5; ++s) v[0] += __shfl_xor_sync(kFullMask, v[0], 16 >> s);
+  for (int s = t; s < 5; ++s) v[0] = __fadd_rn(v[0], __shfl_xor_sync(kFullMask, v[0], 16 >> s));
 }
 
-template <int M, int R, int U, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) q8_gemm_kernel(const Params p) {
-  extern __shared__ __align__(16) unsigned char smem[];
+// Reduce acc[R][M] of every lane and store the slice partials:
+// part[(row * S + s) * M + m] for rows < nrows.
+template <int R, int M>
+__device__ __forceinline__ void store_partials(float (&acc)[R][M], int lane, float* part,
+                                               int row0, int nrows, int s, int S) {
   constexpr int V = next_pow2(R * M);
+  float v[V];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int m = 0; m < M; ++m) v[r * M + m] = acc[r][m];
+#pragma unroll
+  for (int i = R * M; i < V; ++i) v[i] = 0.0f;
+  warp_sum_transposed<V>(v, lane);
+  constexpr int t = log2i(V);
+  if ((lane & ((32 >> t) - 1)) == 0) {
+    const int idx = lane >> (5 - t);
+    if (idx < R * M) {
+      const int r = idx / M;
+      const int m = idx - r * M;
+      if (r < nrows) part[((size_t)(row0 + r) * S + s) * M + m] = v[0];
+    }
+  }
+}
+
+// One block of one weight row against an x block: the exact int32 sum from two
+// 16-byte halves (in either order: integer addition is exact).
+__device__ __forceinline__ int dot_halves(const uint4& w0, const uint4& w1, const uint4& x0,
+                                          const uint4& x1) {
+  int s = 0;
+  s = __dp4a((int)w0.x, (int)x0.x, s);
+  s = __dp4a((int)w0.y, (int)x0.y, s);
+  s = __dp4a((int)w0.z, (int)x0.z, s);
+  s = __dp4a((int)w0.w, (int)x0.w, s);
+  s = __dp4a((int)w1.x, (int)x1.x, s);
+  s = __dp4a((int)w1.y, (int)x1.y, s);
+  s = __dp4a((int)w1.z, (int)x1.z, s);
+  s = __dp4a((int)w1.w, (int)x1.w, s);
+  return s;
+}
+
+__device__ __forceinline__ float block_term_acc(float acc, uint16_t dw_bits, float dx, int s) {
+  const float c = __fmul_rn(__half2float(__ushort_as_half(dw_bits)), dx);
+  return __fmaf_rn(c, (float)s, acc);
+}
+
+// ----------------------------------------------------------------------------
+// Work description shared by both kernels: a CTA's rows come as segments, each a
+// contiguous run of weight rows multiplied by one activation row set.
+// ----------------------------------------------------------------------------
+struct Params {
+  const int8_t* wq;        // dense weights or the expert bank
+  const uint16_t* wd;
+  int64_t N;               // rows of one weight matrix
+  int64_t K;
+  int nb, cpr, S;
+  const int8_t* xq;
+  const float* xd;
+  int xrows;               // activation rows held in shared memory
+  float* y;
+  int64_t units;           // dense/gated: N; ungated: top_k * N
+  // routed experts
+  const int32_t* ids;
+  const float* gate_w;
+  int top_k;
+  int64_t E;
+  int xpe;                 // one activation row per expert
+  int32_t* status;
+  // TMA kernel layout
+  int rps;                 // rows per stage
+  int ns;                  // stages in the ring
+  uint32_t stage_bytes;    // bytes per stage (quants, then scales at wd_off)
+  uint32_t wd_off;
+  uint32_t off_x, off_xd, off_ring, off_part, off_yacc;
+  // register kernel layout
+  int tile_rows;
+};
+
+struct Seg {
+  int64_t row0;   // first weight row (absolute row index into the plane)
+  int nrows;
+  int xrow;       // first activation row used
+  int k;          // routed slot (0 for dense)
+  int64_t out0;   // first output row (dense/ungated)
+  bool valid;
+};
+
+template <int MODE>
+__device__ __forceinline__ int num_segs(const Params& p, int64_t u0, int64_t u1) {
+  if (MODE == kDense) return 1;
+  if (MODE == kMoeGated) return p.top_k;
+  return (int)((u1 - 1) / p.N - u0 / p.N + 1);
+}
+
+template <int MODE>
+__device__ __forceinline__ Seg get_seg(const Params& p, int64_t u0, int64_t u1, int si,
+                                       const int32_t* s_ids) {
+  Seg g;
+  if (MODE == kDense) {
+    g.row0 = u0;
+    g.nrows = (int)(u1 - u0);
+    g.xrow = 0;
+    g.k = 0;
+    g.out0 = u0;
+    g.valid = true;
+  } else if (MODE == kMoeGated) {
+    const int e = s_ids[si];
+    g.k = si;
+    g.valid = e >= 0;
+    g.row0 = (int64_t)(e < 0 ? 0 : e) * p.N + u0;
+    g.nrows = (int)(u1 - u0);
+    g.xrow = p.xpe ? si : 0;
+    g.out0 = u0;
+  } else {
+    const int64_t k = u0 / p.N + si;
+    const int64_t lo = (u0 > k * p.N ? u0 : k * p.N) - k * p.N;
+    const int64_t hi = (u1 < (k + 1) * p.N ? u1 : (k + 1) * p.N) - k * p.N;
+    const int e = s_ids[k];
+    g.k = (int)k;
+    g.valid = e >= 0;
+    g.row0 = (int64_t)(e < 0 ? 0 : e) * p.N + lo;
+    g.nrows = (int)(hi - lo);
+    g.xrow = p.xpe ? (int)k : 0;
+    g.out0 = k * p.N + lo;
+  }
+  return g;
+}
+
+// Load ids (validated) and gate weights into shared memory; flag bad ids.
+template <int MODE>
+__device__ __forceinline__ void load_routing(const Params& p, int32_t* s_ids, float* s_gate,
+                                             int tid, int nthreads) {
+  for (int k = tid; k < p.top_k; k += nthreads) {
+    const int32_t e = p.ids[k];
+    const bool ok = e >= 0 && e < p.E;
+    s_ids[k] = ok ? e : -1;
+    s_gate[k] = (MODE == kMoeGated) ? p.gate_w[k] : 1.0f;
+    if (!ok && p.status && blockIdx.x == 0) atomicOr(p.status, 1);
+  }
+}
+
+// ============================================================================
+// TMA producer/consumer kernel.
+// ============================================================================
+constexpr int kConsumerWarps = 8;
+constexpr int kTmaThreads = 32 * (1 + kConsumerWarps);
+constexpr int kMaxStages = 8;
+constexpr int kHeaderBytes = 1024;  // barriers, abort flag, stage metadata, ids, gates
+
+struct StageMeta {
+  int seg;
+  int r0;
+  int nr;
+  int pad;
+};
+
+template <int M, int R, int MODE>
+__global__ void __launch_bounds__(kTmaThreads, 2) q8_tma_kernel(const Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[8] | empty[8] | xfull
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 8 * (2 * kMaxStages + 1));
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + 160);
+  int32_t* s_ids = reinterpret_cast<int32_t*>(smem + 160 + 16 * kMaxStages);
+  float* s_gate = reinterpret_cast<float*>(s_ids + kMaxTopK);
+  const int8_t* xs = reinterpret_cast<const int8_t*>(smem + p.off_x);
+  const float* xds = reinterpret_cast<const float*>(smem + p.off_xd);
+  unsigned char* ring = smem + p.off_ring;
+  float* part = reinterpret_cast<float*>(smem + p.off_part);
+  float* yacc = reinterpret_cast<float*>(smem + p.off_yacc);
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nb = p.nb;
-  const int cpr = p.cpr;
+  const int S = p.S;
+  const int ns = p.ns;
+  const int64_t u0 = p.units * blockIdx.x / gridDim.x;
+  const int64_t u1 = p.units * (blockIdx.x + 1) / gridDim.x;
+  auto full_bar = [&](int i) { return smem_addr(bars + i); };
+  auto empty_bar = [&](int i) { return smem_addr(bars + kMaxStages + i); };
+  const uint32_t xfull_bar = smem_addr(bars + 2 * kMaxStages);
 
-  // Shared memory: xs | xds | partial sums | expert ids | gate weights.
-  uint4* xs = reinterpret_cast<uint4*>(smem);
-  float* xds = reinterpret_cast<float*>(smem + (size_t)p.xrows * p.K);
-  float* part = xds + (((size_t)p.xrows * nb + 3) & ~(size_t)3);
-  int32_t* s_ids = reinterpret_cast<int32_t*>(part + (size_t)p.tile_rows * cpr * M);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < ns; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), kConsumerWarps);
+    }
+    mbar_init(xfull_bar, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  pdl_launch_dependents();
+  if (MODE != kDense && warp == 0) {
+    pdl_wait();  // ids and gate weights may come from the preceding kernel
+    load_routing<MODE>(p, s_ids, s_gate, lane, 32);
+  }
+  if (MODE == kMoeGated) {
+    for (int64_t i = threadIdx.x; i < u1 - u0; i += kTmaThreads) yacc[i] = 0.0f;
+  }
+  __syncthreads();
+
+  const int nseg = num_segs<MODE>(p, u0, u1);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t policy = l2_evict_first_policy();
+    uint32_t issued = 0;
+    bool x_issued = false;
+    bool ok = true;
+
+    auto issue_x = [&]() {
+      if (MODE == kDense) pdl_wait();  // activations come from the preceding kernel
+      if (lane == 0) {
+        const uint32_t xb = (uint32_t)(p.xrows * p.K);
+        const uint32_t db = (uint32_t)(p.xrows * nb * 4);
+        mbar_arrive_expect_tx(xfull_bar, xb + db);
+        bulk_g2s(smem_addr(xs), p.xq, xb, xfull_bar);
+        bulk_g2s(smem_addr(xds), p.xd, db, xfull_bar);
+      }
+      __syncwarp();
+      x_issued = true;
+    };
+
+    // Reduce the slice partials of the stage in `slot` into the outputs.
+    auto epilogue = [&](int slot) {
+      const StageMeta mt = meta[slot];
+      const Seg g = get_seg<MODE>(p, u0, u1, mt.seg, s_ids);
+      const float* pp = part + (size_t)slot * p.rps * S * M;
+      for (int i = lane; i < mt.nr * M; i += 32) {
+        const int r = i / M;
+        const int m = i - r * M;
+        float tot = pp[((size_t)r * S) * M + m];
+        for (int s = 1; s < S; ++s) tot = __fadd_rn(tot, pp[((size_t)r * S + s) * M + m]);
+        if (MODE == kMoeGated) {
+          const int n = mt.r0 + r;
+          yacc[n] = __fadd_rn(yacc[n], __fmul_rn(s_gate[g.k], tot));
+        } else {
+          p.y[(int64_t)m * p.units + g.out0 + mt.r0 + r] = tot;
+        }
+      }
+      __syncwarp();
+    };
+
+    for (int si = 0; si < nseg && ok; ++si) {
+      const Seg g = get_seg<MODE>(p, u0, u1, si, s_ids);
+      if (!g.valid) {
+        if (MODE == kMoeUngated)
+          for (int i = lane; i < g.nrows; i += 32) p.y[g.out0 + i] = 0.0f;
+        continue;
+      }
+      for (int r0 = 0; r0 < g.nrows; r0 += p.rps) {
+        const int nr = min(p.rps, g.nrows - r0);
+        const int slot = issued % ns;
+        if (issued >= (uint32_t)ns) {
+          if (!mbar_wait(empty_bar(slot), ((issued / ns) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          epilogue(slot);
+        }
+        if (lane == 0) {
+          meta[slot] = StageMeta{si, r0, nr, 0};
+          const uint32_t qb = (uint32_t)(nr * p.K);
+          const uint32_t db = (uint32_t)(nr * nb * 2);
+          const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
+          mbar_arrive_expect_tx(full_bar(slot), qb + db);
+          bulk_g2s_hint(dst, p.wq + (g.row0 + r0) * p.K, qb, full_bar(slot), policy);
+          bulk_g2s_hint(dst + p.wd_off, p.wd + (g.row0 + r0) * nb, db, full_bar(slot), policy);
+        }
+        __syncwarp();
+        ++issued;
+        if (issued == (uint32_t)ns && !x_issued) issue_x();
+      }
+    }
+    if (!x_issued) issue_x();
+    // Drain: the last stages' partials.
+    const uint32_t first = issued > (uint32_t)ns ? issued - ns : 0;
+    for (uint32_t j = first; j < issued && ok; ++j) {
+      const int slot = j % ns;
+      if (!mbar_wait(empty_bar(slot), (j / ns) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      epilogue(slot);
+    }
+    if (!ok || *abort_flag) {
+      // A wait gave up: let the copies already issued land (bounded), then mark
+      // this CTA's outputs invalid with NaN.
+      *abort_flag = 1;
+      for (uint32_t j = first; j < issued; ++j) {
+        const int slot = j % ns;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(full_bar(slot), (j / ns) & 1) && clock64() - t0 < (1ll << 30)) {
+        }
+      }
+      {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(xfull_bar, 0) && clock64() - t0 < (1ll << 30)) {
+        }
+      }
+      const float nan = __int_as_float(0x7fc00000);
+      if (MODE == kMoeGated) {
+        for (int64_t i = lane; i < u1 - u0; i += 32) p.y[u0 + i] = nan;
+      } else if (MODE == kMoeUngated) {
+        for (int64_t i = u0 + lane; i < u1; i += 32) p.y[i] = nan;
+      } else {
+        for (int m = 0; m < M; ++m)
+          for (int64_t i = u0 + lane; i < u1; i += 32) p.y[m * p.units + i] = nan;
+      }
+    } else if (MODE == kMoeGated) {
+      for (int64_t i = lane; i < u1 - u0; i += 32) p.y[u0 + i] = yacc[i];
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int cw = warp - 1;
+    const int h1 = (lane >> 2) & 1;  // which half this lane loads first
+    if (!mbar_wait(xfull_bar, 0, abort_flag)) return;
+    uint32_t it = 0;
+    for (int si = 0; si < nseg; ++si) {
+      const Seg g = get_seg<MODE>(p, u0, u1, si, s_ids);
+      if (!g.valid) continue;
+      const int xrow = (MODE == kDense) ? 0 : g.xrow;
+      for (int r0 = 0; r0 < g.nrows; r0 += p.rps) {
+        const int nr = min(p.rps, g.nrows - r0);
+        const int slot = it % ns;
+        if (!mbar_wait(full_bar(slot), (it / ns) & 1, abort_flag)) return;
+        const int8_t* ws = reinterpret_cast<const int8_t*>(ring + (size_t)slot * p.stage_bytes);
+        const uint16_t* ds =
+            reinterpret_cast<const uint16_t*>(ring + (size_t)slot * p.stage_bytes + p.wd_off);
+        float* pp = part + (size_t)slot * p.rps * S * M;
+        const int groups = (nr + R - 1) / R;
+        const int ntasks = groups * S;
+        for (int t = cw; t < ntasks; t += kConsumerWarps) {
+          const int gi = t / S;
+          const int s = t - gi * S;
+          const int rbase = gi * R;
+          const int plo = slice_begin(s, p.cpr, S);
+          const int phi = slice_begin(s + 1, p.cpr, S);
+          float acc[R][M];
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
+          for (int pt = plo; pt < phi; ++pt) {
+            const int b = pt * 32 + lane;
+            if (b < nb) {
+              uint4 w0[R], w1[R];
+              uint16_t dw[R];
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                // Rows past the stage's end reuse a valid row; their sums are dropped.
+                const int row = rbase + r < nr ? rbase + r : rbase;
+                const uint4* src = reinterpret_cast<const uint4*>(ws + (size_t)row * p.K + b * 32);
+                w0[r] = src[h1];
+                w1[r] = src[h1 ^ 1];
+                dw[r] = ds[(size_t)row * nb + b];
+              }
+#pragma unroll
+              for (int m = 0; m < M; ++m) {
+                const uint4* xsrc =
+                    reinterpret_cast<const uint4*>(xs + (size_t)(xrow + m) * p.K + b * 32);
+                const uint4 x0 = xsrc[h1];
+                const uint4 x1 = xsrc[h1 ^ 1];
+                const float dx = xds[(size_t)(xrow + m) * nb + b];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                  const int sb = dot_halves(w0[r], w1[r], x0, x1);
+                  acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, sb);
+                }
+              }
+            }
+          }
+          store_partials<R, M>(acc, lane, pp, rbase, nr - rbase, s, S);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(slot));
+        ++it;
+      }
+    }
+  }
+}
+
+// ============================================================================
+// Register kernel (fallback): the same tasks, weights loaded into registers.
+// ============================================================================
+#ifndef MEMRA_REG_WARPS
+#define MEMRA_REG_WARPS 16
+#endif
+constexpr int kRegWarps = MEMRA_REG_WARPS;
+constexpr int kRegThreads = kRegWarps * 32;
+// 32 resident warps per SM (64 registers a thread): plain 256-bit streaming needs
+// about that many loads in flight to approach the HBM read ceiling.
+constexpr int kRegCtasPerSm = kRegWarps >= 32 ? 1 : 32 / kRegWarps;
+// Several activation rows need more registers than 64 a thread: those products
+// run half as many warps (128 registers a thread).
+__host__ __device__ constexpr int reg_ctas_per_sm(int M) {
+  return M == 1 ? kRegCtasPerSm : (kRegCtasPerSm > 1 ? kRegCtasPerSm / 2 : 1);
+}
+constexpr int kPartFloats = 8192;  // 32 KB of slice partials per tile
+
+template <int M, int R, int MODE>
+__global__ void __launch_bounds__(kRegThreads, reg_ctas_per_sm(M)) q8_reg_kernel(const Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nb = p.nb;
+  const int S = p.S;
+
+  // Shared memory: xs | xds | partials | ids | gates.
+  int8_t* xs = reinterpret_cast<int8_t*>(smem);
+  float* xds = reinterpret_cast<float*>(smem + p.off_xd);
+  float* part = reinterpret_cast<float*>(smem + p.off_part);
+  int32_t* s_ids = reinterpret_cast<int32_t*>(smem + p.off_yacc);
   float* s_gate = reinterpret_cast<float*>(s_ids + kMaxTopK);
 
-  const int64_t units = p.vrows / p.unit;
-  const int64_t v_begin = units * blockIdx.x / gridDim.x * p.unit;
-  const int64_t v_end = units * (blockIdx.x + 1) / gridDim.x * p.unit;
+  const int64_t u0 = p.units * blockIdx.x / gridDim.x;
+  const int64_t u1 = p.units * (blockIdx.x + 1) / gridDim.x;
 
   pdl_launch_dependents();
-
-  if (MODE != kDense) {
-    // Expert ids and gate weights may come from the preceding kernel.
-    pdl_wait();
-    if (threadIdx.x < p.top_k) {
-      const int32_t e = p.ids[threadIdx.x];
-      const bool ok = e >= 0 && e < p.E;
-      s_ids[threadIdx.x] = ok ? e : -1;
-      s_gate[threadIdx.x] = (MODE == kMoeGated) ? p.gate_w[threadIdx.x] : 1.0f;
-      if (!ok && p.status && blockIdx.x == 0) atomicOr(p.status, 1);
-    }
-    __syncthreads();
+  pdl_wait();
+  if (MODE != kDense) load_routing<MODE>(p, s_ids, s_gate, threadIdx.x, kRegThreads);
+  // Stage the activation rows.
+  {
+    const int64_t words = (int64_t)p.xrows * p.K / 16;
+    for (int64_t i = threadIdx.x; i < words; i += kRegThreads)
+      reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(p.xq)[i];
+    const int64_t nd = (int64_t)p.xrows * nb;
+    for (int64_t i = threadIdx.x; i < nd; i += kRegThreads) xds[i] = p.xd[i];
   }
+  __syncthreads();
 
-  // Weight row of virtual row v (nullptr for an invalid expert) and its x row.
-  auto row_of = [&](int64_t v, const int8_t*& q, const uint16_t*& d, int& xrow) -> bool {
-    if (MODE == kDense) {
-      q = p.wq + v * p.K;
-      d = p.wd + v * nb;
-      xrow = 0;
-      return true;
+  const int nseg = num_segs<MODE>(p, u0, u1);
+  bool any_valid = false;
+  for (int si = 0; si < nseg; ++si) {
+    const Seg g = get_seg<MODE>(p, u0, u1, si, s_ids);
+    if (!g.valid) {
+      if (MODE == kMoeUngated)
+        for (int i = threadIdx.x; i < g.nrows; i += kRegThreads) p.y[g.out0 + i] = 0.0f;
+      continue;
     }
-    int64_t k, n;
-    if (MODE == kMoeUngated) {
-      k = v / p.N;
-      n = v - k * p.N;
-    } else {
-      n = v / p.top_k;
-      k = v - n * p.top_k;
-    }
-    const int e = s_ids[k];
-    xrow = p.x_per_expert ? (int)k : 0;
-    if (e < 0) return false;
-    const int64_t row = (int64_t)e * p.N + n;
-    q = p.wq + row * p.K;
-    d = p.wd + row * nb;
-    return true;
-  };
-
-  bool staged = false;
-  for (int64_t tile_v0 = v_begin; tile_v0 < v_end; tile_v0 += p.tile_rows) {
-    const int tile_n = (int)min((int64_t)p.tile_rows, v_end - tile_v0);
-    const int groups = (tile_n + R - 1) / R;
-    const int nchunks = groups * cpr;
-
-    auto load_chunk = [&](ChunkRegs<R>& regs, int c) {
-      const int g = c / cpr;
-      const int pt = c - g * cpr;
-      const int b = pt * 32 + lane;
+    const int xrow = (MODE == kDense) ? 0 : g.xrow;
+    for (int r0 = 0; r0 < g.nrows; r0 += p.tile_rows) {
+      const int nr = min(p.tile_rows, g.nrows - r0);
+      const int groups = (nr + R - 1) / R;
+      const int ntasks = groups * S;
+      for (int t = warp; t < ntasks; t += kRegWarps) {
+        const int gi = t / S;
+        const int s = t - gi * S;
+        const int rbase = gi * R;
+        const int plo = slice_begin(s, p.cpr, S);
+        const int phi = slice_begin(s + 1, p.cpr, S);
+        float acc[R][M];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int vi = g * R + r;
-        const int8_t* q;
-        const uint16_t* d;
-        int xrow;
-        bool ok = b < nb && vi < tile_n;
-        if (ok) ok = row_of(tile_v0 + vi, q, d, xrow);
-        if (ok) {
-          regs.w[r] = ld_stream_32B(q + (int64_t)b * 32);
-          regs.d[r] = ld_stream_u16(d + b);
-        } else {
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) regs.w[r].w[i] = 0u;
-          regs.d[r] = 0;
-        }
-      }
-    };
-
-    auto compute_chunk = [&](const ChunkRegs<R>& regs, int c) {
-      const int g = c / cpr;
-      const int pt = c - g * cpr;
-      const int b = pt * 32 + lane;
-      float vals[V];
+          for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
+        // Parts in groups of G: every load of a group is issued before its math.
+        constexpr int G = R >= 4 ? 1 : (R == 2 || MODE != kDense ? 2 : kSlicePartsMax);
+        for (int q0 = plo; q0 < phi; q0 += G) {
+          Quants32 w[G][R];
+          uint16_t dw[G][R];
 #pragma unroll
-      for (int i = 0; i < V; ++i) vals[i] = 0.0f;
-      if (b < nb) {
-        int xrow0 = 0;
-        if (MODE != kDense) {
-          const int8_t* q;
-          const uint16_t* d;
-          row_of(tile_v0 + g * R, q, d, xrow0);
-        }
+          for (int q = 0; q < G; ++q) {
+            const int b = (q0 + q) * 32 + lane;
+            const bool inb = q0 + q < phi && b < nb;
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-          const int xr = (MODE == kDense) ? m : xrow0;
-          const uint4 lo = xs[((size_t)xr * 2 + 0) * nb + b];
-          const uint4 hi = xs[((size_t)xr * 2 + 1) * nb + b];
-          const float dx = xds[(size_t)xr * nb + b];
+            for (int r = 0; r < R; ++r) {
+              if (inb && rbase + r < nr) {
+                const int64_t row = g.row0 + r0 + rbase + r;
+                w[q][r] = ld_stream_32B(p.wq + row * p.K + (int64_t)b * 32);
+                dw[q][r] = ld_stream_u16(p.wd + row * nb + b);
+              } else {
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const int s = block_dot(regs.w[r], lo, hi);
-            const float c_b = __half2float(__ushort_as_half(regs.d[r])) * dx;
-            vals[r * M + m] = c_b * (float)s;
+                for (int i = 0; i < 8; ++i) w[q][r].w[i] = 0u;
+                dw[q][r] = 0;
+              }
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < G; ++q) {
+            const int b = (q0 + q) * 32 + lane;
+            if (q0 + q < phi && b < nb) {
+#pragma unroll
+              for (int m = 0; m < M; ++m) {
+                const uint4* xsrc = reinterpret_cast<const uint4*>(
+                    xs + (size_t)(xrow + m) * p.K + (size_t)b * 32);
+                const uint4 x0 = xsrc[0];
+                const uint4 x1 = xsrc[1];
+                const float dx = xds[(size_t)(xrow + m) * nb + b];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                  const uint4 w0 =
+                      make_uint4(w[q][r].w[0], w[q][r].w[1], w[q][r].w[2], w[q][r].w[3]);
+                  const uint4 w1 =
+                      make_uint4(w[q][r].w[4], w[q][r].w[5], w[q][r].w[6], w[q][r].w[7]);
+                  const int sb = dot_halves(w0, w1, x0, x1);
+                  acc[r][m] = block_term_acc(acc[r][m], dw[q][r], dx, sb);
+                }
+              }
+            }
           }
         }
+        store_partials<R, M>(acc, lane, part, rbase, nr - rbase, s, S);
       }
-      warp_sum_transposed<V>(vals, lane);
-      constexpr int t = log2i(V);
-      if ((lane & ((32 >> t) - 1)) == 0) {
-        const int idx = lane >> (5 - t);
-        if (idx < R * M) {
-          const int r = idx / M;
-          const int m = idx - r * M;
-          const int vi = g * R + r;
-          if (vi < tile_n) part[((size_t)vi * cpr + pt) * M + m] = vals[0];
-        }
-      }
-    };
-
-    ChunkRegs<R> ring[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = warp + u * kWarps;
-      if (c < nchunks) load_chunk(ring[u], c);
-    }
-
-    if (!staged) {
-      if (MODE == kDense) pdl_wait();
-      // Stage the activation rows: 16-byte words into the half-block-split layout.
-      const int64_t words = (int64_t)p.xrows * p.K / 16;
-      for (int64_t i = threadIdx.x; i < words; i += kThreads) {
-        const int64_t row = i / (p.K / 16);
-        const int64_t j = i - row * (p.K / 16);
-        const int64_t blk = j >> 1;
-        const int64_t h = j & 1;
-        xs[(row * 2 + h) * nb + blk] = reinterpret_cast<const uint4*>(p.xq)[i];
-      }
-      const int64_t nd = (int64_t)p.xrows * nb;
-      for (int64_t i = threadIdx.x; i < nd; i += kThreads) xds[i] = p.xd[i];
       __syncthreads();
-      staged = true;
-    }
-
-    for (int c = warp; c < nchunks; c += U * kWarps) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int cc = c + u * kWarps;
-        if (cc < nchunks) {
-          compute_chunk(ring[u], cc);
-          const int nc = cc + U * kWarps;
-          if (nc < nchunks) load_chunk(ring[u], nc);
+      // Tile epilogue: slice sums in order.
+      for (int i = threadIdx.x; i < nr * M; i += kRegThreads) {
+        const int r = i / M;
+        const int m = i - r * M;
+        float tot = part[((size_t)r * S) * M + m];
+        for (int s = 1; s < S; ++s) tot = __fadd_rn(tot, part[((size_t)r * S + s) * M + m]);
+        if (MODE == kMoeGated) {
+          // Gated tiles cover the CTA's whole n-range, so each output accumulates
+          // over k (ascending) in its own y word, starting from the first valid k.
+          const int64_t n = u0 + r0 + r;
+          const float prev = any_valid ? p.y[n] : 0.0f;
+          p.y[n] = __fadd_rn(prev, __fmul_rn(s_gate[g.k], tot));
+        } else {
+          p.y[(int64_t)m * p.units + g.out0 + r0 + r] = tot;
         }
       }
+      __syncthreads();
     }
-    __syncthreads();
-
-    // Epilogue: sum each row's parts in order and store.
-    if (MODE == kMoeGated) {
-      const int rows_n = tile_n / p.top_k;
-      for (int i = threadIdx.x; i < rows_n; i += kThreads) {
-        float acc = 0.0f;
-        for (int k = 0; k < p.top_k; ++k) {
-          if (s_ids[k] < 0) continue;
-          const int vi = i * p.top_k + k;
-          float yk = 0.0f;
-          for (int pt = 0; pt < cpr; ++pt) yk += part[(size_t)vi * cpr + pt];
-          acc += s_gate[k] * yk;
-        }
-        p.y[tile_v0 / p.top_k + i] = acc;
-      }
-    } else {
-      for (int i = threadIdx.x; i < tile_n * M; i += kThreads) {
-        const int vi = i / M;
-        const int m = i - vi * M;
-        float acc = 0.0f;
-        for (int pt = 0; pt < cpr; ++pt) acc += part[((size_t)vi * cpr + pt) * M + m];
-        p.y[(int64_t)m * p.vrows + tile_v0 + vi] = acc;
-      }
-    }
-    __syncthreads();
+    any_valid = true;
+  }
+  if (MODE == kMoeGated && !any_valid) {
+    for (int64_t i = u0 + threadIdx.x; i < u1; i += kRegThreads) p.y[i] = 0.0f;
   }
 }
 
@@ -303,7 +625,9 @@ __global__ void __launch_bounds__(256)
     const int64_t b = rem - n * nb;
     const Quants32 w = ld_stream_32B(wq + n * K + b * 32);
     const uint4* xp = reinterpret_cast<const uint4*>(xq + m * K + b * 32);
-    s[i] = block_dot(w, xp[0], xp[1]);
+    const uint4 w0 = make_uint4(w.w[0], w.w[1], w.w[2], w.w[3]);
+    const uint4 w1 = make_uint4(w.w[4], w.w[5], w.w[6], w.w[7]);
+    s[i] = dot_halves(w0, w1, xp[0], xp[1]);
   }
 }
 
@@ -311,64 +635,130 @@ __global__ void __launch_bounds__(256)
 // Host dispatch.
 // ----------------------------------------------------------------------------
 
-size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-size_t smem_bytes(const Params& p, int M) {
-  size_t b = align16((size_t)p.xrows * p.K);                            // xs
-  b += ((size_t)p.xrows * p.nb + 3) / 4 * 16;                           // xds
-  b += align16((size_t)p.tile_rows * p.cpr * M * sizeof(float));        // partial sums
-  b += 2 * kMaxTopK * sizeof(int32_t);                                  // ids, gates
-  return b;
+constexpr size_t kTmaStageTarget = 20 * 1024;
+constexpr size_t kTmaRingBudget = 88 * 1024;
+constexpr size_t kTmaSmemPairLimit = 110 * 1024;  // two CTAs per SM (this + the next kernel)
+
+// Variant seam for tests and benchmarks: MEMRA_GEMV_PATH=tma selects the bulk-copy
+// kernel where it applies (read once per process); the register kernel is the
+// default.
+bool force_tma_path() {
+  static const bool v = [] {
+    const char* e = std::getenv("MEMRA_GEMV_PATH");
+    return e && std::strcmp(e, "tma") == 0;
+  }();
+  return v;
 }
 
-template <int M, int R, int U, int MODE>
-memra_status launch_gemm(Params p, cudaStream_t stream) {
-  DeviceInfo info;
-  if (!device_info(&info)) return MEMRA_ERR_CUDA;
-  p.nb = (int)(p.K / 32);
-  p.cpr = (p.nb + 31) / 32;
-  const int64_t units = p.vrows / p.unit;
-  // Tile: as many rows as the partial-sum budget allows, a multiple of both the
-  // range unit and R.
-  int64_t step = p.unit;
-  while (step % R) step += p.unit;
-  int64_t tile = kPartFloats / ((int64_t)p.cpr * M);
-  tile = std::max<int64_t>(step, tile / step * step);
-  // Resident CTAs per SM from the shared-memory footprint (registers allow two).
-  p.tile_rows = (int)tile;
-  size_t smem = smem_bytes(p, M);
-  if (smem > (size_t)info.max_smem_optin) return MEMRA_ERR_UNSUPPORTED;
-  const int per_sm = (2 * (smem + 1024) <= 228 * 1024) ? 2 : 1;
-  int64_t grid = std::min<int64_t>(units, (int64_t)info.sms * per_sm);
-  // Shrink the tile to the CTA's row range when that is smaller.
-  const int64_t rows_per_cta = (units + grid - 1) / grid * p.unit;
-  if (rows_per_cta < tile) {
-    tile = (rows_per_cta + step - 1) / step * step;
-    p.tile_rows = (int)tile;
-    smem = smem_bytes(p, M);
+int64_t max_units_per_cta(int64_t units, int64_t grid) { return (units + grid - 1) / grid; }
+
+template <int M, int R, int MODE>
+bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out) {
+  if (!force_tma_path()) return false;
+  if (p.K % 256 != 0) return false;
+  if (!aligned(p.wd, 16) || !aligned(p.xd, 16) || !aligned(p.xq, 16) || !aligned(p.wq, 16))
+    return false;
+  const size_t row_bytes = (size_t)p.K + (size_t)p.nb * 2;
+  int rps = (int)std::max<size_t>(1, kTmaStageTarget / row_bytes);
+  rps = std::max(R, rps / R * R);
+  const size_t stage = align_up((size_t)rps * p.K, 128) + align_up((size_t)rps * p.nb * 2, 128);
+  const size_t xbytes =
+      align_up((size_t)p.xrows * p.K, 128) + align_up((size_t)p.xrows * p.nb * 4, 128);
+  const int64_t maxu = max_units_per_cta(p.units, grid);
+  const size_t yacc = MODE == kMoeGated ? align_up((size_t)maxu * 4, 16) : 0;
+  const size_t fixed = kHeaderBytes + xbytes + yacc;
+  const size_t part_per_stage = align_up((size_t)rps * p.S * M * 4, 16);
+  // Ring: up to the budget, and within the two-CTAs-per-SM limit when possible.
+  size_t limit = std::max<size_t>(kTmaSmemPairLimit, fixed + 2 * (stage + part_per_stage));
+  limit = std::min<size_t>(limit, (size_t)info.max_smem_optin);
+  int ns = (int)std::min<size_t>(kMaxStages, kTmaRingBudget / stage);
+  while (ns > 2 && fixed + ns * (stage + part_per_stage) > limit) --ns;
+  if (ns < 2 || fixed + ns * (stage + part_per_stage) > (size_t)info.max_smem_optin) return false;
+  p.rps = rps;
+  p.ns = ns;
+  p.stage_bytes = (uint32_t)stage;
+  p.wd_off = (uint32_t)align_up((size_t)rps * p.K, 128);
+  size_t off = kHeaderBytes;
+  p.off_x = (uint32_t)off;
+  p.off_xd = (uint32_t)(off + align_up((size_t)p.xrows * p.K, 128));
+  off += xbytes;
+  p.off_ring = (uint32_t)off;
+  off += (size_t)ns * stage;
+  p.off_part = (uint32_t)off;
+  off += (size_t)ns * part_per_stage;
+  p.off_yacc = (uint32_t)off;
+  off += yacc;
+  *smem_out = off;
+  return true;
+}
+
+template <int M, int R, int MODE>
+bool plan_reg(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out) {
+  const int64_t maxu = max_units_per_cta(p.units, grid);
+  int64_t tile;
+  if (MODE == kMoeGated) {
+    tile = maxu;  // the gated epilogue needs the whole n-range in one tile
+  } else {
+    tile = std::max<int64_t>(R, kPartFloats / ((int64_t)p.S * M) / R * R);
+    tile = std::min<int64_t>(tile, (maxu + R - 1) / R * R);
   }
-  auto kernel = q8_gemm_kernel<M, R, U, MODE>;
+  p.tile_rows = (int)std::max<int64_t>(tile, 1);
+  const size_t xb = align_up((size_t)p.xrows * p.K, 16);
+  const size_t db = align_up((size_t)p.xrows * p.nb * 4, 16);
+  const size_t pb = align_up((size_t)p.tile_rows * p.S * M * 4, 16);
+  p.off_xd = (uint32_t)xb;
+  p.off_part = (uint32_t)(xb + db);
+  p.off_yacc = (uint32_t)(xb + db + pb);
+  const size_t total = xb + db + pb + 2 * kMaxTopK * 4;
+  if (total > (size_t)info.max_smem_optin) return false;
+  *smem_out = total;
+  return true;
+}
+
+template <typename Kern>
+memra_status launch(Kern kernel, int64_t grid, int threads, size_t smem, cudaStream_t stream,
+                    const Params& p) {
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  cudaError_t e = launch_kernel(kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, p);
+  cudaError_t e = launch_kernel(kernel, dim3((unsigned)grid), dim3(threads), smem, stream, p);
   if (e != cudaSuccess) return cuda_fail(e);
   return MEMRA_OK;
+}
+
+template <int M, int R, int MODE>
+memra_status run_product(Params p, cudaStream_t stream) {
+  DeviceInfo info;
+  if (!device_info(&info)) return MEMRA_ERR_CUDA;
+  p.nb = (int)(p.K / 32);
+  p.cpr = (p.nb + 31) / 32;
+  p.S = slices_for(p.cpr);
+  // One CTA per SM for the TMA kernel.
+  int64_t grid = std::min<int64_t>(p.units, info.sms);
+  size_t smem = 0;
+  if (plan_tma<M, R, MODE>(p, info, grid, &smem))
+    return launch(q8_tma_kernel<M, R, MODE>, grid, kTmaThreads, smem, stream, p);
+  grid = std::min<int64_t>(p.units, (int64_t)info.sms * reg_ctas_per_sm(M));
+  if (plan_reg<M, R, MODE>(p, info, grid, &smem))
+    return launch(q8_reg_kernel<M, R, MODE>, grid, kRegThreads, smem, stream, p);
+  return MEMRA_ERR_UNSUPPORTED;
 }
 
 template <int MODE>
 memra_status dispatch_m(const Params& p, int M, cudaStream_t s) {
   switch (M) {
-    case 1: return launch_gemm<1, 1, 8, MODE>(p, s);
-    case 2: return launch_gemm<2, 1, 8, MODE>(p, s);
-    case 3: return launch_gemm<3, 1, 8, MODE>(p, s);
-    case 4: return launch_gemm<4, 2, 4, MODE>(p, s);
-    case 5: return launch_gemm<5, 2, 4, MODE>(p, s);
-    case 6: return launch_gemm<6, 2, 4, MODE>(p, s);
-    case 7: return launch_gemm<7, 2, 4, MODE>(p, s);
-    case 8: return launch_gemm<8, 4, 2, MODE>(p, s);
+    case 1: return run_product<1, 1, MODE>(p, s);
+    case 2: return run_product<2, 1, MODE>(p, s);
+    case 3: return run_product<3, 1, MODE>(p, s);
+    case 4: return run_product<4, 2, MODE>(p, s);
+    case 5: return run_product<5, 2, MODE>(p, s);
+    case 6: return run_product<6, 2, MODE>(p, s);
+    case 7: return run_product<7, 2, MODE>(p, s);
+    case 8: return run_product<8, 4, MODE>(p, s);
   }
   return MEMRA_ERR_UNSUPPORTED;
 }
@@ -412,8 +802,7 @@ extern "C" memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t
   p.xd = xd;
   p.xrows = (int)M;
   p.y = y;
-  p.vrows = N;
-  p.unit = 1;
+  p.units = N;
   return dispatch_m<kDense>(p, (int)M, stream);
 }
 
@@ -452,19 +841,18 @@ extern "C" memra_status memra_q8_0_moe_gemv(const int8_t* wq_bank, const uint16_
   p.xd = xd;
   p.xrows = (int)xrows;
   p.y = y;
-  p.vrows = top_k * N;
   p.ids = ids;
   p.gate_w = gate_w;
   p.top_k = (int)top_k;
   p.E = E;
-  p.x_per_expert = x_per_expert;
+  p.xpe = x_per_expert;
   p.status = dev_status;
   if (gate_w) {
-    p.unit = (int)top_k;
-    return launch_gemm<1, 1, 8, kMoeGated>(p, stream);
+    p.units = N;
+    return run_product<1, 1, kMoeGated>(p, stream);
   }
-  p.unit = 1;
-  return launch_gemm<1, 1, 8, kMoeUngated>(p, stream);
+  p.units = top_k * N;
+  return run_product<1, 1, kMoeUngated>(p, stream);
 }
 
 extern "C" memra_status memra_q8_0_block_dots(const int8_t* wq, int64_t N, int64_t K,

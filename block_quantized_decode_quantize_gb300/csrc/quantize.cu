@@ -79,11 +79,12 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
-// Weights: d16 = fp16_rne(amax / 127); quants use the stored fp16 value.
+// Weights: d16 = fp16_rne(amax / 127); quants use the stored fp16 value.  This
+// kernel does not let its dependents start early: the products stream weights
+// before waiting on their predecessor, so they must never overlap the ingest.
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_q8_0_kernel(const float* __restrict__ w, int64_t groups, int8_t* __restrict__ q,
                          uint16_t* __restrict__ d) {
-  pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;

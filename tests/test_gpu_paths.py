@@ -1,0 +1,66 @@
+"""The two product kernels (shared-memory TMA stream and register stream) implement
+one summation order, so they must agree bit for bit.  The bulk-copy kernel is
+selected in a child process with MEMRA_GEMV_PATH=tma (read once per process)."""
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import sys, torch
+sys.path.insert(0, %(root)r)
+import synth
+import block_quantized_decode_quantize_gb300 as mem
+out = {}
+for (N, K, M) in [(1003, 4096, 1), (777, 5120, 1), (513, 2048, 4), (300, 5120, 8), (4100, 768, 1),
+                  (64, 17408, 1)]:
+    w = synth.weights_fp32(N, K, 70, N, K, device="cuda")
+    x = synth.activations_bf16(M, K, 71, N, K, M, outlier_frac=0.001, device="cuda")
+    wq, wd = mem.memra_quantize_q8_0(w)
+    xq, xd = mem.memra_quantize_q8_1(x)
+    out["d%%d_%%d_%%d" %% (N, K, M)] = mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd).cpu()
+E, N, K, k = 10, 300, 768, 4
+wb = synth.weights_fp32(E * N, K, 72, device="cuda")
+bq, bd = mem.memra_quantize_q8_0(wb)
+bq, bd = bq.view(E, N, K), bd.view(E, N, K // 32)
+ids = torch.tensor([3, 9, 0, 3], dtype=torch.int32, device="cuda")
+gw = torch.tensor([0.4, 0.3, 0.2, 0.1], device="cuda")
+x = synth.activations_bf16(k, K, 73, device="cuda")
+xq, xd = mem.memra_quantize_q8_1(x)
+out["moe_u"] = mem.memra_q8_0_moe_gemv(bq, bd, ids, None, xq, xd, True).cpu()
+out["moe_g"] = mem.memra_q8_0_moe_gemv(bq, bd, ids, gw, xq, xd, True).cpu()
+out["moe_s"] = mem.memra_q8_0_moe_gemv(bq, bd, ids, gw, xq[0], xd[0], False).cpu()
+torch.cuda.synchronize()
+torch.save(out, sys.argv[1])
+"""
+
+
+def run_child(tmp_path, env_path):
+    path = str(tmp_path / ("out_%s.pt" % (env_path or "default")))
+    env = dict(os.environ)
+    env.pop("MEMRA_GEMV_PATH", None)
+    if env_path:
+        env["MEMRA_GEMV_PATH"] = env_path
+    src = CHILD % {"root": ROOT}
+    r = subprocess.run([sys.executable, "-c", src, path], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    return torch.load(path)
+
+
+def test_tma_and_register_kernels_agree_bitwise(tmp_path):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_quantized_decode_quantize_gb300 import build
+    build.build()
+    a = run_child(tmp_path, None)
+    b = run_child(tmp_path, "tma")
+    assert a.keys() == b.keys()
+    for k in a:
+        assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), k
