@@ -130,7 +130,12 @@ class MoeLayer:
         self.status = torch.zeros((1,), dtype=torch.int32, device=device)
         self.weight_bytes = k * (synth.q8_0_bytes(2 * F, H) + synth.q8_0_bytes(H, F))
 
-    def run(self, mem):
+    def run(self, mem, fused=False):
+        if fused:
+            mem.memra_q8_0_moe_ffn(self.gq, self.gd, self.dq, self.dd, self.ids, self.gw,
+                                   self.x[0], y=self.y, workspace=self.ygu,
+                                   dev_status=self.status)
+            return
         mem.memra_quantize_q8_1(self.x, self.xq, self.xd)
         mem.memra_q8_0_moe_gemv(self.gq, self.gd, self.ids, None, self.xq[0], self.xd[0], False,
                                 y=self.ygu, dev_status=self.status)
@@ -139,7 +144,12 @@ class MoeLayer:
                                 y=self.y, dev_status=self.status)
 
 
-def run_gemv_op(mem, op, quantize=True):
+def run_gemv_op(mem, op, quantize=True, fused=False):
+    """One product of a step: the fused entry point (quantisation in the kernel's
+    prologue), or a q8_1 quantise launch followed by the GEMV / verify GEMM."""
+    if fused:
+        mem.memra_q8_0_quant_gemm(op.wq, op.wd, op.x, y=op.y)
+        return
     if quantize:
         mem.memra_quantize_q8_1(op.x, op.xq, op.xd)
     if op.xq.shape[0] == 1:
@@ -151,8 +161,9 @@ def run_gemv_op(mem, op, quantize=True):
 class Workload:
     """A step = a fixed list of library calls; captured once into a CUDA graph."""
 
-    def __init__(self, name, mem, device, layers=None):
+    def __init__(self, name, mem, device, layers=None, fused=False):
         self.name = name
+        self.fused = fused
         self.mem = mem
         self.device = device
         self.moe = None
@@ -182,8 +193,8 @@ class Workload:
     @property
     def launches_per_step(self):
         if self.moe is not None:
-            return 4 * len(self.moe)
-        return 2 * len(self.ops)
+            return (2 if self.fused else 4) * len(self.moe)
+        return (1 if self.fused else 2) * len(self.ops)
 
     @property
     def gemv_launches_per_step(self):
@@ -194,14 +205,16 @@ class Workload:
     def step(self):
         if self.moe is not None:
             for m in self.moe:
-                m.run(self.mem)
+                m.run(self.mem, fused=self.fused)
         else:
             for op in self.ops:
-                run_gemv_op(self.mem, op)
+                run_gemv_op(self.mem, op, fused=self.fused)
 
     def gemv_only(self):
         """The step's weight-streaming kernels alone (activations already quantised)."""
-        if self.moe is not None:
+        if self.moe is not None and self.fused:
+            self.step()  # both launches of the fused layer stream weights
+        elif self.moe is not None:
             for m in self.moe:
                 self.mem.memra_q8_0_moe_gemv(m.gq, m.gd, m.ids, None, m.xq[0], m.xd[0], False,
                                              y=m.ygu, dev_status=m.status)
@@ -209,7 +222,7 @@ class Workload:
                                              y=m.y, dev_status=m.status)
         else:
             for op in self.ops:
-                run_gemv_op(self.mem, op, quantize=False)
+                run_gemv_op(self.mem, op, quantize=False, fused=self.fused)
 
     def inputs(self):
         if self.moe is not None:
@@ -461,7 +474,7 @@ def run_memra(args):
     barrier(world)
     mem.lib()
 
-    wl = Workload(args.workload, mem, device, layers=args.layers)
+    wl = Workload(args.workload, mem, device, layers=args.layers, fused=args.fused)
     stream = torch.cuda.Stream(device)
     step_graph = wl.capture(wl.step)
     gemv_graph = wl.capture(wl.gemv_only)
@@ -500,7 +513,9 @@ def run_memra(args):
                             if prof else None),
                 "peak_kind": peak_kind + " copy bandwidth (MEASURED_PEAKS hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "kernel": "q8_gemm_kernel (Q8_0 GEMV, M=%s)" % (
+                "kernel": "Q8_0 product kernel (%s, M=%s)" % (
+                    "routed experts" if wl.moe is not None else
+                    ("quantise fused" if wl.fused else "q8_1 input"),
                     1 if wl.moe is not None else wl.ops[0].xq.shape[0]),
                 "avg_launch_us": round(gemv_avg_s * 1e6, 3),
                 "bytes_per_launch": int(bytes_per_launch),
@@ -543,6 +558,10 @@ def run_memra(args):
     if rank == 0:
         cfg = workload_config(args.workload, wl)
         cfg["parallelism"] = "replicas x%d (no data-path collective)" % world
+        if wl.moe is None:
+            cfg["activation_quantise"] = ("fused into the product's prologue "
+                                          "(memra_q8_0_quant_gemm)" if wl.fused else
+                                          "separate memra_quantize_q8_1 launch")
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -614,6 +633,9 @@ def main(argv=None):
     ap.add_argument("--workload", choices=WORKLOADS, default="dense27b_sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--fused", action="store_true",
+                    help="quantise activations in the product's prologue "
+                         "(memra_q8_0_quant_gemm) instead of a separate q8_1 launch")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers than the workload's own (profiling captures only)")
     args = ap.parse_args(argv)

@@ -50,8 +50,11 @@ _SIGS = {
     "memra_quantize_q8_1": [_p, _i32, _i64, _i64, _p, _p, _p],
     "memra_q8_0_gemv": [_p, _p, _i64, _i64, _p, _p, _p, _p],
     "memra_q8_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
+    "memra_q8_0_quant_gemm": [_p, _p, _i64, _i64, _i64, _p, _i32, _p, _p],
     "memra_q8_0_moe_gemv": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p, _p],
     "memra_swiglu_quantize_q8_1": [_p, _i64, _i64, _p, _p, _p],
+    "memra_q8_0_moe_ffn": [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _i32, _p, _p, _p,
+                           _p],
     "memra_q8_0_block_dots": [_p, _i64, _i64, _p, _i64, _p, _p],
 }
 
@@ -168,6 +171,32 @@ def memra_q8_0_gemm_small_m(wq, wd, xq, xd, y=None):
     return y
 
 
+def memra_q8_0_quant_gemm(wq, wd, x, y=None):
+    """y [M, N] = W (Q8_0) x, with x [M, K] (bf16 or fp32) quantised to q8_1 inside the
+    kernel; bit-identical to memra_quantize_q8_1 followed by memra_q8_0_gemm_small_m."""
+    _need(wq, "wq", torch.int8)
+    N, K = wq.shape
+    dev = wq.device
+    _need(wd, "wd", torch.float16, dev, (N, K // 32))
+    if x.dtype == torch.bfloat16:
+        dt = MEMRA_BF16
+    elif x.dtype == torch.float32:
+        dt = MEMRA_F32
+    else:
+        raise TypeError("x must be bfloat16 or float32")
+    _need(x, "x", x.dtype, dev)
+    M = x.shape[0]
+    _need(x, "x", x.dtype, dev, (M, K))
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, (M, N))
+    with torch.cuda.device(dev):
+        _check("memra_q8_0_quant_gemm",
+               lib().memra_q8_0_quant_gemm(_ptr(wq), _ptr(wd), N, K, M, _ptr(x), dt, _ptr(y),
+                                           _stream(wq)))
+    return y
+
+
 def memra_q8_0_gemv(wq, wd, xq, xd, y=None):
     """y [N] = W (Q8_0) x (q8_1) for one activation row (xq [K], xd [K/32])."""
     _need(wq, "wq", torch.int8)
@@ -218,6 +247,45 @@ def memra_q8_0_moe_gemv(wq_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert, y=N
                lib().memra_q8_0_moe_gemv(_ptr(wq_bank), _ptr(wd_bank), E, N, K, _ptr(ids),
                                          _ptr(gate_w), top_k, _ptr(xq), _ptr(xd), xpe, _ptr(y),
                                          _ptr(dev_status), _stream(wq_bank)))
+    return y
+
+
+def memra_q8_0_moe_ffn(gu_q, gu_d, dn_q, dn_d, ids, gate_w, x, y=None, workspace=None,
+                       dev_status=None):
+    """One routed-expert FFN layer: gu_q int8 [E, 2F, H], gu_d float16 [E, 2F, H/32],
+    dn_q int8 [E, H, F], dn_d float16 [E, H, F/32], ids int32 [top_k], gate_w float32
+    [top_k], x [H] (bf16 or fp32).  Returns y float32 [H].  `workspace` (float32
+    [top_k, 2F]) receives the gate|up outputs; allocated here when not given."""
+    _need(gu_q, "gu_q", torch.int8)
+    E, F2, H = gu_q.shape
+    F = F2 // 2
+    dev = gu_q.device
+    _need(gu_d, "gu_d", torch.float16, dev, (E, F2, H // 32))
+    _need(dn_q, "dn_q", torch.int8, dev, (E, H, F))
+    _need(dn_d, "dn_d", torch.float16, dev, (E, H, F // 32))
+    _need(ids, "ids", torch.int32, dev)
+    top_k = ids.shape[0]
+    _need(gate_w, "gate_w", torch.float32, dev, (top_k,))
+    if x.dtype == torch.bfloat16:
+        dt = MEMRA_BF16
+    elif x.dtype == torch.float32:
+        dt = MEMRA_F32
+    else:
+        raise TypeError("x must be bfloat16 or float32")
+    _need(x, "x", x.dtype, dev, (H,))
+    if y is None:
+        y = torch.empty((H,), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, (H,))
+    if workspace is None:
+        workspace = torch.empty((top_k, F2), dtype=torch.float32, device=dev)
+    _need(workspace, "workspace", torch.float32, dev, (top_k, F2))
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    with torch.cuda.device(dev):
+        _check("memra_q8_0_moe_ffn",
+               lib().memra_q8_0_moe_ffn(_ptr(gu_q), _ptr(gu_d), _ptr(dn_q), _ptr(dn_d), E, H, F,
+                                        _ptr(ids), _ptr(gate_w), top_k, _ptr(x), dt, _ptr(y),
+                                        _ptr(workspace), _ptr(dev_status), _stream(gu_q)))
     return y
 
 

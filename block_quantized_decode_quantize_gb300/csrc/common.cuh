@@ -19,14 +19,15 @@ constexpr unsigned kFullMask = 0xffffffffu;
 
 // One Q8_0 block of quants (32 bytes) per lane, streamed: a single 256-bit
 // non-coherent load that does not allocate in L1 (the weights are read once per
-// call).  The pointer must be 32-byte aligned.
+// call).  The pointer must be 32-byte aligned.  Volatile, so that loads issued
+// before a grid-dependency wait stay before it.
 struct Quants32 {
   uint32_t w[8];
 };
 
 __device__ __forceinline__ Quants32 ld_stream_32B(const int8_t* p) {
   Quants32 r;
-  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
       : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
         "=r"(r.w[6]), "=r"(r.w[7])
       : "l"(p));
@@ -35,7 +36,7 @@ __device__ __forceinline__ Quants32 ld_stream_32B(const int8_t* p) {
 
 __device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t* p) {
   unsigned short v;
-  asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
   return v;
 }
 
@@ -159,9 +160,122 @@ __device__ __forceinline__ int quant_value(float v, float d) {
   return (int)r;
 }
 
+// Quantise 8 values with scale d: the same integers as quant_value, computed by a
+// multiply with an approximate reciprocal `inv` of d.  round-half-away only changes
+// at k + 1/2, and r = v * inv differs from the correctly rounded quotient fl(v / d)
+// by less than 5e-5 (|v/d| <= 254 and at most four roundings of relative size 2^-24
+// separate them), so whenever r is farther than 1e-4 from every k + 1/2 both round
+// to the same integer.  Values closer than that (exact ties included) take the IEEE
+// quotient; the warp votes so that the division runs only when some lane needs it.
+// Every lane of the warp must call this.
+__device__ __forceinline__ void quant8_fast(const float v[8], float d, float inv, int q[8]) {
+  unsigned near = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float r = __fmul_rn(v[i], inv);
+    const float a = fabsf(r);
+    const float frac = __fsub_rn(a, floorf(a));
+    near |= (fabsf(__fsub_rn(frac, 0.5f)) <= 1e-4f ? 1u : 0u) << i;
+    q[i] = (int)fminf(fmaxf(roundf(r), -127.0f), 127.0f);
+  }
+  if (d == 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = 0;
+    near = 0;
+  }
+  if (__any_sync(kFullMask, near != 0)) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (near & (1u << i)) q[i] = quant_value(v[i], d);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
   return (uint32_t)(a & 0xff) | ((uint32_t)(b & 0xff) << 8) | ((uint32_t)(c & 0xff) << 16) |
          ((uint32_t)(d & 0xff) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// q8_1 quantisation of one 32-value block held by four consecutive lanes (8
+// values each).  Every lane of the warp must call it (two xor-shuffles).
+// Returns the lane's 8 quants packed in 8 bytes and the block scale
+// d = max|v| / 127 (fp32, IEEE division).  Used by the standalone quantiser and by
+// the products that quantise their activation in the prologue, so both give the
+// same bits.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint2 q8_1_group8(const float v[8], float* d_out) {
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+  a = fmaxf(a, __shfl_xor_sync(kFullMask, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(kFullMask, a, 2));
+  const float d = a / 127.0f;
+  const float inv = a == 0.0f ? 0.0f : 127.0f / a;  // within 2 roundings of 1/d
+  int q[8];
+  quant8_fast(v, d, inv, q);
+  uint2 r;
+  r.x = pack4(q[0], q[1], q[2], q[3]);
+  r.y = pack4(q[4], q[5], q[6], q[7]);
+  *d_out = d;
+  return r;
+}
+
+__device__ __forceinline__ void load8_f32(const float* p, float v[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// exp by Cody & Waite's range reduction ("Software Manual for the Elementary
+// Functions", 1980) and a degree-7 Taylor polynomial: k = rint(x log2 e),
+// r = (x - k*C1) - k*C2 with C1 = 0.693359375 (exact product with k) and C2 =
+// ln 2 - C1, p = sum_{i<=7} r^i / i! in Horner form, result p * 2^k.  Every
+// operation is an explicitly rounded fp32 operation (no contraction), and the
+// argument is clamped to [-87, 88] so 2^k is a normal number.
+__device__ __forceinline__ float exp_cody_waite(float x) {
+  x = fminf(fmaxf(x, -87.0f), 88.0f);
+  const float kf = rintf(__fmul_rn(x, 1.44269504088896341f));
+  float r = __fsub_rn(x, __fmul_rn(kf, 0.693359375f));
+  r = __fsub_rn(r, __fmul_rn(kf, -2.12194440e-4f));
+  float p = 1.0f / 5040.0f;
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 720.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 120.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 24.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 6.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  const int k = (int)kf;
+  return __fmul_rn(p, __int_as_float((k + 127) << 23));
+}
+
+// h[i] = (g[i] / (1 + exp(-g[i]))) * u[i] for 8 consecutive values, each fp32
+// operation rounded once in that order (SwiGLU of the routed-expert FFN).
+__device__ __forceinline__ void swiglu8(const float* g, const float* u, float h[8]) {
+  const float4 g0 = *reinterpret_cast<const float4*>(g);
+  const float4 g1 = *reinterpret_cast<const float4*>(g + 4);
+  const float4 u0 = *reinterpret_cast<const float4*>(u);
+  const float4 u1 = *reinterpret_cast<const float4*>(u + 4);
+  const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float den = __fadd_rn(1.0f, exp_cody_waite(-gv[i]));
+    const float sg = __fdiv_rn(gv[i], den);
+    h[i] = __fmul_rn(sg, uv[i]);
+  }
+}
+
+// 8 bf16 values (16 bytes) to fp32, exactly.
+__device__ __forceinline__ void load8_bf16(const uint16_t* p, float v[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -138,6 +138,7 @@ struct Params {
   int nb, cpr, S;
   const int8_t* xq;
   const float* xd;
+  const void* xin;         // unquantised activation (fused-quantisation entry point)
   int xrows;               // activation rows held in shared memory
   float* y;
   int64_t units;           // dense/gated: N; ungated: top_k * N
@@ -153,7 +154,7 @@ struct Params {
   int ns;                  // stages in the ring
   uint32_t stage_bytes;    // bytes per stage (quants, then scales at wd_off)
   uint32_t wd_off;
-  uint32_t off_x, off_xd, off_ring, off_part, off_yacc;
+  uint32_t off_x, off_xd, off_ring, off_part, off_yacc, off_slice;
   // register kernel layout
   int tile_rows;
 };
@@ -221,6 +222,11 @@ __device__ __forceinline__ void load_routing(const Params& p, int32_t* s_ids, fl
   }
 }
 
+// Slice boundaries (in parts) for the row's S slices: tab[s] = s*cpr/S.
+__device__ __forceinline__ void fill_slice_table(int* tab, int cpr, int S, int tid, int nthreads) {
+  for (int s = tid; s <= S; s += nthreads) tab[s] = (int)(((long long)s * cpr) / S);
+}
+
 // ============================================================================
 // TMA producer/consumer kernel.
 // ============================================================================
@@ -229,6 +235,26 @@ constexpr int kTmaThreads = 32 * (1 + kConsumerWarps);
 constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 1024;  // barriers, abort flag, stage metadata, ids, gates
 
+// Activation input of a product: q8_1 planes, or values quantised in the kernel's
+// prologue (bf16, fp32, or SwiGLU of an fp32 gate|up row pair).
+enum XIn { kXq8 = 0, kXbf16 = 1, kXf32 = 2, kXswiglu = 3 };
+
+// The 8 activation values of group g (row-major [rows][K], K % 8 == 0).
+template <int XIN>
+__device__ __forceinline__ void load_x_group(const void* xin, int g, int K, float v[8]) {
+  if (XIN == kXbf16) {
+    load8_bf16(static_cast<const uint16_t*>(xin) + (size_t)g * 8, v);
+  } else if (XIN == kXf32) {
+    load8_f32(static_cast<const float*>(xin) + (size_t)g * 8, v);
+  } else {
+    const int gpr = K / 8;
+    const int row = g / gpr;
+    const int f0 = (g - row * gpr) * 8;
+    const float* gu = static_cast<const float*>(xin) + (size_t)row * 2 * K;
+    swiglu8(gu + f0, gu + K + f0, v);
+  }
+}
+
 struct StageMeta {
   int seg;
   int r0;
@@ -236,7 +262,33 @@ struct StageMeta {
   int pad;
 };
 
-template <int M, int R, int MODE>
+// Quantise `rows` activation rows of K values (bf16 bits or fp32) into the
+// shared-memory q8_1 planes.  Called by `nwarps` whole warps (warp index w).
+template <int XIN>
+__device__ __forceinline__ void quantize_rows_to_smem(const void* xin, int rows, int K,
+                                                      int8_t* xs, float* xds, int w, int nwarps,
+                                                      int lane) {
+  const int groups = rows * K / 8;  // fits: rows * K is bounded by MEMRA_MAX_X_BYTES
+  for (int base = w * 32; base < groups; base += nwarps * 32) {
+    const int g = base + lane;
+    const bool valid = g < groups;
+    float v[8];
+    if (valid) {
+      load_x_group<XIN>(xin, g, K, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+    float d;
+    const uint2 q = q8_1_group8(v, &d);
+    if (valid) {
+      *reinterpret_cast<uint2*>(xs + g * 8) = q;
+      if ((lane & 3) == 0) xds[g >> 2] = d;
+    }
+  }
+}
+
+template <int M, int R, int MODE, int XIN>
 __global__ void __launch_bounds__(kTmaThreads, 2) q8_tma_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[8] | empty[8] | xfull
@@ -244,11 +296,12 @@ __global__ void __launch_bounds__(kTmaThreads, 2) q8_tma_kernel(const Params p) 
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + 160);
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem + 160 + 16 * kMaxStages);
   float* s_gate = reinterpret_cast<float*>(s_ids + kMaxTopK);
-  const int8_t* xs = reinterpret_cast<const int8_t*>(smem + p.off_x);
-  const float* xds = reinterpret_cast<const float*>(smem + p.off_xd);
+  int8_t* xs = reinterpret_cast<int8_t*>(smem + p.off_x);
+  float* xds = reinterpret_cast<float*>(smem + p.off_xd);
   unsigned char* ring = smem + p.off_ring;
   float* part = reinterpret_cast<float*>(smem + p.off_part);
   float* yacc = reinterpret_cast<float*>(smem + p.off_yacc);
+  int* s_slice = reinterpret_cast<int*>(smem + p.off_slice);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -278,6 +331,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) q8_tma_kernel(const Params p) 
   if (MODE == kMoeGated) {
     for (int64_t i = threadIdx.x; i < u1 - u0; i += kTmaThreads) yacc[i] = 0.0f;
   }
+  fill_slice_table(s_slice, p.cpr, S, threadIdx.x, kTmaThreads);
   __syncthreads();
 
   const int nseg = num_segs<MODE>(p, u0, u1);
@@ -286,7 +340,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) q8_tma_kernel(const Params p) 
     // ------------------------------------------------------------ producer
     const uint64_t policy = l2_evict_first_policy();
     uint32_t issued = 0;
-    bool x_issued = false;
+    bool x_issued = XIN != kXq8;  // fused quantisation: the consumers build x themselves
     bool ok = true;
 
     auto issue_x = [&]() {
@@ -374,7 +428,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) q8_tma_kernel(const Params p) 
         while (!mbar_try_wait(full_bar(slot), (j / ns) & 1) && clock64() - t0 < (1ll << 30)) {
         }
       }
-      {
+      if (XIN == kXq8) {
         const long long t0 = clock64();
         while (!mbar_try_wait(xfull_bar, 0) && clock64() - t0 < (1ll << 30)) {
         }
@@ -395,8 +449,17 @@ __global__ void __launch_bounds__(kTmaThreads, 2) q8_tma_kernel(const Params p) 
     // ------------------------------------------------------------ consumers
     const int cw = warp - 1;
     const int h1 = (lane >> 2) & 1;  // which half this lane loads first
-    if (!mbar_wait(xfull_bar, 0, abort_flag)) return;
+    const int Ki = (int)p.K;
+    const bool last_ok = lane < nb - (p.cpr - 1) * 32;
+    if (XIN == kXq8) {
+      if (!mbar_wait(xfull_bar, 0, abort_flag)) return;
+    } else {
+      pdl_wait();  // the activation comes from the preceding kernel
+      quantize_rows_to_smem<XIN>(p.xin, p.xrows, (int)p.K, xs, xds, cw, kConsumerWarps, lane);
+      asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    }
     uint32_t it = 0;
+    uint32_t tbase = 0;  // tasks in all earlier stages: deals tasks round-robin over warps
     for (int si = 0; si < nseg; ++si) {
       const Seg g = get_seg<MODE>(p, u0, u1, si, s_ids);
       if (!g.valid) continue;
@@ -404,45 +467,59 @@ __global__ void __launch_bounds__(kTmaThreads, 2) q8_tma_kernel(const Params p) 
       for (int r0 = 0; r0 < g.nrows; r0 += p.rps) {
         const int nr = min(p.rps, g.nrows - r0);
         const int slot = it % ns;
+        const int groups = (nr + R - 1) / R;
+        const int ntasks = groups * S;
+        const int t0 = (int)((cw + kConsumerWarps - (int)(tbase % kConsumerWarps)) %
+                             kConsumerWarps);
+        tbase += ntasks;
+        // Every warp waits for every stage, tasks or not: an arrival on the stage's
+        // empty barrier must never run ahead of the stage itself.
         if (!mbar_wait(full_bar(slot), (it / ns) & 1, abort_flag)) return;
         const int8_t* ws = reinterpret_cast<const int8_t*>(ring + (size_t)slot * p.stage_bytes);
         const uint16_t* ds =
             reinterpret_cast<const uint16_t*>(ring + (size_t)slot * p.stage_bytes + p.wd_off);
         float* pp = part + (size_t)slot * p.rps * S * M;
-        const int groups = (nr + R - 1) / R;
-        const int ntasks = groups * S;
-        for (int t = cw; t < ntasks; t += kConsumerWarps) {
+        for (int t = t0; t < ntasks; t += kConsumerWarps) {
           const int gi = t / S;
           const int s = t - gi * S;
           const int rbase = gi * R;
-          const int plo = slice_begin(s, p.cpr, S);
-          const int phi = slice_begin(s + 1, p.cpr, S);
+          const int plo = s_slice[s];
+          const int phi = s_slice[s + 1];
+          // Per-lane pointers at the task's first block; a part is 1024 bytes on.
+          const int8_t* wl[R];
+          const uint16_t* dl[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            // Rows past the stage's end reuse a valid row; their sums are dropped.
+            const int row = rbase + r < nr ? rbase + r : rbase;
+            wl[r] = ws + row * Ki + (plo * 32 + lane) * 32 + h1 * 16;
+            dl[r] = ds + row * nb + plo * 32 + lane;
+          }
+          const int8_t* xl = xs + (size_t)xrow * Ki + (plo * 32 + lane) * 32 + h1 * 16;
+          const float* xdl = xds + (size_t)xrow * nb + plo * 32 + lane;
           float acc[R][M];
 #pragma unroll
           for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
           for (int pt = plo; pt < phi; ++pt) {
-            const int b = pt * 32 + lane;
-            if (b < nb) {
+            const int q = pt - plo;
+            if (pt < p.cpr - 1 || last_ok) {
               uint4 w0[R], w1[R];
               uint16_t dw[R];
 #pragma unroll
               for (int r = 0; r < R; ++r) {
-                // Rows past the stage's end reuse a valid row; their sums are dropped.
-                const int row = rbase + r < nr ? rbase + r : rbase;
-                const uint4* src = reinterpret_cast<const uint4*>(ws + (size_t)row * p.K + b * 32);
-                w0[r] = src[h1];
-                w1[r] = src[h1 ^ 1];
-                dw[r] = ds[(size_t)row * nb + b];
+                // The two halves in this lane quad's order (see the file comment).
+                w0[r] = *reinterpret_cast<const uint4*>(wl[r] + q * 1024);
+                w1[r] = *reinterpret_cast<const uint4*>(wl[r] + q * 1024 + 16 - 32 * h1);
+                dw[r] = dl[r][q * 32];
               }
 #pragma unroll
               for (int m = 0; m < M; ++m) {
-                const uint4* xsrc =
-                    reinterpret_cast<const uint4*>(xs + (size_t)(xrow + m) * p.K + b * 32);
-                const uint4 x0 = xsrc[h1];
-                const uint4 x1 = xsrc[h1 ^ 1];
-                const float dx = xds[(size_t)(xrow + m) * nb + b];
+                const int8_t* xm = xl + (size_t)m * Ki + q * 1024;
+                const uint4 x0 = *reinterpret_cast<const uint4*>(xm);
+                const uint4 x1 = *reinterpret_cast<const uint4*>(xm + 16 - 32 * h1);
+                const float dx = xdl[(size_t)m * nb + q * 32];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                   const int sb = dot_halves(w0[r], w1[r], x0, x1);
@@ -479,35 +556,135 @@ __host__ __device__ constexpr int reg_ctas_per_sm(int M) {
 }
 constexpr int kPartFloats = 8192;  // 32 KB of slice partials per tile
 
-template <int M, int R, int MODE>
+// Activation rows in shared memory for the register kernel: half-block planes
+// xs[row][half][block][16 bytes], so that lane-consecutive blocks read
+// consecutive 16-byte words (no bank conflicts) with the halves in register order.
+__device__ __forceinline__ int split_offset(int row, int byte, int nb) {
+  const int blk = byte >> 5;
+  const int h = (byte >> 4) & 1;
+  return ((row * 2 + h) * nb + blk) * 16 + (byte & 15);
+}
+
+template <int XIN>
+__device__ __forceinline__ void stage_x_split(const Params& p, int8_t* xs, float* xds, int w,
+                                              int nwarps, int lane, int tid, int nthreads) {
+  const int nb = p.nb;
+  // rows * K is bounded by MEMRA_MAX_X_BYTES, so 32-bit indices suffice.
+  const int K = (int)p.K;
+  if (XIN == kXq8) {
+    const int wpr = K / 16;  // 16-byte words per row
+    const int words = p.xrows * wpr;
+    for (int i = tid; i < words; i += nthreads) {
+      const int row = i / wpr;
+      const int j = i - row * wpr;
+      *reinterpret_cast<uint4*>(xs + split_offset(row, j * 16, nb)) =
+          reinterpret_cast<const uint4*>(p.xq)[i];
+    }
+    const int nd = p.xrows * nb;
+    for (int i = tid; i < nd; i += nthreads) xds[i] = p.xd[i];
+  } else {
+    // Quantise 8-value groups; a warp handles 2 groups per lane per round with both
+    // loads issued first (the prefetched weights still hold registers here).
+    constexpr int U = 2;
+    const int gpr = K / 8;
+    const int groups = p.xrows * gpr;
+    for (int base = w * 32 * U; base < groups; base += nwarps * 32 * U) {
+      float v[U][8];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int g = base + u * 32 + lane;
+        if (g < groups) {
+          load_x_group<XIN>(p.xin, g, K, v[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[u][i] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int g = base + u * 32 + lane;
+        float d;
+        const uint2 q = q8_1_group8(v[u], &d);
+        if (g < groups) {
+          const int row = g / gpr;
+          const int byte = (g - row * gpr) * 8;
+          *reinterpret_cast<uint2*>(xs + split_offset(row, byte, nb)) = q;
+          if ((lane & 3) == 0) xds[g >> 2] = d;
+        }
+      }
+    }
+  }
+}
+
+template <int M, int R, int MODE, int XIN>
 __global__ void __launch_bounds__(kRegThreads, reg_ctas_per_sm(M)) q8_reg_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nb = p.nb;
   const int S = p.S;
+  const int64_t K = p.K;
 
-  // Shared memory: xs | xds | partials | ids | gates.
+  // Shared memory: xs | xds | partials | ids | gates | slice table.
   int8_t* xs = reinterpret_cast<int8_t*>(smem);
   float* xds = reinterpret_cast<float*>(smem + p.off_xd);
   float* part = reinterpret_cast<float*>(smem + p.off_part);
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem + p.off_yacc);
   float* s_gate = reinterpret_cast<float*>(s_ids + kMaxTopK);
+  int* s_slice = reinterpret_cast<int*>(s_gate + kMaxTopK);
 
   const int64_t u0 = p.units * blockIdx.x / gridDim.x;
   const int64_t u1 = p.units * (blockIdx.x + 1) / gridDim.x;
+  // Lanes past the end of a row's last part hold no block.
+  const bool last_ok = lane < nb - (p.cpr - 1) * 32;
+
+  // Parts in groups of G: every load of a group is issued before its math.
+  constexpr int G = R >= 4 ? 1 : (R == 2 || MODE != kDense ? 2 : kSlicePartsMax);
+  Quants32 w[G][R];
+  uint16_t dw[G][R];
+
+  // wt/dt: this lane's first block of the task's first part in row rbase.
+  auto load_group = [&](const int8_t* wt, const uint16_t* dt, int q0, int npart, int plo,
+                        int rows_left) {
+#pragma unroll
+    for (int q = 0; q < G; ++q) {
+      const int pq = q0 + q;
+      const bool inb = pq < npart && (plo + pq < p.cpr - 1 || last_ok);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (inb && r < rows_left) {
+          w[q][r] = ld_stream_32B(wt + r * K + pq * 1024);
+          dw[q][r] = ld_stream_u16(dt + r * nb + pq * 32);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[q][r].w[i] = 0u;
+          dw[q][r] = 0;
+        }
+      }
+    }
+  };
 
   pdl_launch_dependents();
+  // Dense products stream weights that the preceding kernel does not write: the
+  // first group of this warp's first task is requested before waiting for it.
+  bool prefetched = false;
+  if (MODE == kDense) {
+    const int nr = (int)min((int64_t)p.tile_rows, u1 - u0);
+    if (warp < ((nr + R - 1) / R) * S) {
+      const int gi = warp / S;
+      const int s = warp - gi * S;
+      const int plo = (int)(((long long)s * p.cpr) / S);
+      const int phi = (int)(((long long)(s + 1) * p.cpr) / S);
+      const int64_t row = u0 + gi * R;
+      load_group(p.wq + row * K + (plo * 32 + lane) * 32, p.wd + row * nb + plo * 32 + lane, 0,
+                 phi - plo, plo, nr - gi * R);
+      prefetched = true;
+    }
+  }
+  fill_slice_table(s_slice, p.cpr, S, threadIdx.x, kRegThreads);
   pdl_wait();
   if (MODE != kDense) load_routing<MODE>(p, s_ids, s_gate, threadIdx.x, kRegThreads);
-  // Stage the activation rows.
-  {
-    const int64_t words = (int64_t)p.xrows * p.K / 16;
-    for (int64_t i = threadIdx.x; i < words; i += kRegThreads)
-      reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(p.xq)[i];
-    const int64_t nd = (int64_t)p.xrows * nb;
-    for (int64_t i = threadIdx.x; i < nd; i += kRegThreads) xds[i] = p.xd[i];
-  }
+  stage_x_split<XIN>(p, xs, xds, warp, kRegWarps, lane, threadIdx.x, kRegThreads);
   __syncthreads();
 
   const int nseg = num_segs<MODE>(p, u0, u1);
@@ -520,6 +697,9 @@ __global__ void __launch_bounds__(kRegThreads, reg_ctas_per_sm(M)) q8_reg_kernel
       continue;
     }
     const int xrow = (MODE == kDense) ? 0 : g.xrow;
+    const int8_t* xlo = xs + ((size_t)xrow * 2) * nb * 16 + lane * 16;       // half 0
+    const int8_t* xhi = xs + ((size_t)xrow * 2 + 1) * nb * 16 + lane * 16;   // half 1
+    const float* xdl = xds + (size_t)xrow * nb + lane;
     for (int r0 = 0; r0 < g.nrows; r0 += p.tile_rows) {
       const int nr = min(p.tile_rows, g.nrows - r0);
       const int groups = (nr + R - 1) / R;
@@ -528,46 +708,32 @@ __global__ void __launch_bounds__(kRegThreads, reg_ctas_per_sm(M)) q8_reg_kernel
         const int gi = t / S;
         const int s = t - gi * S;
         const int rbase = gi * R;
-        const int plo = slice_begin(s, p.cpr, S);
-        const int phi = slice_begin(s + 1, p.cpr, S);
+        const int plo = s_slice[s];
+        const int npart = s_slice[s + 1] - plo;
+        const int64_t row = g.row0 + r0 + rbase;
+        const int8_t* wt = p.wq + row * K + (plo * 32 + lane) * 32;
+        const uint16_t* dt = p.wd + row * nb + plo * 32 + lane;
         float acc[R][M];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
           for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
-        // Parts in groups of G: every load of a group is issued before its math.
-        constexpr int G = R >= 4 ? 1 : (R == 2 || MODE != kDense ? 2 : kSlicePartsMax);
-        for (int q0 = plo; q0 < phi; q0 += G) {
-          Quants32 w[G][R];
-          uint16_t dw[G][R];
-#pragma unroll
-          for (int q = 0; q < G; ++q) {
-            const int b = (q0 + q) * 32 + lane;
-            const bool inb = q0 + q < phi && b < nb;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-              if (inb && rbase + r < nr) {
-                const int64_t row = g.row0 + r0 + rbase + r;
-                w[q][r] = ld_stream_32B(p.wq + row * p.K + (int64_t)b * 32);
-                dw[q][r] = ld_stream_u16(p.wd + row * nb + b);
-              } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) w[q][r].w[i] = 0u;
-                dw[q][r] = 0;
-              }
-            }
+        for (int q0 = 0; q0 < npart; q0 += G) {
+          if (prefetched) {
+            prefetched = false;  // the prologue already requested this group
+          } else {
+            load_group(wt, dt, q0, npart, plo, nr - rbase);
           }
 #pragma unroll
           for (int q = 0; q < G; ++q) {
-            const int b = (q0 + q) * 32 + lane;
-            if (q0 + q < phi && b < nb) {
+            const int pq = q0 + q;
+            if (pq < npart && (plo + pq < p.cpr - 1 || last_ok)) {
+              const int off = (plo + pq) * 32;  // block index of lane 0
 #pragma unroll
               for (int m = 0; m < M; ++m) {
-                const uint4* xsrc = reinterpret_cast<const uint4*>(
-                    xs + (size_t)(xrow + m) * p.K + (size_t)b * 32);
-                const uint4 x0 = xsrc[0];
-                const uint4 x1 = xsrc[1];
-                const float dx = xds[(size_t)(xrow + m) * nb + b];
+                const uint4 x0 = *reinterpret_cast<const uint4*>(xlo + ((size_t)m * 2 * nb + off) * 16);
+                const uint4 x1 = *reinterpret_cast<const uint4*>(xhi + ((size_t)m * 2 * nb + off) * 16);
+                const float dx = xdl[(size_t)m * nb + off];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                   const uint4 w0 =
@@ -637,7 +803,7 @@ __global__ void __launch_bounds__(256)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr size_t kTmaStageTarget = 20 * 1024;
+constexpr size_t kTmaStageTarget = 28 * 1024;  // bulk copies below ~16 KB stream slower
 constexpr size_t kTmaRingBudget = 88 * 1024;
 constexpr size_t kTmaSmemPairLimit = 110 * 1024;  // two CTAs per SM (this + the next kernel)
 
@@ -654,12 +820,12 @@ bool force_tma_path() {
 
 int64_t max_units_per_cta(int64_t units, int64_t grid) { return (units + grid - 1) / grid; }
 
-template <int M, int R, int MODE>
+template <int M, int R, int MODE, int XIN>
 bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out) {
   if (!force_tma_path()) return false;
   if (p.K % 256 != 0) return false;
-  if (!aligned(p.wd, 16) || !aligned(p.xd, 16) || !aligned(p.xq, 16) || !aligned(p.wq, 16))
-    return false;
+  if (!aligned(p.wd, 16) || !aligned(p.wq, 16)) return false;
+  if (XIN == kXq8 && (!aligned(p.xd, 16) || !aligned(p.xq, 16))) return false;
   const size_t row_bytes = (size_t)p.K + (size_t)p.nb * 2;
   int rps = (int)std::max<size_t>(1, kTmaStageTarget / row_bytes);
   rps = std::max(R, rps / R * R);
@@ -668,7 +834,7 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
       align_up((size_t)p.xrows * p.K, 128) + align_up((size_t)p.xrows * p.nb * 4, 128);
   const int64_t maxu = max_units_per_cta(p.units, grid);
   const size_t yacc = MODE == kMoeGated ? align_up((size_t)maxu * 4, 16) : 0;
-  const size_t fixed = kHeaderBytes + xbytes + yacc;
+  const size_t fixed = kHeaderBytes + xbytes + yacc + align_up((size_t)(p.S + 1) * 4, 16);
   const size_t part_per_stage = align_up((size_t)rps * p.S * M * 4, 16);
   // Ring: up to the budget, and within the two-CTAs-per-SM limit when possible.
   size_t limit = std::max<size_t>(kTmaSmemPairLimit, fixed + 2 * (stage + part_per_stage));
@@ -690,11 +856,13 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   off += (size_t)ns * part_per_stage;
   p.off_yacc = (uint32_t)off;
   off += yacc;
+  p.off_slice = (uint32_t)off;
+  off += align_up((size_t)(p.S + 1) * 4, 16);
   *smem_out = off;
   return true;
 }
 
-template <int M, int R, int MODE>
+template <int M, int R, int MODE, int XIN>
 bool plan_reg(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out) {
   const int64_t maxu = max_units_per_cta(p.units, grid);
   int64_t tile;
@@ -711,7 +879,7 @@ bool plan_reg(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   p.off_xd = (uint32_t)xb;
   p.off_part = (uint32_t)(xb + db);
   p.off_yacc = (uint32_t)(xb + db + pb);
-  const size_t total = xb + db + pb + 2 * kMaxTopK * 4;
+  const size_t total = xb + db + pb + 2 * kMaxTopK * 4 + align_up((size_t)(p.S + 1) * 4, 16);
   if (total > (size_t)info.max_smem_optin) return false;
   *smem_out = total;
   return true;
@@ -730,7 +898,7 @@ memra_status launch(Kern kernel, int64_t grid, int threads, size_t smem, cudaStr
   return MEMRA_OK;
 }
 
-template <int M, int R, int MODE>
+template <int M, int R, int MODE, int XIN>
 memra_status run_product(Params p, cudaStream_t stream) {
   DeviceInfo info;
   if (!device_info(&info)) return MEMRA_ERR_CUDA;
@@ -740,25 +908,25 @@ memra_status run_product(Params p, cudaStream_t stream) {
   // One CTA per SM for the TMA kernel.
   int64_t grid = std::min<int64_t>(p.units, info.sms);
   size_t smem = 0;
-  if (plan_tma<M, R, MODE>(p, info, grid, &smem))
-    return launch(q8_tma_kernel<M, R, MODE>, grid, kTmaThreads, smem, stream, p);
+  if (plan_tma<M, R, MODE, XIN>(p, info, grid, &smem))
+    return launch(q8_tma_kernel<M, R, MODE, XIN>, grid, kTmaThreads, smem, stream, p);
   grid = std::min<int64_t>(p.units, (int64_t)info.sms * reg_ctas_per_sm(M));
-  if (plan_reg<M, R, MODE>(p, info, grid, &smem))
-    return launch(q8_reg_kernel<M, R, MODE>, grid, kRegThreads, smem, stream, p);
+  if (plan_reg<M, R, MODE, XIN>(p, info, grid, &smem))
+    return launch(q8_reg_kernel<M, R, MODE, XIN>, grid, kRegThreads, smem, stream, p);
   return MEMRA_ERR_UNSUPPORTED;
 }
 
-template <int MODE>
+template <int MODE, int XIN>
 memra_status dispatch_m(const Params& p, int M, cudaStream_t s) {
   switch (M) {
-    case 1: return run_product<1, 1, MODE>(p, s);
-    case 2: return run_product<2, 1, MODE>(p, s);
-    case 3: return run_product<3, 1, MODE>(p, s);
-    case 4: return run_product<4, 2, MODE>(p, s);
-    case 5: return run_product<5, 2, MODE>(p, s);
-    case 6: return run_product<6, 2, MODE>(p, s);
-    case 7: return run_product<7, 2, MODE>(p, s);
-    case 8: return run_product<8, 4, MODE>(p, s);
+    case 1: return run_product<1, 1, MODE, XIN>(p, s);
+    case 2: return run_product<2, 1, MODE, XIN>(p, s);
+    case 3: return run_product<3, 1, MODE, XIN>(p, s);
+    case 4: return run_product<4, 2, MODE, XIN>(p, s);
+    case 5: return run_product<5, 2, MODE, XIN>(p, s);
+    case 6: return run_product<6, 2, MODE, XIN>(p, s);
+    case 7: return run_product<7, 2, MODE, XIN>(p, s);
+    case 8: return run_product<8, 4, MODE, XIN>(p, s);
   }
   return MEMRA_ERR_UNSUPPORTED;
 }
@@ -803,13 +971,40 @@ extern "C" memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t
   p.xrows = (int)M;
   p.y = y;
   p.units = N;
-  return dispatch_m<kDense>(p, (int)M, stream);
+  return dispatch_m<kDense, kXq8>(p, (int)M, stream);
 }
 
 extern "C" memra_status memra_q8_0_gemv(const int8_t* wq, const uint16_t* wd, int64_t N, int64_t K,
                                         const int8_t* xq, const float* xd, float* y,
                                         cudaStream_t stream) {
   return memra_q8_0_gemm_small_m(wq, wd, N, K, 1, xq, xd, y, stream);
+}
+
+extern "C" memra_status memra_q8_0_quant_gemm(const int8_t* wq, const uint16_t* wd, int64_t N,
+                                              int64_t K, int64_t M, const void* x, int32_t dtype,
+                                              float* y, cudaStream_t stream) {
+  if (N < 0 || K < 0 || M < 0 || K % 32 != 0) return MEMRA_ERR_INVALID_ARG;
+  if (dtype != MEMRA_BF16 && dtype != MEMRA_F32) return MEMRA_ERR_INVALID_ARG;
+  if (M > MEMRA_MAX_M) return MEMRA_ERR_UNSUPPORTED;
+  if (N > INT32_MAX || K > INT32_MAX) return MEMRA_ERR_UNSUPPORTED;
+  if (N == 0 || M == 0) return MEMRA_OK;
+  if (!y) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(y, 4)) return MEMRA_ERR_ALIGNMENT;
+  if (K == 0) return zero_fill(y, M * N, stream);
+  if (!wq || !wd || !x) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(wq, 32) || !aligned(wd, 2) || !aligned(x, 16)) return MEMRA_ERR_ALIGNMENT;
+  if (!x_fits(M, K)) return MEMRA_ERR_UNSUPPORTED;
+  Params p{};
+  p.wq = wq;
+  p.wd = wd;
+  p.N = N;
+  p.K = K;
+  p.xin = x;
+  p.xrows = (int)M;
+  p.y = y;
+  p.units = N;
+  if (dtype == MEMRA_BF16) return dispatch_m<kDense, kXbf16>(p, (int)M, stream);
+  return dispatch_m<kDense, kXf32>(p, (int)M, stream);
 }
 
 extern "C" memra_status memra_q8_0_moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank,
@@ -849,10 +1044,69 @@ extern "C" memra_status memra_q8_0_moe_gemv(const int8_t* wq_bank, const uint16_
   p.status = dev_status;
   if (gate_w) {
     p.units = N;
-    return run_product<1, 1, kMoeGated>(p, stream);
+    return run_product<1, 1, kMoeGated, kXq8>(p, stream);
   }
   p.units = top_k * N;
-  return run_product<1, 1, kMoeUngated>(p, stream);
+  return run_product<1, 1, kMoeUngated, kXq8>(p, stream);
+}
+
+extern "C" memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* gu_d,
+                                           const int8_t* dn_q, const uint16_t* dn_d, int64_t E,
+                                           int64_t H, int64_t F, const int32_t* ids,
+                                           const float* gate_w, int64_t top_k, const void* x,
+                                           int32_t dtype, float* y, float* workspace,
+                                           int32_t* dev_status, cudaStream_t stream) {
+  if (E < 1 || H < 0 || F < 0 || H % 32 != 0 || F % 32 != 0 || top_k < 1)
+    return MEMRA_ERR_INVALID_ARG;
+  if (dtype != MEMRA_BF16 && dtype != MEMRA_F32) return MEMRA_ERR_INVALID_ARG;
+  if (top_k > MEMRA_MAX_TOP_K) return MEMRA_ERR_UNSUPPORTED;
+  if (H > INT32_MAX / 2 || F > INT32_MAX / 2 || E > INT32_MAX) return MEMRA_ERR_UNSUPPORTED;
+  if (H == 0) return MEMRA_OK;
+  if (!y || !ids || !gate_w) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(y, 4) || !aligned(ids, 4) || !aligned(gate_w, 4) ||
+      (dev_status && !aligned(dev_status, 4)))
+    return MEMRA_ERR_ALIGNMENT;
+  if (F == 0) return zero_fill(y, H, stream);
+  if (!gu_q || !gu_d || !dn_q || !dn_d || !x || !workspace) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(gu_q, 32) || !aligned(gu_d, 2) || !aligned(dn_q, 32) || !aligned(dn_d, 2) ||
+      !aligned(x, 16) || !aligned(workspace, 16))
+    return MEMRA_ERR_ALIGNMENT;
+  if (!x_fits(1, H) || !x_fits(top_k, F)) return MEMRA_ERR_UNSUPPORTED;
+  // gate|up rows of every selected expert: workspace[k][0, 2F) = W_gu[ids[k]] x.
+  Params a{};
+  a.wq = gu_q;
+  a.wd = gu_d;
+  a.N = 2 * F;
+  a.K = H;
+  a.xin = x;
+  a.xrows = 1;
+  a.y = workspace;
+  a.ids = ids;
+  a.top_k = (int)top_k;
+  a.E = E;
+  a.xpe = 0;
+  a.status = dev_status;
+  a.units = top_k * 2 * F;
+  memra_status st = dtype == MEMRA_BF16 ? run_product<1, 1, kMoeUngated, kXbf16>(a, stream)
+                                        : run_product<1, 1, kMoeUngated, kXf32>(a, stream);
+  if (st != MEMRA_OK) return st;
+  // down rows with SwiGLU + q8_1 of each expert's gate|up row in the prologue.
+  Params b{};
+  b.wq = dn_q;
+  b.wd = dn_d;
+  b.N = H;
+  b.K = F;
+  b.xin = workspace;
+  b.xrows = (int)top_k;
+  b.y = y;
+  b.ids = ids;
+  b.gate_w = gate_w;
+  b.top_k = (int)top_k;
+  b.E = E;
+  b.xpe = 1;
+  b.status = dev_status;
+  b.units = H;
+  return run_product<1, 1, kMoeGated, kXswiglu>(b, stream);
 }
 
 extern "C" memra_status memra_q8_0_block_dots(const int8_t* wq, int64_t N, int64_t K,

@@ -14,22 +14,8 @@ namespace {
 
 constexpr int kQuantThreads = 256;
 
-__device__ __forceinline__ void load8(const float* p, float v[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-
-__device__ __forceinline__ void load8(const uint16_t* p, float v[8]) {
-  const uint4 a = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);             // bf16 -> fp32 is exact
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
+__device__ __forceinline__ void load8(const float* p, float v[8]) { load8_f32(p, v); }
+__device__ __forceinline__ void load8(const uint16_t* p, float v[8]) { load8_bf16(p, v); }
 
 __device__ __forceinline__ float group4_amax(const float v[8]) {
   float a = 0.0f;
@@ -40,14 +26,6 @@ __device__ __forceinline__ float group4_amax(const float v[8]) {
   return a;
 }
 
-__device__ __forceinline__ uint2 quant8(const float v[8], float d) {
-  uint2 r;
-  r.x = pack4(quant_value(v[0], d), quant_value(v[1], d), quant_value(v[2], d),
-              quant_value(v[3], d));
-  r.y = pack4(quant_value(v[4], d), quant_value(v[5], d), quant_value(v[6], d),
-              quant_value(v[7], d));
-  return r;
-}
 
 // Activations: d = amax / 127 in fp32.  T = float or uint16_t (bf16 bits).
 template <typename T>
@@ -69,9 +47,8 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = 0.0f;
     }
-    const float amax = group4_amax(v);
-    const float dv = amax / 127.0f;
-    const uint2 packed = quant8(v, dv);
+    float dv;
+    const uint2 packed = q8_1_group8(v, &dv);
     if (valid) {
       *reinterpret_cast<uint2*>(q + g * 8) = packed;
       if ((lane & 3) == 0) d[g >> 2] = dv;
@@ -102,35 +79,17 @@ __global__ void __launch_bounds__(kQuantThreads)
     const float amax = group4_amax(v);
     const __half d16 = __float2half_rn(amax / 127.0f);
     const float dv = __half2float(d16);
-    const uint2 packed = quant8(v, dv);
+    const float inv = dv == 0.0f ? 0.0f : 1.0f / dv;
+    int qv[8];
+    quant8_fast(v, dv, inv, qv);
+    uint2 packed;
+    packed.x = pack4(qv[0], qv[1], qv[2], qv[3]);
+    packed.y = pack4(qv[4], qv[5], qv[6], qv[7]);
     if (valid) {
       *reinterpret_cast<uint2*>(q + g * 8) = packed;
       if ((lane & 3) == 0) d[g >> 2] = __half_as_ushort(d16);
     }
   }
-}
-
-// exp by Cody & Waite's range reduction ("Software Manual for the Elementary
-// Functions", 1980) and a degree-7 Taylor polynomial: k = rint(x log2 e),
-// r = (x - k*C1) - k*C2 with C1 = 0.693359375 (exact product with k) and C2 =
-// ln 2 - C1, p = sum_{i<=7} r^i / i! in Horner form, result p * 2^k.  Every
-// operation is an explicitly rounded fp32 operation (no contraction), and the
-// argument is clamped to [-87, 88] so 2^k is a normal number.
-__device__ __forceinline__ float exp_cody_waite(float x) {
-  x = fminf(fmaxf(x, -87.0f), 88.0f);
-  const float kf = rintf(__fmul_rn(x, 1.44269504088896341f));
-  float r = __fsub_rn(x, __fmul_rn(kf, 0.693359375f));
-  r = __fsub_rn(r, __fmul_rn(kf, -2.12194440e-4f));
-  float p = 1.0f / 5040.0f;
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 720.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 120.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 24.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 6.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-  const int k = (int)kf;
-  return __fmul_rn(p, __int_as_float((k + 127) << 23));
 }
 
 // h = (g / (1 + exp(-g))) * u, one rounding per operation, then q8_1 of h.
@@ -152,22 +111,13 @@ __global__ void __launch_bounds__(kQuantThreads)
     if (valid) {
       const int64_t r = g / gpr;
       const int64_t f0 = (g - r * gpr) * 8;
-      float gv[8], uv[8];
-      load8(gu + r * 2 * F + f0, gv);
-      load8(gu + r * 2 * F + F + f0, uv);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float den = __fadd_rn(1.0f, exp_cody_waite(-gv[i]));
-        const float sg = __fdiv_rn(gv[i], den);
-        h[i] = __fmul_rn(sg, uv[i]);
-      }
+      swiglu8(gu + r * 2 * F + f0, gu + r * 2 * F + F + f0, h);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) h[i] = 0.0f;
     }
-    const float amax = group4_amax(h);
-    const float dv = amax / 127.0f;
-    const uint2 packed = quant8(h, dv);
+    float dv;
+    const uint2 packed = q8_1_group8(h, &dv);
     if (valid) {
       *reinterpret_cast<uint2*>(q + g * 8) = packed;
       if ((lane & 3) == 0) d[g >> 2] = dv;

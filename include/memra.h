@@ -110,6 +110,20 @@ memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t* wd, int64
                                      cudaStream_t stream);
 
 /*
+ * The verify GEMM (or, with M = 1, the decode GEMV) with the activation's q8_1
+ * quantisation done in the kernel's prologue: each CTA quantises x [M][K] (bf16
+ * bits or fp32, 16-byte aligned) into on-chip memory while the weight stream is
+ * already in flight, instead of a separate memra_quantize_q8_1 launch.  This is
+ * the pages' m=1 fusion chain applied to the quantise-then-matvec pair (memra
+ * performance, "Serving performance": the B=1 decode path that keeps the m=1
+ * fusion chain).  Bit-identical to
+ * memra_quantize_q8_1 followed by memra_q8_0_gemm_small_m.  y fp32 [M][N].
+ */
+memra_status memra_q8_0_quant_gemm(const int8_t* wq, const uint16_t* wd, int64_t N, int64_t K,
+                                   int64_t M, const void* x, int32_t dtype, float* y,
+                                   cudaStream_t stream);
+
+/*
  * Routed-expert GEMV for one token (memra wiki, feature list: MoE routed experts).
  * Bank: wq_bank [E][N][K], wd_bank [E][N][K/32] (expert e's planes are the slices
  * at e*N*K and e*N*(K/32)).  ids: device int32 [top_k]; gate_w: device fp32
@@ -142,6 +156,28 @@ memra_status memra_q8_0_moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank,
  */
 memra_status memra_swiglu_quantize_q8_1(const float* gu, int64_t R, int64_t F, int8_t* hq,
                                         float* hd, cudaStream_t stream);
+
+/*
+ * One routed-expert FFN layer for one token, in two kernels:
+ *   y = sum_k gate_w[k] * W_dn[ids[k]] q8_1( swiglu( W_gu[ids[k]] q8_1(x) ) ),
+ * with the gate|up product quantising x in its prologue and the down product
+ * computing SwiGLU and its q8_1 quantisation of each expert's gate|up row in its
+ * own prologue (the same arithmetic as memra_swiglu_quantize_q8_1).  Bit-identical
+ * to memra_quantize_q8_1, memra_q8_0_moe_gemv (no gate weights, shared x),
+ * memra_swiglu_quantize_q8_1 and memra_q8_0_moe_gemv (gate weights, x per expert)
+ * run in sequence.
+ *   gu_q [E][2F][H], gu_d [E][2F][H/32]: gate rows [0, F), up rows [F, 2F).
+ *   dn_q [E][H][F], dn_d [E][H][F/32].  x [H] (dtype bf16 bits or fp32, 16-byte
+ *   aligned).  ids, gate_w [top_k] (device).  y fp32 [H].
+ *   workspace: caller-allocated device fp32 [top_k][2F], 16-byte aligned; it holds
+ *   the gate|up outputs between the two kernels and keeps them after the call.
+ * Bad ids behave as in memra_q8_0_moe_gemv.  H % 32 == 0, F % 32 == 0.
+ */
+memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* gu_d, const int8_t* dn_q,
+                                const uint16_t* dn_d, int64_t E, int64_t H, int64_t F,
+                                const int32_t* ids, const float* gate_w, int64_t top_k,
+                                const void* x, int32_t dtype, float* y, float* workspace,
+                                int32_t* dev_status, cudaStream_t stream);
 
 /*
  * Exact int32 block sums s[m][n][b] = sum_{i<32} wq[n][32b+i] * xq[m][32b+i],

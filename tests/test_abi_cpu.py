@@ -66,6 +66,16 @@ def test_gemv_argument_errors(L):
     assert L.memra_q8_0_gemv(A256, A256, 64, 33, A256, A256, A256, None) == 1
 
 
+def test_fused_argument_errors(L):
+    f = L.memra_q8_0_quant_gemm
+    assert f(A256, A256, 64, 48, 1, A256, 0, A256, None) == 1       # K % 32
+    assert f(A256, A256, 64, 64, 1, A256, 5, A256, None) == 1       # dtype
+    assert f(A256, A256, 64, 64, 9, A256, 0, A256, None) == 3       # M > 8
+    assert f(A256, A256, 64, 64, 1, A256 + 8, 0, A256, None) == 2   # x not 16-aligned
+    assert f(A256 + 16, A256, 64, 64, 1, A256, 0, A256, None) == 2  # wq not 32-aligned
+    assert f(None, None, 0, 64, 1, None, 0, None, None) == 0
+
+
 def test_quantizer_argument_errors(L):
     assert L.memra_quantize_q8_1(A256, 0, 2, 40, A256, A256, None) == 1   # K % 32
     assert L.memra_quantize_q8_1(A256, 7, 2, 64, A256, A256, None) == 1   # bad dtype

@@ -318,3 +318,105 @@ def test_misaligned_views_are_rejected(mem):
                                     torch.zeros((9, K), dtype=torch.int8, device=dev),
                                     torch.zeros((9, K // 32), dtype=torch.float32, device=dev))
     assert ei.value.status == 3
+
+
+# ----------------------------------------------------------------------------
+# Quantisation fused into the product's prologue.
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("N,K,M", [(1003, 1184, 1), (4096, 4096, 1), (257, 17408, 1),
+                                   (513, 5120, 3), (130, 768, 8), (64, 32, 2)])
+def test_fused_quant_gemm_matches_two_step(mem, orc, dtype, N, K, M):
+    w = synth.weights_fp32(N, K, 80, N, K)
+    x = synth.activations_fp32(M, K, 81, N, K, M, outlier_frac=0.001).to(dtype).cuda()
+    wq, wd = mem.memra_quantize_q8_0(w.cuda())
+    xq, xd = mem.memra_quantize_q8_1(x)
+    y2 = mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd)
+    y = Guarded((M, N), torch.float32)
+    mem.memra_q8_0_quant_gemm(wq, wd, x, y=y.view)
+    torch.cuda.synchronize()
+    assert y.intact()
+    assert torch.equal(y.view.view(torch.int32), y2.view(torch.int32))
+    # and against the oracle's own pipeline
+    oq, od = orc.quantize_q8_0(np_(w))
+    xo = bf16_bits_np(x.cpu()) if dtype == torch.bfloat16 else np_(x)
+    oxq, oxd = orc.quantize_q8_1(xo)
+    assert_within(np_(y.view), orc.gemm(oq, od, oxq, oxd),
+                  abs_terms(orc.block_dots(oq, oxq), od, oxd), "fused N=%d K=%d M=%d" % (N, K, M))
+
+
+@pytest.mark.parametrize("scale", [0.1, 1.0 / 3.0, 7.77e-3, 3.3e4])
+def test_quantizers_near_rounding_boundaries(mem, orc, scale):
+    """Values within +-3e-5 (and just outside 1e-4) of k + 1/2 quanta, where a
+    quotient computed by reciprocal could round differently from the IEEE one."""
+    rng = np.random.default_rng(int(scale * 1e6) % 1000)
+    d = np.float32(scale)
+    blocks = []
+    for eps in (-2e-4, -3e-5, -1e-6, 0.0, 1e-6, 3e-5, 2e-4):
+        k = rng.integers(-126, 126, size=31)
+        v = ((k + 0.5 + eps) * np.float64(d)).astype(np.float32)
+        blocks.append(np.concatenate([[np.float32(127.0) * d], v]))   # max sets d = 127*d/127
+    x = np.stack(blocks).astype(np.float32).reshape(1, -1)
+    xt = torch.from_numpy(x).cuda()
+    xq, xd = mem.memra_quantize_q8_1(xt)
+    oq, od = orc.quantize_q8_1(x)
+    assert np.array_equal(np_(xq), oq)
+    assert np.array_equal(np_(xd).view(np.uint32), od.view(np.uint32))
+    # the fused product quantises the same way
+    wq, wd = mem.memra_quantize_q8_0(torch.from_numpy(x).repeat(3, 1).cuda())
+    y1 = mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd)
+    y2 = mem.memra_q8_0_quant_gemm(wq, wd, xt)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    # weights: fp16 scales, same construction
+    owq, owd = orc.quantize_q8_0(np.repeat(x, 3, axis=0))
+    assert np.array_equal(np_(wq), owq)
+    assert np.array_equal(wd_bits(wd), owd)
+
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("E,H,F,top_k", [(16, 2048, 768, 8), (5, 256, 96, 3), (3, 512, 32, 1)])
+def test_moe_ffn_matches_four_step_pipeline(mem, orc, dtype, E, H, F, top_k):
+    """The two-kernel FFN entry point against the four calls it fuses (bit for bit),
+    and against the oracle's layer."""
+    _, gq, gd = make_bank(mem, E, 2 * F, H, 90 + H)
+    _, dq, dd = make_bank(mem, E, H, F, 91 + F)
+    ids, gw = synth.routing(E, top_k, 92, E, H)
+    ids, gw = ids.cuda(), gw.cuda()
+    x = synth.normal((H,), 93, H).to(dtype).cuda()
+    st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.full((top_k, 2 * F), 5.0, device="cuda")
+    y = mem.memra_q8_0_moe_ffn(gq, gd, dq, dd, ids, gw, x, workspace=ws, dev_status=st1)
+    xq, xd = mem.memra_quantize_q8_1(x[None])
+    ygu = mem.memra_q8_0_moe_gemv(gq, gd, ids, None, xq[0], xd[0], False)
+    hq, hd = mem.memra_swiglu_quantize_q8_1(ygu)
+    y4 = mem.memra_q8_0_moe_gemv(dq, dd, ids, gw, hq, hd, True)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == 0
+    assert torch.equal(ws.view(torch.int32), ygu.view(torch.int32))
+    assert torch.equal(y.view(torch.int32), y4.view(torch.int32))
+    xo = bf16_bits_np(x.cpu()) if dtype == torch.bfloat16 else np_(x)
+    oxq, oxd = orc.quantize_q8_1(xo[None])
+    assert np.array_equal(np_(xq), oxq)
+    ygu_ref, _ = orc.moe_gemv(np_(gq), wd_bits(gd), np_(ids), None, oxq, oxd, 0)
+    ohq, ohd = orc.swiglu_quantize_q8_1(ygu_ref)
+    y_ref, bad = orc.moe_gemv(np_(dq), wd_bits(dd), np_(ids), np_(gw), ohq, ohd, 1)
+    assert bad == 0
+    err = np.abs(np_(y).astype(np.float64) - y_ref)
+    assert np.all(err <= 0.02 * np.abs(y_ref).max() + 1e-5)
+
+
+def test_moe_ffn_bad_ids(mem):
+    E, H, F = 4, 256, 64
+    _, gq, gd = make_bank(mem, E, 2 * F, H, 94)
+    _, dq, dd = make_bank(mem, E, H, F, 95)
+    ids = torch.tensor([1, 9], dtype=torch.int32, device="cuda")
+    gw = torch.tensor([0.6, 0.4], device="cuda")
+    x = synth.normal((H,), 96).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = mem.memra_q8_0_moe_ffn(gq, gd, dq, dd, ids, gw, x, dev_status=st)
+    y1 = mem.memra_q8_0_moe_ffn(gq, gd, dq, dd, ids[:1].contiguous(), gw[:1].contiguous(), x)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 1
+    assert torch.equal(y.view(torch.int32), y1.view(torch.int32))

@@ -25,6 +25,7 @@ for (N, K, M) in [(1003, 4096, 1), (777, 5120, 1), (513, 2048, 4), (300, 5120, 8
     wq, wd = mem.memra_quantize_q8_0(w)
     xq, xd = mem.memra_quantize_q8_1(x)
     out["d%%d_%%d_%%d" %% (N, K, M)] = mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd).cpu()
+    out["f%%d_%%d_%%d" %% (N, K, M)] = mem.memra_q8_0_quant_gemm(wq, wd, x).cpu()
 E, N, K, k = 10, 300, 768, 4
 wb = synth.weights_fp32(E * N, K, 72, device="cuda")
 bq, bd = mem.memra_quantize_q8_0(wb)
