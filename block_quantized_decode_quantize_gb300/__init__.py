@@ -24,6 +24,7 @@ MEMRA_BF16 = 0
 MEMRA_F32 = 1
 MAX_M = 8
 MAX_TOP_K = 64
+MOE_NOALLOC_SCRATCH_FLOATS = 65536
 
 _STATUS = {0: "MEMRA_OK", 1: "MEMRA_ERR_INVALID_ARG", 2: "MEMRA_ERR_ALIGNMENT",
            3: "MEMRA_ERR_UNSUPPORTED", 4: "MEMRA_ERR_CUDA"}
@@ -55,6 +56,8 @@ _SIGS = {
     "memra_swiglu_quantize_q8_1": [_p, _i64, _i64, _p, _p, _p],
     "memra_q8_0_moe_ffn": [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _i32, _p, _p, _p,
                            _p],
+    "memra_q8_0_moe_ffn_noalloc": [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _i32, _p,
+                                   _p, _p],
     "memra_q8_0_block_dots": [_p, _i64, _i64, _p, _i64, _p, _p],
 }
 
@@ -286,6 +289,40 @@ def memra_q8_0_moe_ffn(gu_q, gu_d, dn_q, dn_d, ids, gate_w, x, y=None, workspace
                lib().memra_q8_0_moe_ffn(_ptr(gu_q), _ptr(gu_d), _ptr(dn_q), _ptr(dn_d), E, H, F,
                                         _ptr(ids), _ptr(gate_w), top_k, _ptr(x), dt, _ptr(y),
                                         _ptr(workspace), _ptr(dev_status), _stream(gu_q)))
+    return y
+
+
+def memra_q8_0_moe_ffn_noalloc(gu_q, gu_d, dn_q, dn_d, ids, gate_w, x, y, dev_status=None):
+    """memra_q8_0_moe_ffn with the gate|up workspace inside the library: the C call
+    allocates no device memory (the caller provides y).  For callers that cannot
+    allocate at call time; top_k * 2F must not exceed MOE_NOALLOC_SCRATCH_FLOATS.
+    The first call on a device should come before any stream capture; calls that
+    overlap on the GPU share one scratch array and race."""
+    _need(gu_q, "gu_q", torch.int8)
+    E, F2, H = gu_q.shape
+    F = F2 // 2
+    dev = gu_q.device
+    _need(gu_d, "gu_d", torch.float16, dev, (E, F2, H // 32))
+    _need(dn_q, "dn_q", torch.int8, dev, (E, H, F))
+    _need(dn_d, "dn_d", torch.float16, dev, (E, H, F // 32))
+    _need(ids, "ids", torch.int32, dev)
+    top_k = ids.shape[0]
+    _need(gate_w, "gate_w", torch.float32, dev, (top_k,))
+    if x.dtype == torch.bfloat16:
+        dt = MEMRA_BF16
+    elif x.dtype == torch.float32:
+        dt = MEMRA_F32
+    else:
+        raise TypeError("x must be bfloat16 or float32")
+    _need(x, "x", x.dtype, dev, (H,))
+    _need(y, "y", torch.float32, dev, (H,))
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    with torch.cuda.device(dev):
+        _check("memra_q8_0_moe_ffn_noalloc",
+               lib().memra_q8_0_moe_ffn_noalloc(_ptr(gu_q), _ptr(gu_d), _ptr(dn_q), _ptr(dn_d), E,
+                                                H, F, _ptr(ids), _ptr(gate_w), top_k, _ptr(x),
+                                                dt, _ptr(y), _ptr(dev_status), _stream(gu_q)))
     return y
 
 

@@ -33,6 +33,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -1107,6 +1108,61 @@ extern "C" memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* g
   b.status = dev_status;
   b.units = H;
   return run_product<1, 1, kMoeGated, kXswiglu>(b, stream);
+}
+
+// ----------------------------------------------------------------------------
+// memra_q8_0_moe_ffn_noalloc: the routed FFN with its gate|up workspace in a
+// fixed device array owned by this library instead of caller memory.
+// ----------------------------------------------------------------------------
+
+// The array lives on every GPU that loads the library, until the process exits.
+static __device__ __align__(256) float g_moe_ffn_scratch[MEMRA_MOE_NOALLOC_SCRATCH_FLOATS];
+
+namespace memra {
+namespace {
+constexpr int kScratchDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_addr[kScratchDevices] = {};
+
+// The scratch array's device address on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+memra_status moe_scratch_address(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kScratchDevices) return MEMRA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_moe_ffn_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_scratch_addr[dev] = static_cast<float*>(ptr);
+  }
+  *out = g_scratch_addr[dev];
+  return MEMRA_OK;
+}
+}  // namespace
+}  // namespace memra
+
+extern "C" memra_status memra_q8_0_moe_ffn_noalloc(const int8_t* gu_q, const uint16_t* gu_d,
+                                                   const int8_t* dn_q, const uint16_t* dn_d,
+                                                   int64_t E, int64_t H, int64_t F,
+                                                   const int32_t* ids, const float* gate_w,
+                                                   int64_t top_k, const void* x, int32_t dtype,
+                                                   float* y, int32_t* dev_status,
+                                                   cudaStream_t stream) {
+  if (top_k >= 1 && F >= 0 && top_k * 2 * F > MEMRA_MOE_NOALLOC_SCRATCH_FLOATS)
+    return MEMRA_ERR_UNSUPPORTED;
+  float* ws = nullptr;
+  if (H > 0 && F > 0 && top_k >= 1) {
+    const memra_status st = memra::moe_scratch_address(&ws);
+    if (st != MEMRA_OK) return st;
+  }
+  // Same checks and kernels as the workspace entry point.  Calls that return before
+  // launching (empty or invalid sizes) never look at the workspace pointer.
+  return memra_q8_0_moe_ffn(gu_q, gu_d, dn_q, dn_d, E, H, F, ids, gate_w, top_k, x, dtype, y,
+                            ws, dev_status, stream);
 }
 
 extern "C" memra_status memra_q8_0_block_dots(const int8_t* wq, int64_t N, int64_t K,

@@ -180,6 +180,36 @@ memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* gu_d, const 
                                 int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * memra_q8_0_moe_ffn without caller memory.  The pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory when they call
+ * -- code running under a fixed memory arena or budget, plug-ins and embedded
+ * runtimes that are handed device pointers but no allocator, and real-time decode
+ * loops that must not pay for (or risk failing) an allocation per layer.  It takes
+ * the same arguments minus `workspace` and returns bit-identical results.
+ *
+ * The gate|up outputs go to a fixed array of MEMRA_MOE_NOALLOC_SCRATCH_FLOATS
+ * floats (256 KB) inside the library, which every GPU that loads the library holds
+ * until the process exits.  Calls whose top_k * 2F exceeds that size return
+ * MEMRA_ERR_UNSUPPORTED and launch nothing.  The call itself allocates nothing
+ * (no cudaMalloc, no library allocation).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before
+ *     any stream capture on the device.
+ *   - Every call shares the one array.  Calls that may overlap on the GPU (on
+ *     different streams, or before an earlier one has finished on another stream)
+ *     race on it; keep such calls on one stream.  The array keeps the last call's
+ *     gate|up outputs; nothing in it needs clearing because each call writes every
+ *     element it later reads.
+ */
+#define MEMRA_MOE_NOALLOC_SCRATCH_FLOATS 65536
+memra_status memra_q8_0_moe_ffn_noalloc(const int8_t* gu_q, const uint16_t* gu_d,
+                                        const int8_t* dn_q, const uint16_t* dn_d, int64_t E,
+                                        int64_t H, int64_t F, const int32_t* ids,
+                                        const float* gate_w, int64_t top_k, const void* x,
+                                        int32_t dtype, float* y, int32_t* dev_status,
+                                        cudaStream_t stream);
+
+/*
  * Exact int32 block sums s[m][n][b] = sum_{i<32} wq[n][32b+i] * xq[m][32b+i],
  * computed with the same dp4a block-dot routine as the product kernels.  For
  * verification of the integer stage.  s: int32 [M][N][K/32], 4-byte aligned.
