@@ -474,7 +474,10 @@ def run_memra(args):
     barrier(world)
     mem.lib()
 
-    wl = Workload(args.workload, mem, device, layers=args.layers, fused=args.fused)
+    # Dense products quantise with a separate launch unless --fused; the routed FFN
+    # uses its two-kernel entry point unless --unfused.
+    fused = (not args.unfused) if args.workload == "moe_top8" else args.fused
+    wl = Workload(args.workload, mem, device, layers=args.layers, fused=fused)
     stream = torch.cuda.Stream(device)
     step_graph = wl.capture(wl.step)
     gemv_graph = wl.capture(wl.gemv_only)
@@ -562,6 +565,9 @@ def run_memra(args):
             cfg["activation_quantise"] = ("fused into the product's prologue "
                                           "(memra_q8_0_quant_gemm)" if wl.fused else
                                           "separate memra_quantize_q8_1 launch")
+        else:
+            cfg["layer_calls"] = ("memra_q8_0_moe_ffn (2 kernels)" if wl.fused else
+                                  "quantize, moe_gemv, swiglu_quantize, moe_gemv")
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -634,8 +640,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--fused", action="store_true",
-                    help="quantise activations in the product's prologue "
+                    help="dense workloads: quantise activations in the product's prologue "
                          "(memra_q8_0_quant_gemm) instead of a separate q8_1 launch")
+    ap.add_argument("--unfused", action="store_true",
+                    help="moe_top8: four calls per layer instead of memra_q8_0_moe_ffn")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers than the workload's own (profiling captures only)")
     args = ap.parse_args(argv)

@@ -54,9 +54,6 @@ __host__ __device__ constexpr int log2i(int v) { return v <= 1 ? 0 : 1 + log2i(v
 __host__ __device__ inline int slices_for(int cpr) {
   return (cpr + kSlicePartsMax - 1) / kSlicePartsMax;
 }
-__host__ __device__ inline int slice_begin(int s, int cpr, int S) {
-  return (int)(((long long)s * cpr) / S);
-}
 
 // Sum V = 2^t values across the warp with the xor-butterfly tree (masks 16, 8, 4,
 // 2, 1), exchanging half of the remaining values at each of the first t stages.
@@ -231,7 +228,10 @@ __device__ __forceinline__ void fill_slice_table(int* tab, int cpr, int S, int t
 // ============================================================================
 // TMA producer/consumer kernel.
 // ============================================================================
-constexpr int kConsumerWarps = 8;
+#ifndef MEMRA_TMA_CONSUMER_WARPS
+#define MEMRA_TMA_CONSUMER_WARPS 12
+#endif
+constexpr int kConsumerWarps = MEMRA_TMA_CONSUMER_WARPS;
 constexpr int kTmaThreads = 32 * (1 + kConsumerWarps);
 constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 1024;  // barriers, abort flag, stage metadata, ids, gates
@@ -804,17 +804,35 @@ __global__ void __launch_bounds__(256)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr size_t kTmaStageTarget = 28 * 1024;  // bulk copies below ~16 KB stream slower
-constexpr size_t kTmaRingBudget = 88 * 1024;
-constexpr size_t kTmaSmemPairLimit = 110 * 1024;  // two CTAs per SM (this + the next kernel)
+// Ring and stage sizes measured on GB300: two CTAs per SM, each streaming through
+// about 88 KB of 28-KB stages, keep HBM busiest (bulk copies below ~16 KB stream
+// markedly slower per CTA).
+#ifndef MEMRA_TMA_RING_KB
+#define MEMRA_TMA_RING_KB 88
+#endif
+#ifndef MEMRA_TMA_STAGE_KB
+#define MEMRA_TMA_STAGE_KB 28
+#endif
+#ifndef MEMRA_TMA_CTAS_PER_SM
+#define MEMRA_TMA_CTAS_PER_SM 2
+#endif
+constexpr size_t kTmaStageTarget = MEMRA_TMA_STAGE_KB * 1024;
+constexpr size_t kTmaRingBudget = MEMRA_TMA_RING_KB * 1024;
+// Shared memory of one CTA when two must fit on an SM (228 KB, 1 KB per CTA kept
+// by the hardware).
+constexpr size_t kTmaSmemPairLimit = 113 * 1024;
 
-// Variant seam for tests and benchmarks: MEMRA_GEMV_PATH=tma selects the bulk-copy
-// kernel where it applies (read once per process); the register kernel is the
-// default.
-bool force_tma_path() {
-  static const bool v = [] {
+// Kernel selection seam for tests and benchmarks (read once per process):
+// MEMRA_GEMV_PATH=reg forces the register kernel; MEMRA_GEMV_PATH=tma uses the
+// bulk-copy kernel wherever it applies, also for M > 1.  By default the bulk-copy
+// kernel serves M = 1 products (decode GEMV of at least ~24 MB of weights, and
+// routed experts) and the register kernel the rest.
+int gemv_path_override() {
+  static const int v = [] {
     const char* e = std::getenv("MEMRA_GEMV_PATH");
-    return e && std::strcmp(e, "tma") == 0;
+    if (e && std::strcmp(e, "reg") == 0) return 1;
+    if (e && std::strcmp(e, "tma") == 0) return 2;
+    return 0;
   }();
   return v;
 }
@@ -823,7 +841,11 @@ int64_t max_units_per_cta(int64_t units, int64_t grid) { return (units + grid - 
 
 template <int M, int R, int MODE, int XIN>
 bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out) {
-  if (!force_tma_path()) return false;
+  const int path = gemv_path_override();
+  if (path == 1 || (path == 0 && M > 1)) return false;
+  // Per-shape dispatch: below ~24 MB of weights the register kernel's faster start
+  // wins over the deeper bulk-copy stream (measured on GB300).
+  if (path == 0 && MODE == kDense && p.units * p.K < (int64_t)24 * 1024 * 1024) return false;
   if (p.K % 256 != 0) return false;
   if (!aligned(p.wd, 16) || !aligned(p.wq, 16)) return false;
   if (XIN == kXq8 && (!aligned(p.xd, 16) || !aligned(p.xq, 16))) return false;
@@ -840,7 +862,7 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   // Ring: up to the budget, and within the two-CTAs-per-SM limit when possible.
   size_t limit = std::max<size_t>(kTmaSmemPairLimit, fixed + 2 * (stage + part_per_stage));
   limit = std::min<size_t>(limit, (size_t)info.max_smem_optin);
-  int ns = (int)std::min<size_t>(kMaxStages, kTmaRingBudget / stage);
+  int ns = (int)std::min<size_t>(kMaxStages, std::max<size_t>(2, kTmaRingBudget / stage));
   while (ns > 2 && fixed + ns * (stage + part_per_stage) > limit) --ns;
   if (ns < 2 || fixed + ns * (stage + part_per_stage) > (size_t)info.max_smem_optin) return false;
   p.rps = rps;
@@ -906,11 +928,19 @@ memra_status run_product(Params p, cudaStream_t stream) {
   p.nb = (int)(p.K / 32);
   p.cpr = (p.nb + 31) / 32;
   p.S = slices_for(p.cpr);
-  // One CTA per SM for the TMA kernel.
-  int64_t grid = std::min<int64_t>(p.units, info.sms);
+#ifndef MEMRA_TMA_CTAS_PER_SM
+#define MEMRA_TMA_CTAS_PER_SM 1
+#endif
+  int64_t grid = std::min<int64_t>(p.units, (int64_t)info.sms * MEMRA_TMA_CTAS_PER_SM);
   size_t smem = 0;
-  if (plan_tma<M, R, MODE, XIN>(p, info, grid, &smem))
+  if (plan_tma<M, R, MODE, XIN>(p, info, grid, &smem)) {
+    if (grid > info.sms && smem > kTmaSmemPairLimit) {
+      // Only one such CTA fits per SM: one per SM, so the grid stays a single wave.
+      grid = std::min<int64_t>(p.units, info.sms);
+      if (!plan_tma<M, R, MODE, XIN>(p, info, grid, &smem)) return MEMRA_ERR_UNSUPPORTED;
+    }
     return launch(q8_tma_kernel<M, R, MODE, XIN>, grid, kTmaThreads, smem, stream, p);
+  }
   grid = std::min<int64_t>(p.units, (int64_t)info.sms * reg_ctas_per_sm(M));
   if (plan_reg<M, R, MODE, XIN>(p, info, grid, &smem))
     return launch(q8_reg_kernel<M, R, MODE, XIN>, grid, kRegThreads, smem, stream, p);

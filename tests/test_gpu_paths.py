@@ -1,6 +1,8 @@
-"""The two product kernels (shared-memory TMA stream and register stream) implement
-one summation order, so they must agree bit for bit.  The bulk-copy kernel is
-selected in a child process with MEMRA_GEMV_PATH=tma (read once per process)."""
+"""The two product kernels (shared-memory bulk-copy stream and register stream)
+implement one summation order, so they must agree bit for bit.  Each child process
+pins the kernel choice with MEMRA_GEMV_PATH (read once per process): the default
+selection, the register kernel everywhere, and the bulk-copy kernel wherever it
+applies (also for M > 1)."""
 import os
 import subprocess
 import sys
@@ -61,7 +63,8 @@ def test_tma_and_register_kernels_agree_bitwise(tmp_path):
     from block_quantized_decode_quantize_gb300 import build
     build.build()
     a = run_child(tmp_path, None)
-    b = run_child(tmp_path, "tma")
-    assert a.keys() == b.keys()
-    for k in a:
-        assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), k
+    for other in ("reg", "tma"):
+        b = run_child(tmp_path, other)
+        assert a.keys() == b.keys()
+        for k in a:
+            assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), (other, k)
