@@ -161,9 +161,10 @@ def run_gemv_op(mem, op, quantize=True, fused=False):
 class Workload:
     """A step = a fixed list of library calls; captured once into a CUDA graph."""
 
-    def __init__(self, name, mem, device, layers=None, fused=False):
+    def __init__(self, name, mem, device, layers=None, fused=False, chain=False):
         self.name = name
         self.fused = fused
+        self.chain = None
         self.mem = mem
         self.device = device
         self.moe = None
@@ -182,6 +183,10 @@ class Workload:
             self.moe = [MoeLayer(mem, layer, device) for layer in range(n)]
         else:
             raise ValueError(name)
+        if chain:
+            if self.moe is not None or any(op.x.shape[0] != 1 for op in self.ops):
+                raise ValueError("--chain runs M = 1 dense products only")
+            self.chain = mem.GemvChain([(op.wq, op.wd, op.x[0], op.y[0]) for op in self.ops])
         torch.cuda.synchronize(device)
 
     @property
@@ -192,17 +197,24 @@ class Workload:
 
     @property
     def launches_per_step(self):
+        if self.chain is not None:
+            return 1
         if self.moe is not None:
             return (2 if self.fused else 4) * len(self.moe)
         return (1 if self.fused else 2) * len(self.ops)
 
     @property
     def gemv_launches_per_step(self):
+        if self.chain is not None:
+            return 1
         if self.moe is not None:
             return 2 * len(self.moe)
         return len(self.ops)
 
     def step(self):
+        if self.chain is not None:
+            self.chain.run()
+            return
         if self.moe is not None:
             for m in self.moe:
                 m.run(self.mem, fused=self.fused)
@@ -212,7 +224,9 @@ class Workload:
 
     def gemv_only(self):
         """The step's weight-streaming kernels alone (activations already quantised)."""
-        if self.moe is not None and self.fused:
+        if self.chain is not None:
+            self.chain.run()  # one launch streams every product of the step
+        elif self.moe is not None and self.fused:
             self.step()  # both launches of the fused layer stream weights
         elif self.moe is not None:
             for m in self.moe:
@@ -363,7 +377,7 @@ def profile_traffic(kernel_source_hash):
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("gemm.cu", "common.cuh"):
+    for name in ("gemm.cu", "product.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "block_quantized_decode_quantize_gb300", "csrc",
                                name), "rb") as f:
             h.update(f.read())
@@ -477,7 +491,8 @@ def run_memra(args):
     # Dense products quantise with a separate launch unless --fused; the routed FFN
     # uses its two-kernel entry point unless --unfused.
     fused = (not args.unfused) if args.workload == "moe_top8" else args.fused
-    wl = Workload(args.workload, mem, device, layers=args.layers, fused=fused)
+    wl = Workload(args.workload, mem, device, layers=args.layers, fused=fused,
+                  chain=args.chain)
     stream = torch.cuda.Stream(device)
     step_graph = wl.capture(wl.step)
     gemv_graph = wl.capture(wl.gemv_only)
@@ -517,6 +532,7 @@ def run_memra(args):
                 "peak_kind": peak_kind + " copy bandwidth (MEASURED_PEAKS hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "kernel": "Q8_0 product kernel (%s, M=%s)" % (
+                    "chained, one launch per step" if wl.chain is not None else
                     "routed experts" if wl.moe is not None else
                     ("quantise fused" if wl.fused else "q8_1 input"),
                     1 if wl.moe is not None else wl.ops[0].xq.shape[0]),
@@ -561,7 +577,10 @@ def run_memra(args):
     if rank == 0:
         cfg = workload_config(args.workload, wl)
         cfg["parallelism"] = "replicas x%d (no data-path collective)" % world
-        if wl.moe is None:
+        if wl.chain is not None:
+            cfg["activation_quantise"] = ("in the chained kernel, after a grid barrier on the "
+                                          "previous product (memra_q8_0_gemv_chain)")
+        elif wl.moe is None:
             cfg["activation_quantise"] = ("fused into the product's prologue "
                                           "(memra_q8_0_quant_gemm)" if wl.fused else
                                           "separate memra_quantize_q8_1 launch")
@@ -642,6 +661,9 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true",
                     help="dense workloads: quantise activations in the product's prologue "
                          "(memra_q8_0_quant_gemm) instead of a separate q8_1 launch")
+    ap.add_argument("--chain", action="store_true",
+                    help="dense M = 1 workloads: the whole step as one memra_q8_0_gemv_chain "
+                         "launch")
     ap.add_argument("--unfused", action="store_true",
                     help="moe_top8: four calls per layer instead of memra_q8_0_moe_ffn")
     ap.add_argument("--layers", type=int, default=None,

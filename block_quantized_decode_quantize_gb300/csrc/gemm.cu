@@ -36,93 +36,33 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "product.cuh"
+
+// Ring and stage sizes measured on GB300: two CTAs per SM, each streaming through
+// about 88 KB of 28-KB stages, keep HBM busiest (bulk copies below ~16 KB stream
+// markedly slower per CTA).
+#ifndef MEMRA_TMA_RING_KB
+#define MEMRA_TMA_RING_KB 88
+#endif
+#ifndef MEMRA_TMA_STAGE_KB
+#define MEMRA_TMA_STAGE_KB 28
+#endif
+#ifndef MEMRA_TMA_CTAS_PER_SM
+#define MEMRA_TMA_CTAS_PER_SM 2
+#endif
+#ifndef MEMRA_TMA_SMEM_LIMIT_KB
+#define MEMRA_TMA_SMEM_LIMIT_KB 113
+#endif
+#ifndef MEMRA_TMA_MIN_BLOCKS
+#define MEMRA_TMA_MIN_BLOCKS 2
+#endif
 
 namespace memra {
 namespace {
 
-#ifndef MEMRA_SLICE_PARTS
-#define MEMRA_SLICE_PARTS 4
-#endif
-constexpr int kSlicePartsMax = MEMRA_SLICE_PARTS;
 constexpr int kMaxTopK = MEMRA_MAX_TOP_K;
 
 enum Mode { kDense = 0, kMoeUngated = 1, kMoeGated = 2 };
-
-__host__ __device__ constexpr int next_pow2(int v) { return v <= 1 ? 1 : 2 * next_pow2((v + 1) / 2); }
-__host__ __device__ constexpr int log2i(int v) { return v <= 1 ? 0 : 1 + log2i(v / 2); }
-
-__host__ __device__ inline int slices_for(int cpr) {
-  return (cpr + kSlicePartsMax - 1) / kSlicePartsMax;
-}
-
-// Sum V = 2^t values across the warp with the xor-butterfly tree (masks 16, 8, 4,
-// 2, 1), exchanging half of the remaining values at each of the first t stages.
-// Every value goes through the same tree of pairwise sums as a plain butterfly
-// (fp32 addition is commutative).  Afterwards lane l holds value (l >> (5 - t)).
-template <int V>
-__device__ __forceinline__ void warp_sum_transposed(float (&v)[V], int lane) {
-  constexpr int t = log2i(V);
-#pragma unroll
-  for (int s = 0; s < t; ++s) {
-    const int mask = 16 >> s;
-    const int half = V >> (s + 1);
-    const bool upper = (lane & mask) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      v[i] = __fadd_rn(keep, __shfl_xor_sync(kFullMask, send, mask));
-    }
-  }
-#pragma unroll
-  for (int s = t; s < 5; ++s) v[0] = __fadd_rn(v[0], __shfl_xor_sync(kFullMask, v[0], 16 >> s));
-}
-
-// Reduce acc[R][M] of every lane and store the slice partials:
-// part[(row * S + s) * M + m] for rows < nrows.
-template <int R, int M>
-__device__ __forceinline__ void store_partials(float (&acc)[R][M], int lane, float* part,
-                                               int row0, int nrows, int s, int S) {
-  constexpr int V = next_pow2(R * M);
-  float v[V];
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int m = 0; m < M; ++m) v[r * M + m] = acc[r][m];
-#pragma unroll
-  for (int i = R * M; i < V; ++i) v[i] = 0.0f;
-  warp_sum_transposed<V>(v, lane);
-  constexpr int t = log2i(V);
-  if ((lane & ((32 >> t) - 1)) == 0) {
-    const int idx = lane >> (5 - t);
-    if (idx < R * M) {
-      const int r = idx / M;
-      const int m = idx - r * M;
-      if (r < nrows) part[((size_t)(row0 + r) * S + s) * M + m] = v[0];
-    }
-  }
-}
-
-// One block of one weight row against an x block: the exact int32 sum from two
-// 16-byte halves (in either order: integer addition is exact).
-__device__ __forceinline__ int dot_halves(const uint4& w0, const uint4& w1, const uint4& x0,
-                                          const uint4& x1) {
-  int s = 0;
-  s = __dp4a((int)w0.x, (int)x0.x, s);
-  s = __dp4a((int)w0.y, (int)x0.y, s);
-  s = __dp4a((int)w0.z, (int)x0.z, s);
-  s = __dp4a((int)w0.w, (int)x0.w, s);
-  s = __dp4a((int)w1.x, (int)x1.x, s);
-  s = __dp4a((int)w1.y, (int)x1.y, s);
-  s = __dp4a((int)w1.z, (int)x1.z, s);
-  s = __dp4a((int)w1.w, (int)x1.w, s);
-  return s;
-}
-
-__device__ __forceinline__ float block_term_acc(float acc, uint16_t dw_bits, float dx, int s) {
-  const float c = __fmul_rn(__half2float(__ushort_as_half(dw_bits)), dx);
-  return __fmaf_rn(c, (float)s, acc);
-}
 
 // ----------------------------------------------------------------------------
 // Work description shared by both kernels: a CTA's rows come as segments, each a
@@ -220,11 +160,6 @@ __device__ __forceinline__ void load_routing(const Params& p, int32_t* s_ids, fl
   }
 }
 
-// Slice boundaries (in parts) for the row's S slices: tab[s] = s*cpr/S.
-__device__ __forceinline__ void fill_slice_table(int* tab, int cpr, int S, int tid, int nthreads) {
-  for (int s = tid; s <= S; s += nthreads) tab[s] = (int)(((long long)s * cpr) / S);
-}
-
 // ============================================================================
 // TMA producer/consumer kernel.
 // ============================================================================
@@ -236,26 +171,6 @@ constexpr int kTmaThreads = 32 * (1 + kConsumerWarps);
 constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 1024;  // barriers, abort flag, stage metadata, ids, gates
 
-// Activation input of a product: q8_1 planes, or values quantised in the kernel's
-// prologue (bf16, fp32, or SwiGLU of an fp32 gate|up row pair).
-enum XIn { kXq8 = 0, kXbf16 = 1, kXf32 = 2, kXswiglu = 3 };
-
-// The 8 activation values of group g (row-major [rows][K], K % 8 == 0).
-template <int XIN>
-__device__ __forceinline__ void load_x_group(const void* xin, int g, int K, float v[8]) {
-  if (XIN == kXbf16) {
-    load8_bf16(static_cast<const uint16_t*>(xin) + (size_t)g * 8, v);
-  } else if (XIN == kXf32) {
-    load8_f32(static_cast<const float*>(xin) + (size_t)g * 8, v);
-  } else {
-    const int gpr = K / 8;
-    const int row = g / gpr;
-    const int f0 = (g - row * gpr) * 8;
-    const float* gu = static_cast<const float*>(xin) + (size_t)row * 2 * K;
-    swiglu8(gu + f0, gu + K + f0, v);
-  }
-}
-
 struct StageMeta {
   int seg;
   int r0;
@@ -263,34 +178,8 @@ struct StageMeta {
   int pad;
 };
 
-// Quantise `rows` activation rows of K values (bf16 bits or fp32) into the
-// shared-memory q8_1 planes.  Called by `nwarps` whole warps (warp index w).
-template <int XIN>
-__device__ __forceinline__ void quantize_rows_to_smem(const void* xin, int rows, int K,
-                                                      int8_t* xs, float* xds, int w, int nwarps,
-                                                      int lane) {
-  const int groups = rows * K / 8;  // fits: rows * K is bounded by MEMRA_MAX_X_BYTES
-  for (int base = w * 32; base < groups; base += nwarps * 32) {
-    const int g = base + lane;
-    const bool valid = g < groups;
-    float v[8];
-    if (valid) {
-      load_x_group<XIN>(xin, g, K, v);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-    }
-    float d;
-    const uint2 q = q8_1_group8(v, &d);
-    if (valid) {
-      *reinterpret_cast<uint2*>(xs + g * 8) = q;
-      if ((lane & 3) == 0) xds[g >> 2] = d;
-    }
-  }
-}
-
 template <int M, int R, int MODE, int XIN>
-__global__ void __launch_bounds__(kTmaThreads, 2) q8_tma_kernel(const Params p) {
+__global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[8] | empty[8] | xfull
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 8 * (2 * kMaxStages + 1));
@@ -804,23 +693,11 @@ __global__ void __launch_bounds__(256)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Ring and stage sizes measured on GB300: two CTAs per SM, each streaming through
-// about 88 KB of 28-KB stages, keep HBM busiest (bulk copies below ~16 KB stream
-// markedly slower per CTA).
-#ifndef MEMRA_TMA_RING_KB
-#define MEMRA_TMA_RING_KB 88
-#endif
-#ifndef MEMRA_TMA_STAGE_KB
-#define MEMRA_TMA_STAGE_KB 28
-#endif
-#ifndef MEMRA_TMA_CTAS_PER_SM
-#define MEMRA_TMA_CTAS_PER_SM 2
-#endif
 constexpr size_t kTmaStageTarget = MEMRA_TMA_STAGE_KB * 1024;
 constexpr size_t kTmaRingBudget = MEMRA_TMA_RING_KB * 1024;
 // Shared memory of one CTA when two must fit on an SM (228 KB, 1 KB per CTA kept
 // by the hardware).
-constexpr size_t kTmaSmemPairLimit = 113 * 1024;
+constexpr size_t kTmaSmemPairLimit = MEMRA_TMA_SMEM_LIMIT_KB * 1024;
 
 // Kernel selection seam for tests and benchmarks (read once per process):
 // MEMRA_GEMV_PATH=reg forces the register kernel; MEMRA_GEMV_PATH=tma uses the
@@ -928,9 +805,6 @@ memra_status run_product(Params p, cudaStream_t stream) {
   p.nb = (int)(p.K / 32);
   p.cpr = (p.nb + 31) / 32;
   p.S = slices_for(p.cpr);
-#ifndef MEMRA_TMA_CTAS_PER_SM
-#define MEMRA_TMA_CTAS_PER_SM 1
-#endif
   int64_t grid = std::min<int64_t>(p.units, (int64_t)info.sms * MEMRA_TMA_CTAS_PER_SM);
   size_t smem = 0;
   if (plan_tma<M, R, MODE, XIN>(p, info, grid, &smem)) {

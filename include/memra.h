@@ -50,6 +50,7 @@
 #ifndef MEMRA_H
 #define MEMRA_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -122,6 +123,51 @@ memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t* wd, int64
 memra_status memra_q8_0_quant_gemm(const int8_t* wq, const uint16_t* wd, int64_t N, int64_t K,
                                    int64_t M, const void* x, int32_t dtype, float* y,
                                    cudaStream_t stream);
+
+/*
+ * One M = 1 product of a chain (memra_q8_0_gemv_chain).  wq [N][K] (32-byte
+ * aligned) and wd [N][K/32] (16-byte aligned) are the Q8_0 planes, x [K] the
+ * unquantised activation (bf16 bits or fp32 per x_dtype, 16-byte aligned), y [N]
+ * the output.  K must be a positive multiple of 256.
+ */
+typedef struct memra_q8_0_step {
+  const int8_t* wq;
+  const uint16_t* wd;
+  const void* x;
+  float* y;
+  int64_t N;
+  int64_t K;
+  int32_t x_dtype;
+  int32_t reserved;
+} memra_q8_0_step;
+
+/*
+ * A decode step's chain of M = 1 products in one persistent launch: for i = 0, 1,
+ * ..., n_steps-1, y_i = W_i q8_1(x_i), where x_i is read only after every output of
+ * steps 0..i-1 is written (so x_i may be one of those outputs, fp32, or an
+ * independent input).  The pages drive a decode token as one CUDA-graph replay
+ * (memra wiki, feature list: CUDA-graph decode); this is the GB300 counterpart:
+ * the weights of step i+1 stream while step i finishes, instead of every product
+ * paying its own launch ramp and drain.  Each y_i is bit-identical to
+ * memra_q8_0_quant_gemm(W_i, x_i) with M = 1.
+ *   steps: DEVICE array of n_steps descriptors (16-byte aligned); host_steps: the
+ *   same descriptors in host memory (validated and used to size the launch).
+ *   N <= 2^30 per step.
+ *   sync_words: caller-allocated device scratch of at least
+ *   memra_q8_0_gemv_chain_sync_bytes(n_steps) bytes, 16-byte aligned: per-step row
+ *   counters and an abort word, zeroed by this call (on `stream`) before the launch.
+ *   Two chains in flight at once need separate sync_words.
+ *   dev_status (nullable): OR-ed with 2 if the kernel gave up waiting (bounded wait
+ *   of about a second; outputs are then incomplete).
+ * The launch is cooperative (every CTA resident at once); MEMRA_ERR_CUDA if the
+ * device cannot host the grid.
+ */
+memra_status memra_q8_0_gemv_chain(const memra_q8_0_step* steps,
+                                   const memra_q8_0_step* host_steps, int32_t n_steps,
+                                   uint32_t* sync_words, int32_t* dev_status, cudaStream_t stream);
+
+/* Bytes of sync_words that memra_q8_0_gemv_chain needs for n_steps >= 0 steps. */
+size_t memra_q8_0_gemv_chain_sync_bytes(int32_t n_steps);
 
 /*
  * Routed-expert GEMV for one token (memra wiki, feature list: MoE routed experts).
