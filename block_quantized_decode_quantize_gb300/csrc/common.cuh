@@ -34,6 +34,16 @@ __device__ __forceinline__ Quants32 ld_stream_32B(const int8_t* p) {
   return r;
 }
 
+// 16 bytes cached in L2 only (never a stale L1 line): for data written by the
+// preceding kernel, read after the grid-dependency wait.
+__device__ __forceinline__ uint4 ld_cg_16B(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
 __device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t* p) {
   unsigned short v;
   asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));

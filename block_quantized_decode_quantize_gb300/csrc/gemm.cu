@@ -13,19 +13,21 @@
 //
 // Two kernels implement it.
 //
-// q8_tma_kernel (the GB300 path; K % 256 == 0 and 16-byte aligned planes): one
-//   CTA per SM owns a contiguous range of weight rows (or, for the routed product,
-//   a few contiguous row ranges, one per selected expert).  Warp 0 is the
+// q8_tma_kernel (the GB300 path; K % 256 == 0 and 16-byte aligned planes): two
+//   CTAs per SM, each owning a contiguous range of weight rows (or, for the routed
+//   product, a few contiguous row ranges, one per selected expert).  Warp 0 is the
 //   producer: one lane streams whole rows of the quant and scale planes into a ring
 //   of shared-memory stages with cp.async.bulk, completing on per-stage mbarriers,
-//   and the warp reduces each finished stage's slice partials into y.  Warps 1..8
+//   records each stage's rows in shared memory, closes the stream with a sentinel
+//   stage, and reduces each finished stage's slice partials into y.  Warps 1..12
 //   consume stages: each task is (R rows, one slice), read from shared memory with
 //   128-bit loads whose half-block order alternates between lane quads so that no
 //   two lanes of a phase hit the same banks.  The HBM stream is set by the ring
-//   (tens of KB in flight per SM), not by how tasks divide among warps.  With
-//   programmatic dependent launch the producer fills the ring before waiting for the
-//   preceding kernel; the CTA is sized so that the next kernel's CTA fits beside it
-//   on the SM and starts its own stream while this one drains.
+//   (about 176 KB in flight per SM), not by how tasks divide among warps.  With
+//   programmatic dependent launch the producer starts the ring as soon as the CTA
+//   is resident, before the preceding kernel has finished (dense weights do not
+//   depend on it); the consumers wait for that kernel and then stage the
+//   activation with plain loads.
 //
 // q8_reg_kernel (everything else): the same tasks with weights loaded straight
 //   into registers (256-bit loads, a slice's blocks issued together), activations
@@ -40,7 +42,8 @@
 
 // Ring and stage sizes measured on GB300: two CTAs per SM, each streaming through
 // about 88 KB of 28-KB stages, keep HBM busiest (bulk copies below ~16 KB stream
-// markedly slower per CTA).
+// markedly slower per CTA).  Each can be overridden at run time by the environment
+// variable of the same name (read once per process; see TmaTuning).
 #ifndef MEMRA_TMA_RING_KB
 #define MEMRA_TMA_RING_KB 88
 #endif
@@ -52,6 +55,10 @@
 #endif
 #ifndef MEMRA_TMA_SMEM_LIMIT_KB
 #define MEMRA_TMA_SMEM_LIMIT_KB 113
+#endif
+// Dense products below this many MB of weights use the register kernel.
+#ifndef MEMRA_TMA_DENSE_MIN_MB
+#define MEMRA_TMA_DENSE_MIN_MB 24
 #endif
 #ifndef MEMRA_TMA_MIN_BLOCKS
 #define MEMRA_TMA_MIN_BLOCKS 2
@@ -171,17 +178,19 @@ constexpr int kTmaThreads = 32 * (1 + kConsumerWarps);
 constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 1024;  // barriers, abort flag, stage metadata, ids, gates
 
+// What the producer put in a ring slot: rows [r0, r0 + nr) of segment `seg`, with
+// activation row `xrow`.  nr == 0 marks the end of the CTA's stages.
 struct StageMeta {
   int seg;
   int r0;
   int nr;
-  int pad;
+  int xrow;
 };
 
 template <int M, int R, int MODE, int XIN>
 __global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[8] | empty[8] | xfull
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[8] | empty[8]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 8 * (2 * kMaxStages + 1));
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + 160);
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem + 160 + 16 * kMaxStages);
@@ -202,54 +211,70 @@ __global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kern
   const int64_t u1 = p.units * (blockIdx.x + 1) / gridDim.x;
   auto full_bar = [&](int i) { return smem_addr(bars + i); };
   auto empty_bar = [&](int i) { return smem_addr(bars + kMaxStages + i); };
-  const uint32_t xfull_bar = smem_addr(bars + 2 * kMaxStages);
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < ns; ++i) {
-      mbar_init(full_bar(i), 1);
-      mbar_init(empty_bar(i), kConsumerWarps);
-    }
-    mbar_init(xfull_bar, 1);
-    *abort_flag = 0;
-    mbar_init_fence();
-  }
   pdl_launch_dependents();
-  if (MODE != kDense && warp == 0) {
-    pdl_wait();  // ids and gate weights may come from the preceding kernel
-    load_routing<MODE>(p, s_ids, s_gate, lane, 32);
+  // Start-up.  The producer warp initialises the barriers (and, for routed
+  // products, loads the routing), signals the consumers with a non-blocking arrive
+  // on named barrier 2 and starts streaming at once; the consumers build the slice
+  // table and wait there before touching any barrier.
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < ns; ++i) {
+        mbar_init(full_bar(i), 1);
+        mbar_init(empty_bar(i), kConsumerWarps);
+      }
+      *abort_flag = 0;
+      mbar_init_fence();
+    }
+    if (MODE != kDense) {
+      pdl_wait();  // ids and gate weights may come from the preceding kernel
+      load_routing<MODE>(p, s_ids, s_gate, lane, 32);
+    }
+    if (MODE == kMoeGated) {
+      for (int64_t i = lane; i < u1 - u0; i += 32) yacc[i] = 0.0f;
+    }
+    __syncwarp();
+    asm volatile("bar.arrive 2, %0;" ::"n"(kTmaThreads) : "memory");
+  } else {
+    fill_slice_table(s_slice, p.cpr, S, threadIdx.x - 32, kTmaThreads - 32);
+    asm volatile("bar.sync 2, %0;" ::"n"(kTmaThreads) : "memory");
   }
-  if (MODE == kMoeGated) {
-    for (int64_t i = threadIdx.x; i < u1 - u0; i += kTmaThreads) yacc[i] = 0.0f;
-  }
-  fill_slice_table(s_slice, p.cpr, S, threadIdx.x, kTmaThreads);
-  __syncthreads();
 
   const int nseg = num_segs<MODE>(p, u0, u1);
+  auto seg_of = [&](int si) { return get_seg<MODE>(p, u0, u1, si, s_ids); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = l2_evict_first_policy();
-    uint32_t issued = 0;
-    bool x_issued = XIN != kXq8;  // fused quantisation: the consumers build x themselves
+    uint32_t issued = 0;  // ring slots filled, the closing sentinel included
     bool ok = true;
 
-    auto issue_x = [&]() {
-      if (MODE == kDense) pdl_wait();  // activations come from the preceding kernel
-      if (lane == 0) {
-        const uint32_t xb = (uint32_t)(p.xrows * p.K);
-        const uint32_t db = (uint32_t)(p.xrows * nb * 4);
-        mbar_arrive_expect_tx(xfull_bar, xb + db);
-        bulk_g2s(smem_addr(xs), p.xq, xb, xfull_bar);
-        bulk_g2s(smem_addr(xds), p.xd, db, xfull_bar);
+    // Stage source: the CTA's own segments in order, rps rows at a time.
+    int cur_si = 0, cur_r0 = 0;
+    auto static_next = [&](StageMeta& m) -> bool {
+      while (cur_si < nseg) {
+        const Seg g = get_seg<MODE>(p, u0, u1, cur_si, s_ids);
+        if (!g.valid || cur_r0 >= g.nrows) {
+          if (!g.valid && MODE == kMoeUngated)
+            for (int i = lane; i < g.nrows; i += 32) p.y[g.out0 + i] = 0.0f;
+          ++cur_si;
+          cur_r0 = 0;
+          continue;
+        }
+        m.seg = cur_si;
+        m.r0 = cur_r0;
+        m.nr = min(p.rps, g.nrows - cur_r0);
+        m.xrow = g.xrow;
+        cur_r0 += p.rps;
+        return true;
       }
-      __syncwarp();
-      x_issued = true;
+      return false;
     };
 
     // Reduce the slice partials of the stage in `slot` into the outputs.
     auto epilogue = [&](int slot) {
       const StageMeta mt = meta[slot];
-      const Seg g = get_seg<MODE>(p, u0, u1, mt.seg, s_ids);
+      const Seg g = seg_of(mt.seg);
       const float* pp = part + (size_t)slot * p.rps * S * M;
       for (int i = lane; i < mt.nr * M; i += 32) {
         const int r = i / M;
@@ -266,41 +291,63 @@ __global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kern
       __syncwarp();
     };
 
-    for (int si = 0; si < nseg && ok; ++si) {
-      const Seg g = get_seg<MODE>(p, u0, u1, si, s_ids);
-      if (!g.valid) {
-        if (MODE == kMoeUngated)
-          for (int i = lane; i < g.nrows; i += 32) p.y[g.out0 + i] = 0.0f;
-        continue;
+    // Make ring slot issued % ns free: wait until its previous stage is consumed
+    // and reduce it.
+    bool acquired = false;
+    auto acquire = [&]() -> bool {
+      if (acquired) return true;
+      const int slot = issued % ns;
+      if (issued >= (uint32_t)ns) {
+        if (!mbar_wait(empty_bar(slot), ((issued / ns) - 1) & 1, abort_flag)) return false;
+        epilogue(slot);
       }
-      for (int r0 = 0; r0 < g.nrows; r0 += p.rps) {
-        const int nr = min(p.rps, g.nrows - r0);
-        const int slot = issued % ns;
-        if (issued >= (uint32_t)ns) {
-          if (!mbar_wait(empty_bar(slot), ((issued / ns) - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          epilogue(slot);
-        }
-        if (lane == 0) {
-          meta[slot] = StageMeta{si, r0, nr, 0};
-          const uint32_t qb = (uint32_t)(nr * p.K);
-          const uint32_t db = (uint32_t)(nr * nb * 2);
+      acquired = true;
+      return true;
+    };
+    // Fill the acquired slot with stage `m`, or with the closing sentinel.
+    auto fill = [&](const StageMeta* m) {
+      const int slot = issued % ns;
+      if (lane == 0) {
+        if (m) {
+          meta[slot] = *m;
+          const Seg g = seg_of(m->seg);
+          const uint32_t qb = (uint32_t)(m->nr * p.K);
+          const uint32_t db = (uint32_t)(m->nr * nb * 2);
           const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
           mbar_arrive_expect_tx(full_bar(slot), qb + db);
-          bulk_g2s_hint(dst, p.wq + (g.row0 + r0) * p.K, qb, full_bar(slot), policy);
-          bulk_g2s_hint(dst + p.wd_off, p.wd + (g.row0 + r0) * nb, db, full_bar(slot), policy);
+          bulk_g2s_hint(dst, p.wq + (g.row0 + m->r0) * p.K, qb, full_bar(slot), policy);
+          bulk_g2s_hint(dst + p.wd_off, p.wd + (g.row0 + m->r0) * nb, db, full_bar(slot), policy);
+        } else {
+          meta[slot] = StageMeta{0, 0, 0, 0};  // sentinel: no more stages
+          mbar_arrive(full_bar(slot));
         }
-        __syncwarp();
-        ++issued;
-        if (issued == (uint32_t)ns && !x_issued) issue_x();
+      }
+      __syncwarp();
+      ++issued;
+      acquired = false;
+    };
+
+    for (;;) {
+      StageMeta m;
+      if (!static_next(m)) break;
+      if (!acquire()) {
+        ok = false;
+        break;
+      }
+      fill(&m);
+    }
+    if (ok) {
+      if (acquire()) {
+        fill(nullptr);
+      } else {
+        ok = false;
       }
     }
-    if (!x_issued) issue_x();
-    // Drain: the last stages' partials.
+    // Drain: the partials of the stages still in the ring (after a normal end the
+    // last slot filled holds the sentinel).
     const uint32_t first = issued > (uint32_t)ns ? issued - ns : 0;
-    for (uint32_t j = first; j < issued && ok; ++j) {
+    const uint32_t last = ok ? issued - 1 : issued;
+    for (uint32_t j = first; j < last && ok; ++j) {
       const int slot = j % ns;
       if (!mbar_wait(empty_bar(slot), (j / ns) & 1, abort_flag)) {
         ok = false;
@@ -309,18 +356,15 @@ __global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kern
       epilogue(slot);
     }
     if (!ok || *abort_flag) {
-      // A wait gave up: let the copies already issued land (bounded), then mark
-      // this CTA's outputs invalid with NaN.
+      // A wait gave up: let the copies already issued land (bounded), then mark the
+      // outputs this CTA owns invalid with NaN (after the preceding kernel, which
+      // may still read them).
       *abort_flag = 1;
+      pdl_wait();
       for (uint32_t j = first; j < issued; ++j) {
         const int slot = j % ns;
         const long long t0 = clock64();
         while (!mbar_try_wait(full_bar(slot), (j / ns) & 1) && clock64() - t0 < (1ll << 30)) {
-        }
-      }
-      if (XIN == kXq8) {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(xfull_bar, 0) && clock64() - t0 < (1ll << 30)) {
         }
       }
       const float nan = __int_as_float(0x7fc00000);
@@ -341,89 +385,89 @@ __global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kern
     const int h1 = (lane >> 2) & 1;  // which half this lane loads first
     const int Ki = (int)p.K;
     const bool last_ok = lane < nb - (p.cpr - 1) * 32;
+    // The activation comes from the preceding kernel.  The consumers stage it with
+    // plain loads: a bulk copy would queue behind the weight stages already issued
+    // and land only after all of them.
+    pdl_wait();
     if (XIN == kXq8) {
-      if (!mbar_wait(xfull_bar, 0, abort_flag)) return;
+      copy_x_to_smem<4>(p.xq, p.xd, p.xrows * Ki, p.xrows * nb * 4, xs, xds, threadIdx.x - 32,
+                        kConsumerWarps * 32);
     } else {
-      pdl_wait();  // the activation comes from the preceding kernel
       quantize_rows_to_smem<XIN>(p.xin, p.xrows, (int)p.K, xs, xds, cw, kConsumerWarps, lane);
-      asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     }
-    uint32_t it = 0;
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     uint32_t tbase = 0;  // tasks in all earlier stages: deals tasks round-robin over warps
-    for (int si = 0; si < nseg; ++si) {
-      const Seg g = get_seg<MODE>(p, u0, u1, si, s_ids);
-      if (!g.valid) continue;
-      const int xrow = (MODE == kDense) ? 0 : g.xrow;
-      for (int r0 = 0; r0 < g.nrows; r0 += p.rps) {
-        const int nr = min(p.rps, g.nrows - r0);
-        const int slot = it % ns;
-        const int groups = (nr + R - 1) / R;
-        const int ntasks = groups * S;
-        const int t0 = (int)((cw + kConsumerWarps - (int)(tbase % kConsumerWarps)) %
-                             kConsumerWarps);
-        tbase += ntasks;
-        // Every warp waits for every stage, tasks or not: an arrival on the stage's
-        // empty barrier must never run ahead of the stage itself.
-        if (!mbar_wait(full_bar(slot), (it / ns) & 1, abort_flag)) return;
-        const int8_t* ws = reinterpret_cast<const int8_t*>(ring + (size_t)slot * p.stage_bytes);
-        const uint16_t* ds =
-            reinterpret_cast<const uint16_t*>(ring + (size_t)slot * p.stage_bytes + p.wd_off);
-        float* pp = part + (size_t)slot * p.rps * S * M;
-        for (int t = t0; t < ntasks; t += kConsumerWarps) {
-          const int gi = t / S;
-          const int s = t - gi * S;
-          const int rbase = gi * R;
-          const int plo = s_slice[s];
-          const int phi = s_slice[s + 1];
-          // Per-lane pointers at the task's first block; a part is 1024 bytes on.
-          const int8_t* wl[R];
-          const uint16_t* dl[R];
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it % ns;
+      // Every warp waits for every stage, tasks or not: an arrival on the stage's
+      // empty barrier must never run ahead of the stage itself.
+      if (!mbar_wait(full_bar(slot), (it / ns) & 1, abort_flag)) return;
+      const StageMeta mt = meta[slot];
+      if (mt.nr <= 0) break;
+      const int nr = mt.nr;
+      const int xrow = mt.xrow;
+      const int groups = (nr + R - 1) / R;
+      const int ntasks = groups * S;
+      const int t0 =
+          (int)((cw + kConsumerWarps - (int)(tbase % kConsumerWarps)) % kConsumerWarps);
+      tbase += ntasks;
+      const int8_t* ws = reinterpret_cast<const int8_t*>(ring + (size_t)slot * p.stage_bytes);
+      const uint16_t* ds =
+          reinterpret_cast<const uint16_t*>(ring + (size_t)slot * p.stage_bytes + p.wd_off);
+      float* pp = part + (size_t)slot * p.rps * S * M;
+      for (int t = t0; t < ntasks; t += kConsumerWarps) {
+        const int gi = t / S;
+        const int s = t - gi * S;
+        const int rbase = gi * R;
+        const int plo = s_slice[s];
+        const int phi = s_slice[s + 1];
+        // Per-lane pointers at the task's first block; a part is 1024 bytes on.
+        const int8_t* wl[R];
+        const uint16_t* dl[R];
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            // Rows past the stage's end reuse a valid row; their sums are dropped.
-            const int row = rbase + r < nr ? rbase + r : rbase;
-            wl[r] = ws + row * Ki + (plo * 32 + lane) * 32 + h1 * 16;
-            dl[r] = ds + row * nb + plo * 32 + lane;
-          }
-          const int8_t* xl = xs + (size_t)xrow * Ki + (plo * 32 + lane) * 32 + h1 * 16;
-          const float* xdl = xds + (size_t)xrow * nb + plo * 32 + lane;
-          float acc[R][M];
+        for (int r = 0; r < R; ++r) {
+          // Rows past the stage's end reuse a valid row; their sums are dropped.
+          const int row = rbase + r < nr ? rbase + r : rbase;
+          wl[r] = ws + row * Ki + (plo * 32 + lane) * 32 + h1 * 16;
+          dl[r] = ds + row * nb + plo * 32 + lane;
+        }
+        const int8_t* xl = xs + (size_t)xrow * Ki + (plo * 32 + lane) * 32 + h1 * 16;
+        const float* xdl = xds + (size_t)xrow * nb + plo * 32 + lane;
+        float acc[R][M];
 #pragma unroll
-          for (int r = 0; r < R; ++r)
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
-          for (int pt = plo; pt < phi; ++pt) {
-            const int q = pt - plo;
-            if (pt < p.cpr - 1 || last_ok) {
-              uint4 w0[R], w1[R];
-              uint16_t dw[R];
+          for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
+        for (int pt = plo; pt < phi; ++pt) {
+          const int q = pt - plo;
+          if (pt < p.cpr - 1 || last_ok) {
+            uint4 w0[R], w1[R];
+            uint16_t dw[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              // The two halves in this lane quad's order (see the file comment).
+              w0[r] = *reinterpret_cast<const uint4*>(wl[r] + q * 1024);
+              w1[r] = *reinterpret_cast<const uint4*>(wl[r] + q * 1024 + 16 - 32 * h1);
+              dw[r] = dl[r][q * 32];
+            }
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+              const int8_t* xm = xl + (size_t)m * Ki + q * 1024;
+              const uint4 x0 = *reinterpret_cast<const uint4*>(xm);
+              const uint4 x1 = *reinterpret_cast<const uint4*>(xm + 16 - 32 * h1);
+              const float dx = xdl[(size_t)m * nb + q * 32];
 #pragma unroll
               for (int r = 0; r < R; ++r) {
-                // The two halves in this lane quad's order (see the file comment).
-                w0[r] = *reinterpret_cast<const uint4*>(wl[r] + q * 1024);
-                w1[r] = *reinterpret_cast<const uint4*>(wl[r] + q * 1024 + 16 - 32 * h1);
-                dw[r] = dl[r][q * 32];
-              }
-#pragma unroll
-              for (int m = 0; m < M; ++m) {
-                const int8_t* xm = xl + (size_t)m * Ki + q * 1024;
-                const uint4 x0 = *reinterpret_cast<const uint4*>(xm);
-                const uint4 x1 = *reinterpret_cast<const uint4*>(xm + 16 - 32 * h1);
-                const float dx = xdl[(size_t)m * nb + q * 32];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                  const int sb = dot_halves(w0[r], w1[r], x0, x1);
-                  acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, sb);
-                }
+                const int sb = dot_halves(w0[r], w1[r], x0, x1);
+                acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, sb);
               }
             }
           }
-          store_partials<R, M>(acc, lane, pp, rbase, nr - rbase, s, S);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(slot));
-        ++it;
+        store_partials<R, M>(acc, lane, pp, rbase, nr - rbase, s, S);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(slot));
     }
   }
 }
@@ -693,11 +737,40 @@ __global__ void __launch_bounds__(256)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr size_t kTmaStageTarget = MEMRA_TMA_STAGE_KB * 1024;
-constexpr size_t kTmaRingBudget = MEMRA_TMA_RING_KB * 1024;
-// Shared memory of one CTA when two must fit on an SM (228 KB, 1 KB per CTA kept
-// by the hardware).
-constexpr size_t kTmaSmemPairLimit = MEMRA_TMA_SMEM_LIMIT_KB * 1024;
+// Sizes of the bulk-copy kernel.  The compiled-in defaults can be overridden per
+// process by environment variables of the same names (MEMRA_TMA_RING_KB, ...), read
+// on first use; a value that is not a non-negative integer keeps the default.
+struct TmaTuning {
+  size_t stage_target;    // bytes per ring stage (rounded to whole rows)
+  size_t ring_budget;     // bytes of ring per CTA
+  size_t smem_pair_limit; // shared memory of one CTA when two must fit on an SM
+  int ctas_per_sm;
+  int64_t dense_min_bytes;  // smaller dense products use the register kernel
+};
+
+long env_long(const char* name, long dflt, long lo) {
+  const char* e = std::getenv(name);
+  if (!e || !*e) return dflt;
+  char* end = nullptr;
+  const long v = std::strtol(e, &end, 10);
+  if (*end != '\0' || v < lo || v > (1L << 20)) return dflt;
+  return v;
+}
+
+const TmaTuning& tma_tuning() {
+  static const TmaTuning t = [] {
+    TmaTuning r;
+    r.stage_target = (size_t)env_long("MEMRA_TMA_STAGE_KB", MEMRA_TMA_STAGE_KB, 1) * 1024;
+    r.ring_budget = (size_t)env_long("MEMRA_TMA_RING_KB", MEMRA_TMA_RING_KB, 1) * 1024;
+    r.smem_pair_limit =
+        (size_t)env_long("MEMRA_TMA_SMEM_LIMIT_KB", MEMRA_TMA_SMEM_LIMIT_KB, 1) * 1024;
+    r.ctas_per_sm = (int)env_long("MEMRA_TMA_CTAS_PER_SM", MEMRA_TMA_CTAS_PER_SM, 1);
+    r.dense_min_bytes =
+        (int64_t)env_long("MEMRA_TMA_DENSE_MIN_MB", MEMRA_TMA_DENSE_MIN_MB, 0) * 1024 * 1024;
+    return r;
+  }();
+  return t;
+}
 
 // Kernel selection seam for tests and benchmarks (read once per process):
 // MEMRA_GEMV_PATH=reg forces the register kernel; MEMRA_GEMV_PATH=tma uses the
@@ -719,15 +792,16 @@ int64_t max_units_per_cta(int64_t units, int64_t grid) { return (units + grid - 
 template <int M, int R, int MODE, int XIN>
 bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out) {
   const int path = gemv_path_override();
+  const TmaTuning& tune = tma_tuning();
   if (path == 1 || (path == 0 && M > 1)) return false;
-  // Per-shape dispatch: below ~24 MB of weights the register kernel's faster start
-  // wins over the deeper bulk-copy stream (measured on GB300).
-  if (path == 0 && MODE == kDense && p.units * p.K < (int64_t)24 * 1024 * 1024) return false;
+  // Per-shape dispatch: below a few tens of MB of weights the register kernel's
+  // faster start wins over the deeper bulk-copy stream (measured on GB300).
+  if (path == 0 && MODE == kDense && p.units * p.K < tune.dense_min_bytes) return false;
   if (p.K % 256 != 0) return false;
   if (!aligned(p.wd, 16) || !aligned(p.wq, 16)) return false;
   if (XIN == kXq8 && (!aligned(p.xd, 16) || !aligned(p.xq, 16))) return false;
   const size_t row_bytes = (size_t)p.K + (size_t)p.nb * 2;
-  int rps = (int)std::max<size_t>(1, kTmaStageTarget / row_bytes);
+  int rps = (int)std::max<size_t>(1, tune.stage_target / row_bytes);
   rps = std::max(R, rps / R * R);
   const size_t stage = align_up((size_t)rps * p.K, 128) + align_up((size_t)rps * p.nb * 2, 128);
   const size_t xbytes =
@@ -737,9 +811,9 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   const size_t fixed = kHeaderBytes + xbytes + yacc + align_up((size_t)(p.S + 1) * 4, 16);
   const size_t part_per_stage = align_up((size_t)rps * p.S * M * 4, 16);
   // Ring: up to the budget, and within the two-CTAs-per-SM limit when possible.
-  size_t limit = std::max<size_t>(kTmaSmemPairLimit, fixed + 2 * (stage + part_per_stage));
+  size_t limit = std::max<size_t>(tune.smem_pair_limit, fixed + 2 * (stage + part_per_stage));
   limit = std::min<size_t>(limit, (size_t)info.max_smem_optin);
-  int ns = (int)std::min<size_t>(kMaxStages, std::max<size_t>(2, kTmaRingBudget / stage));
+  int ns = (int)std::min<size_t>(kMaxStages, std::max<size_t>(2, tune.ring_budget / stage));
   while (ns > 2 && fixed + ns * (stage + part_per_stage) > limit) --ns;
   if (ns < 2 || fixed + ns * (stage + part_per_stage) > (size_t)info.max_smem_optin) return false;
   p.rps = rps;
@@ -805,10 +879,10 @@ memra_status run_product(Params p, cudaStream_t stream) {
   p.nb = (int)(p.K / 32);
   p.cpr = (p.nb + 31) / 32;
   p.S = slices_for(p.cpr);
-  int64_t grid = std::min<int64_t>(p.units, (int64_t)info.sms * MEMRA_TMA_CTAS_PER_SM);
+  int64_t grid = std::min<int64_t>(p.units, (int64_t)info.sms * tma_tuning().ctas_per_sm);
   size_t smem = 0;
   if (plan_tma<M, R, MODE, XIN>(p, info, grid, &smem)) {
-    if (grid > info.sms && smem > kTmaSmemPairLimit) {
+    if (grid > info.sms && smem > tma_tuning().smem_pair_limit) {
       // Only one such CTA fits per SM: one per SM, so the grid stays a single wave.
       grid = std::min<int64_t>(p.units, info.sms);
       if (!plan_tma<M, R, MODE, XIN>(p, info, grid, &smem)) return MEMRA_ERR_UNSUPPORTED;

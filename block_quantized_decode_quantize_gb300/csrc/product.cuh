@@ -143,6 +143,37 @@ __device__ __forceinline__ void quantize_rows_to_smem(const void* xin, int rows,
   }
 }
 
+// Copy q8_1 activation planes (xq: qbytes, xd: dbytes; both multiples of 16 and
+// 16-byte aligned) into shared memory with L2-only 16-byte loads, U loads in flight
+// per thread before any store.  Called by `nt` threads (index t).
+template <int U>
+__device__ __forceinline__ void copy_x_to_smem(const int8_t* xq, const float* xd, int qbytes,
+                                               int dbytes, int8_t* xs, float* xds, int t,
+                                               int nt) {
+  const int nq = qbytes / 16;
+  const int total = nq + dbytes / 16;
+  for (int base = t; base < total; base += nt * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * nt;
+      if (i < total)
+        v[u] = i < nq ? ld_cg_16B(xq + (size_t)i * 16)
+                      : ld_cg_16B(reinterpret_cast<const int8_t*>(xd) + (size_t)(i - nq) * 16);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * nt;
+      if (i < total) {
+        if (i < nq)
+          reinterpret_cast<uint4*>(xs)[i] = v[u];
+        else
+          reinterpret_cast<uint4*>(xds)[i - nq] = v[u];
+      }
+    }
+  }
+}
+
 // Slice boundaries (in parts) for the row's S slices: tab[s] = s*cpr/S.
 __device__ __forceinline__ void fill_slice_table(int* tab, int cpr, int S, int tid, int nthreads) {
   for (int s = tid; s <= S; s += nthreads) tab[s] = (int)(((long long)s * cpr) / S);

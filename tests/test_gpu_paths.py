@@ -2,7 +2,8 @@
 implement one summation order, so they must agree bit for bit.  Each child process
 pins the kernel choice with MEMRA_GEMV_PATH (read once per process): the default
 selection, the register kernel everywhere, and the bulk-copy kernel wherever it
-applies (also for M > 1)."""
+applies (also for M > 1).  The shapes include products with many ring stages per
+CTA (12289 x 4096 ends in a one-row stage; 5120 x 17408 has one-row stages)."""
 import os
 import subprocess
 import sys
@@ -21,7 +22,7 @@ import synth
 import block_quantized_decode_quantize_gb300 as mem
 out = {}
 for (N, K, M) in [(1003, 4096, 1), (777, 5120, 1), (513, 2048, 4), (300, 5120, 8), (4100, 768, 1),
-                  (64, 17408, 1)]:
+                  (64, 17408, 1), (12289, 4096, 1), (5120, 17408, 1), (12289, 4096, 2)]:
     w = synth.weights_fp32(N, K, 70, N, K, device="cuda")
     x = synth.activations_bf16(M, K, 71, N, K, M, outlier_frac=0.001, device="cuda")
     wq, wd = mem.memra_quantize_q8_0(w)
