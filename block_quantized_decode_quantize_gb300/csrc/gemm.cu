@@ -94,6 +94,9 @@ struct Params {
   int64_t E;
   int xpe;                 // one activation row per expert
   int32_t* status;
+  // The routing was already waited for by the preceding kernel of the same call, and
+  // that kernel let this one launch only after its own wait: read it at once.
+  int routing_ready;
   // TMA kernel layout
   int rps;                 // rows per stage
   int ns;                  // stages in the ring
@@ -159,10 +162,10 @@ template <int MODE>
 __device__ __forceinline__ void load_routing(const Params& p, int32_t* s_ids, float* s_gate,
                                              int tid, int nthreads) {
   for (int k = tid; k < p.top_k; k += nthreads) {
-    const int32_t e = p.ids[k];
+    const int32_t e = __ldcg(p.ids + k);
     const bool ok = e >= 0 && e < p.E;
     s_ids[k] = ok ? e : -1;
-    s_gate[k] = (MODE == kMoeGated) ? p.gate_w[k] : 1.0f;
+    s_gate[k] = (MODE == kMoeGated) ? __ldcg(p.gate_w + k) : 1.0f;
     if (!ok && p.status && blockIdx.x == 0) atomicOr(p.status, 1);
   }
 }
@@ -175,8 +178,14 @@ __device__ __forceinline__ void load_routing(const Params& p, int32_t* s_ids, fl
 #endif
 constexpr int kConsumerWarps = MEMRA_TMA_CONSUMER_WARPS;
 constexpr int kTmaThreads = 32 * (1 + kConsumerWarps);
-constexpr int kMaxStages = 8;
-constexpr int kHeaderBytes = 1024;  // barriers, abort flag, stage metadata, ids, gates
+constexpr int kMaxStages = 16;
+// Shared-memory header: full[kMaxStages] | empty[kMaxStages] mbarriers, the abort
+// flag, the stage metadata, the routed ids and gate weights.
+constexpr int kOffAbort = 8 * 2 * kMaxStages;
+constexpr int kOffMeta = kOffAbort + 16;
+constexpr int kOffIds = kOffMeta + 16 * kMaxStages;
+constexpr int kOffGate = kOffIds + 4 * kMaxTopK;
+constexpr int kHeaderBytes = (kOffGate + 4 * kMaxTopK + 127) / 128 * 128;
 
 // What the producer put in a ring slot: rows [r0, r0 + nr) of segment `seg`, with
 // activation row `xrow`.  nr == 0 marks the end of the CTA's stages.
@@ -191,10 +200,10 @@ template <int M, int R, int MODE, int XIN>
 __global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[8] | empty[8]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 8 * (2 * kMaxStages + 1));
-  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + 160);
-  int32_t* s_ids = reinterpret_cast<int32_t*>(smem + 160 + 16 * kMaxStages);
-  float* s_gate = reinterpret_cast<float*>(s_ids + kMaxTopK);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + kOffMeta);
+  int32_t* s_ids = reinterpret_cast<int32_t*>(smem + kOffIds);
+  float* s_gate = reinterpret_cast<float*>(smem + kOffGate);
   int8_t* xs = reinterpret_cast<int8_t*>(smem + p.off_x);
   float* xds = reinterpret_cast<float*>(smem + p.off_xd);
   unsigned char* ring = smem + p.off_ring;
@@ -212,7 +221,7 @@ __global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kern
   auto full_bar = [&](int i) { return smem_addr(bars + i); };
   auto empty_bar = [&](int i) { return smem_addr(bars + kMaxStages + i); };
 
-  pdl_launch_dependents();
+  if (MODE == kDense) pdl_launch_dependents();
   // Start-up.  The producer warp initialises the barriers (and, for routed
   // products, loads the routing), signals the consumers with a non-blocking arrive
   // on named barrier 2 and starts streaming at once; the consumers build the slice
@@ -227,7 +236,9 @@ __global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kern
       mbar_init_fence();
     }
     if (MODE != kDense) {
-      pdl_wait();  // ids and gate weights may come from the preceding kernel
+      // ids and gate weights may come from the preceding kernel (L2 reads: never a
+      // stale L1 line).
+      if (!p.routing_ready) pdl_wait();
       load_routing<MODE>(p, s_ids, s_gate, lane, 32);
     }
     if (MODE == kMoeGated) {
@@ -239,6 +250,10 @@ __global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kern
     fill_slice_table(s_slice, p.cpr, S, threadIdx.x - 32, kTmaThreads - 32);
     asm volatile("bar.sync 2, %0;" ::"n"(kTmaThreads) : "memory");
   }
+  // A routed product lets the next kernel launch only once its routing has been
+  // read after the wait for its own predecessor, so that a following kernel of the
+  // same call (routing_ready) can read the same routing before it waits.
+  if (MODE != kDense) pdl_launch_dependents();
 
   const int nseg = num_segs<MODE>(p, u0, u1);
   auto seg_of = [&](int si) { return get_seg<MODE>(p, u0, u1, si, s_ids); };
@@ -598,7 +613,9 @@ __global__ void __launch_bounds__(kRegThreads, reg_ctas_per_sm(M)) q8_reg_kernel
     }
   };
 
-  pdl_launch_dependents();
+  // Routed products signal their dependents only after the routing has been read
+  // behind the wait (a following kernel of the same call may rely on that).
+  if (MODE == kDense) pdl_launch_dependents();
   // Dense products stream weights that the preceding kernel does not write: the
   // first group of this warp's first task is requested before waiting for it.
   bool prefetched = false;
@@ -617,7 +634,10 @@ __global__ void __launch_bounds__(kRegThreads, reg_ctas_per_sm(M)) q8_reg_kernel
   }
   fill_slice_table(s_slice, p.cpr, S, threadIdx.x, kRegThreads);
   pdl_wait();
-  if (MODE != kDense) load_routing<MODE>(p, s_ids, s_gate, threadIdx.x, kRegThreads);
+  if (MODE != kDense) {
+    load_routing<MODE>(p, s_ids, s_gate, threadIdx.x, kRegThreads);
+    pdl_launch_dependents();
+  }
   stage_x_split<XIN>(p, xs, xds, warp, kRegWarps, lane, threadIdx.x, kRegThreads);
   __syncthreads();
 
@@ -801,12 +821,16 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   if (!aligned(p.wd, 16) || !aligned(p.wq, 16)) return false;
   if (XIN == kXq8 && (!aligned(p.xd, 16) || !aligned(p.xq, 16))) return false;
   const size_t row_bytes = (size_t)p.K + (size_t)p.nb * 2;
+  const int64_t maxu = max_units_per_cta(p.units, grid);
   int rps = (int)std::max<size_t>(1, tune.stage_target / row_bytes);
+  // A stage never spans two segments, and no segment is longer than a CTA's share
+  // of the units (routed: of one expert's rows): size stages, and so the ring's
+  // depth, by what a stage can actually hold.
+  rps = (int)std::min<int64_t>(rps, MODE == kMoeUngated ? std::min<int64_t>(maxu, p.N) : maxu);
   rps = std::max(R, rps / R * R);
   const size_t stage = align_up((size_t)rps * p.K, 128) + align_up((size_t)rps * p.nb * 2, 128);
   const size_t xbytes =
       align_up((size_t)p.xrows * p.K, 128) + align_up((size_t)p.xrows * p.nb * 4, 128);
-  const int64_t maxu = max_units_per_cta(p.units, grid);
   const size_t yacc = MODE == kMoeGated ? align_up((size_t)maxu * 4, 16) : 0;
   const size_t fixed = kHeaderBytes + xbytes + yacc + align_up((size_t)(p.S + 1) * 4, 16);
   const size_t part_per_stage = align_up((size_t)rps * p.S * M * 4, 16);
@@ -872,6 +896,14 @@ memra_status launch(Kern kernel, int64_t grid, int threads, size_t smem, cudaStr
   return MEMRA_OK;
 }
 
+// CTAs per SM in a register-kernel grid: the occupancy the kernel is built for,
+// or fewer (MEMRA_REG_CTAS_PER_SM, read once per process).
+int reg_grid_ctas_per_sm(int M) {
+  static const long v = env_long("MEMRA_REG_CTAS_PER_SM", 0, 0);
+  const int built = reg_ctas_per_sm(M);
+  return v > 0 && v < built ? (int)v : built;
+}
+
 template <int M, int R, int MODE, int XIN>
 memra_status run_product(Params p, cudaStream_t stream) {
   DeviceInfo info;
@@ -889,7 +921,7 @@ memra_status run_product(Params p, cudaStream_t stream) {
     }
     return launch(q8_tma_kernel<M, R, MODE, XIN>, grid, kTmaThreads, smem, stream, p);
   }
-  grid = std::min<int64_t>(p.units, (int64_t)info.sms * reg_ctas_per_sm(M));
+  grid = std::min<int64_t>(p.units, (int64_t)info.sms * reg_grid_ctas_per_sm(M));
   if (plan_reg<M, R, MODE, XIN>(p, info, grid, &smem))
     return launch(q8_reg_kernel<M, R, MODE, XIN>, grid, kRegThreads, smem, stream, p);
   return MEMRA_ERR_UNSUPPORTED;
@@ -1084,6 +1116,7 @@ extern "C" memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* g
   b.E = E;
   b.xpe = 1;
   b.status = dev_status;
+  b.routing_ready = 1;  // the gate|up kernel above waited for the routing
   b.units = H;
   return run_product<1, 1, kMoeGated, kXswiglu>(b, stream);
 }

@@ -110,34 +110,67 @@ __device__ __forceinline__ void load_x_group(const void* xin, int g, int K, floa
 
 // Quantise `rows` activation rows of K values (bf16 bits, fp32, or SwiGLU of gate|up
 // pairs) into the shared-memory q8_1 planes (natural layout).  Called by `nwarps`
-// whole warps (warp index w).  Each round a lane loads U groups before quantising
-// any of them, so the prologue pays one memory latency per U groups.
+// whole warps (warp index w).  Thread t = 32w + lane takes groups t, t + T, t + 2T,
+// ... (T = 32 nwarps; four consecutive lanes hold one 32-value block) and issues the
+// loads of up to U of them before quantising any, so the prologue pays one memory
+// latency per U T groups; bf16 rows are loaded raw (16 bytes a group), which lets U
+// reach 6, enough for any K <= 18432 in a single round with 12 warps.
 template <int XIN>
 __device__ __forceinline__ void quantize_rows_to_smem(const void* xin, int rows, int K,
                                                       int8_t* xs, float* xds, int w, int nwarps,
                                                       int lane) {
-  constexpr int U = 2;
+  constexpr int U = XIN == kXbf16 ? 6 : 2;
   const int groups = rows * K / 8;  // fits: rows * K is bounded by MEMRA_MAX_X_BYTES
-  for (int base = w * 32 * U; base < groups; base += nwarps * 32 * U) {
-    float v[U][8];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int g = base + u * 32 + lane;
-      if (g < groups) {
-        load_x_group<XIN>(xin, g, K, v[u]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[u][i] = 0.0f;
-      }
+  const int T = nwarps * 32;
+  const int t = w * 32 + lane;
+  auto store = [&](int g, const float (&v)[8]) {
+    float d;
+    const uint2 q = q8_1_group8(v, &d);
+    if (g < groups) {
+      *reinterpret_cast<uint2*>(xs + (size_t)g * 8) = q;
+      if ((lane & 3) == 0) xds[g >> 2] = d;
     }
+  };
+  for (int base = 0; base < groups; base += U * T) {
+    if (base + w * 32 >= groups) break;  // warp-uniform: no group of this warp is left
+    if (XIN == kXbf16) {
+      uint4 raw[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int g = base + u * 32 + lane;
-      float d;
-      const uint2 q = q8_1_group8(v[u], &d);
-      if (g < groups) {
-        *reinterpret_cast<uint2*>(xs + (size_t)g * 8) = q;
-        if ((lane & 3) == 0) xds[g >> 2] = d;
+      for (int u = 0; u < U; ++u) {
+        const int g = base + u * T + t;
+        raw[u] = g < groups
+                     ? *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(xin) +
+                                                       (size_t)g * 8)
+                     : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (base + u * T + w * 32 >= groups) break;  // warp-uniform
+        const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[2 * i] = __uint_as_float(wv[i] << 16);
+          v[2 * i + 1] = __uint_as_float(wv[i] & 0xffff0000u);
+        }
+        store(base + u * T + t, v);
+      }
+    } else {
+      float v[U][8];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int g = base + u * T + t;
+        if (g < groups) {
+          load_x_group<XIN>(xin, g, K, v[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[u][i] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (base + u * T + w * 32 >= groups) break;  // warp-uniform
+        store(base + u * T + t, v[u]);
       }
     }
   }
