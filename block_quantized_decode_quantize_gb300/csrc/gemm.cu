@@ -14,7 +14,8 @@
 // Two kernels implement it.
 //
 // q8_tma_kernel (the GB300 path; K % 256 == 0 and 16-byte aligned planes): two
-//   CTAs per SM, each owning a contiguous range of weight rows (or, for the routed
+//   CTAs per SM for M = 1 (one, with a deeper ring and more registers per thread,
+//   for M > 1), each owning a contiguous range of weight rows (or, for the routed
 //   product, a few contiguous row ranges, one per selected expert).  Warp 0 is the
 //   producer: one lane streams whole rows of the quant and scale planes into a ring
 //   of shared-memory stages with cp.async.bulk, completing on per-stage mbarriers,
@@ -55,6 +56,14 @@
 #endif
 #ifndef MEMRA_TMA_SMEM_LIMIT_KB
 #define MEMRA_TMA_SMEM_LIMIT_KB 113
+#endif
+// M > 1 products: one CTA per SM (the consumers need more registers) with a deeper
+// ring of larger stages (measured on GB300: 200 KB of 44 KB stages).
+#ifndef MEMRA_TMA_MULTI_RING_KB
+#define MEMRA_TMA_MULTI_RING_KB 200
+#endif
+#ifndef MEMRA_TMA_MULTI_STAGE_KB
+#define MEMRA_TMA_MULTI_STAGE_KB 44
 #endif
 // Dense products below this many MB of weights use the register kernel.
 #ifndef MEMRA_TMA_DENSE_MIN_MB
@@ -197,7 +206,8 @@ struct StageMeta {
 };
 
 template <int M, int R, int MODE, int XIN>
-__global__ void __launch_bounds__(kTmaThreads, MEMRA_TMA_MIN_BLOCKS) q8_tma_kernel(const Params p) {
+__global__ void __launch_bounds__(kTmaThreads, M == 1 ? MEMRA_TMA_MIN_BLOCKS : 1)
+    q8_tma_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[8] | empty[8]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
@@ -765,6 +775,9 @@ struct TmaTuning {
   size_t ring_budget;     // bytes of ring per CTA
   size_t smem_pair_limit; // shared memory of one CTA when two must fit on an SM
   int ctas_per_sm;
+  size_t multi_ring_budget;  // M > 1: bytes of ring per CTA (one CTA per SM)
+  size_t multi_stage_target; // M > 1: bytes per ring stage
+  bool multi_default;        // M > 1 products use this kernel by default
   int64_t dense_min_bytes;  // smaller dense products use the register kernel
 };
 
@@ -784,6 +797,11 @@ const TmaTuning& tma_tuning() {
     r.ring_budget = (size_t)env_long("MEMRA_TMA_RING_KB", MEMRA_TMA_RING_KB, 1) * 1024;
     r.smem_pair_limit =
         (size_t)env_long("MEMRA_TMA_SMEM_LIMIT_KB", MEMRA_TMA_SMEM_LIMIT_KB, 1) * 1024;
+    r.multi_ring_budget =
+        (size_t)env_long("MEMRA_TMA_MULTI_RING_KB", MEMRA_TMA_MULTI_RING_KB, 1) * 1024;
+    r.multi_stage_target =
+        (size_t)env_long("MEMRA_TMA_MULTI_STAGE_KB", MEMRA_TMA_MULTI_STAGE_KB, 1) * 1024;
+    r.multi_default = env_long("MEMRA_TMA_MULTI", 1, 0) != 0;
     r.ctas_per_sm = (int)env_long("MEMRA_TMA_CTAS_PER_SM", MEMRA_TMA_CTAS_PER_SM, 1);
     r.dense_min_bytes =
         (int64_t)env_long("MEMRA_TMA_DENSE_MIN_MB", MEMRA_TMA_DENSE_MIN_MB, 0) * 1024 * 1024;
@@ -794,9 +812,10 @@ const TmaTuning& tma_tuning() {
 
 // Kernel selection seam for tests and benchmarks (read once per process):
 // MEMRA_GEMV_PATH=reg forces the register kernel; MEMRA_GEMV_PATH=tma uses the
-// bulk-copy kernel wherever it applies, also for M > 1.  By default the bulk-copy
-// kernel serves M = 1 products (decode GEMV of at least ~24 MB of weights, and
-// routed experts) and the register kernel the rest.
+// bulk-copy kernel wherever it applies, whatever the size.  By default the bulk-copy
+// kernel serves products of at least ~24 MB of weights (M = 1 and M > 1), routed
+// experts, and the register kernel the rest (small products, K % 256 != 0, planes
+// not 16-byte aligned).
 int gemv_path_override() {
   static const int v = [] {
     const char* e = std::getenv("MEMRA_GEMV_PATH");
@@ -813,7 +832,7 @@ template <int M, int R, int MODE, int XIN>
 bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out) {
   const int path = gemv_path_override();
   const TmaTuning& tune = tma_tuning();
-  if (path == 1 || (path == 0 && M > 1)) return false;
+  if (path == 1 || (path == 0 && M > 1 && !tune.multi_default)) return false;
   // Per-shape dispatch: below a few tens of MB of weights the register kernel's
   // faster start wins over the deeper bulk-copy stream (measured on GB300).
   if (path == 0 && MODE == kDense && p.units * p.K < tune.dense_min_bytes) return false;
@@ -822,7 +841,8 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   if (XIN == kXq8 && (!aligned(p.xd, 16) || !aligned(p.xq, 16))) return false;
   const size_t row_bytes = (size_t)p.K + (size_t)p.nb * 2;
   const int64_t maxu = max_units_per_cta(p.units, grid);
-  int rps = (int)std::max<size_t>(1, tune.stage_target / row_bytes);
+  int rps = (int)std::max<size_t>(1, (M > 1 ? tune.multi_stage_target : tune.stage_target) /
+                                          row_bytes);
   // A stage never spans two segments, and no segment is longer than a CTA's share
   // of the units (routed: of one expert's rows): size stages, and so the ring's
   // depth, by what a stage can actually hold.
@@ -834,10 +854,14 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   const size_t yacc = MODE == kMoeGated ? align_up((size_t)maxu * 4, 16) : 0;
   const size_t fixed = kHeaderBytes + xbytes + yacc + align_up((size_t)(p.S + 1) * 4, 16);
   const size_t part_per_stage = align_up((size_t)rps * p.S * M * 4, 16);
-  // Ring: up to the budget, and within the two-CTAs-per-SM limit when possible.
-  size_t limit = std::max<size_t>(tune.smem_pair_limit, fixed + 2 * (stage + part_per_stage));
+  // Ring: up to the budget, and within the two-CTAs-per-SM limit when possible.  M > 1
+  // products run one CTA per SM (their consumers need more registers) with a deeper
+  // ring.
+  size_t limit = M > 1 ? (size_t)info.max_smem_optin
+                       : std::max<size_t>(tune.smem_pair_limit, fixed + 2 * (stage + part_per_stage));
   limit = std::min<size_t>(limit, (size_t)info.max_smem_optin);
-  int ns = (int)std::min<size_t>(kMaxStages, std::max<size_t>(2, tune.ring_budget / stage));
+  const size_t budget = M > 1 ? tune.multi_ring_budget : tune.ring_budget;
+  int ns = (int)std::min<size_t>(kMaxStages, std::max<size_t>(2, budget / stage));
   while (ns > 2 && fixed + ns * (stage + part_per_stage) > limit) --ns;
   if (ns < 2 || fixed + ns * (stage + part_per_stage) > (size_t)info.max_smem_optin) return false;
   p.rps = rps;
@@ -911,7 +935,7 @@ memra_status run_product(Params p, cudaStream_t stream) {
   p.nb = (int)(p.K / 32);
   p.cpr = (p.nb + 31) / 32;
   p.S = slices_for(p.cpr);
-  int64_t grid = std::min<int64_t>(p.units, (int64_t)info.sms * tma_tuning().ctas_per_sm);
+  int64_t grid = std::min<int64_t>(p.units, (int64_t)info.sms * (M > 1 ? 1 : tma_tuning().ctas_per_sm));
   size_t smem = 0;
   if (plan_tma<M, R, MODE, XIN>(p, info, grid, &smem)) {
     if (grid > info.sms && smem > tma_tuning().smem_pair_limit) {
