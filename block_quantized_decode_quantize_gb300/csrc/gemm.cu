@@ -185,8 +185,17 @@ __device__ __forceinline__ void load_routing(const Params& p, int32_t* s_ids, fl
 #ifndef MEMRA_TMA_CONSUMER_WARPS
 #define MEMRA_TMA_CONSUMER_WARPS 12
 #endif
-constexpr int kConsumerWarps = MEMRA_TMA_CONSUMER_WARPS;
-constexpr int kTmaThreads = 32 * (1 + kConsumerWarps);
+// M > 1 products run one CTA per SM, where dp4a issue rather than the stream limits
+// them.  With M <= 3 a task holds few accumulators and more consumer warps help
+// (measured: M = 2 at 20 warps 4.72 ms per sweep token, at 12 warps 5.01 ms); from
+// M = 4 on, more warps only shrink the register budget (M = 8 spills from 16 warps).
+#ifndef MEMRA_TMA_FEW_M_CONSUMER_WARPS
+#define MEMRA_TMA_FEW_M_CONSUMER_WARPS 20
+#endif
+__host__ __device__ constexpr int tma_consumer_warps(int M) {
+  return M == 1 || M > 3 ? MEMRA_TMA_CONSUMER_WARPS : MEMRA_TMA_FEW_M_CONSUMER_WARPS;
+}
+__host__ __device__ constexpr int tma_threads(int M) { return 32 * (1 + tma_consumer_warps(M)); }
 constexpr int kMaxStages = 16;
 // Shared-memory header: full[kMaxStages] | empty[kMaxStages] mbarriers, the abort
 // flag, the stage metadata, the routed ids and gate weights.
@@ -206,8 +215,10 @@ struct StageMeta {
 };
 
 template <int M, int R, int MODE, int XIN>
-__global__ void __launch_bounds__(kTmaThreads, M == 1 ? MEMRA_TMA_MIN_BLOCKS : 1)
+__global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS : 1)
     q8_tma_kernel(const Params p) {
+  constexpr int kConsumerWarps = tma_consumer_warps(M);
+  constexpr int kTmaThreads = tma_threads(M);
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[8] | empty[8]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
@@ -943,7 +954,7 @@ memra_status run_product(Params p, cudaStream_t stream) {
       grid = std::min<int64_t>(p.units, info.sms);
       if (!plan_tma<M, R, MODE, XIN>(p, info, grid, &smem)) return MEMRA_ERR_UNSUPPORTED;
     }
-    return launch(q8_tma_kernel<M, R, MODE, XIN>, grid, kTmaThreads, smem, stream, p);
+    return launch(q8_tma_kernel<M, R, MODE, XIN>, grid, tma_threads(M), smem, stream, p);
   }
   grid = std::min<int64_t>(p.units, (int64_t)info.sms * reg_grid_ctas_per_sm(M));
   if (plan_reg<M, R, MODE, XIN>(p, info, grid, &smem))
