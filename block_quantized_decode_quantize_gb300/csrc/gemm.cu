@@ -106,6 +106,9 @@ struct Params {
   // The routing was already waited for by the preceding kernel of the same call, and
   // that kernel let this one launch only after its own wait: read it at once.
   int routing_ready;
+  // Gated routed product whose CTA takes all of its top_k segments (rps rows each at
+  // most) in one packed stage: segment k's rows at stage rows [k*n, (k+1)*n).
+  int packed;
   // TMA kernel layout
   int rps;                 // rows per stage
   int ns;                  // stages in the ring
@@ -206,7 +209,9 @@ constexpr int kOffGate = kOffIds + 4 * kMaxTopK;
 constexpr int kHeaderBytes = (kOffGate + 4 * kMaxTopK + 127) / 128 * 128;
 
 // What the producer put in a ring slot: rows [r0, r0 + nr) of segment `seg`, with
-// activation row `xrow`.  nr == 0 marks the end of the CTA's stages.
+// activation row `xrow`.  nr == 0 marks the end of the CTA's stages.  A packed stage
+// (seg < 0) holds every routed segment of the CTA, xrow rows each, segment after
+// segment.
 struct StageMeta {
   int seg;
   int r0;
@@ -310,8 +315,25 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
     // Reduce the slice partials of the stage in `slot` into the outputs.
     auto epilogue = [&](int slot) {
       const StageMeta mt = meta[slot];
-      const Seg g = seg_of(mt.seg);
       const float* pp = part + (size_t)slot * p.rps * S * M;
+      if (MODE == kMoeGated && mt.seg < 0) {
+        // Packed stage: each output accumulates its segments in ascending k.
+        const int n = mt.xrow;
+        for (int i = lane; i < n; i += 32) {
+          float acc = yacc[i];
+          for (int k = 0; k < p.top_k; ++k) {
+            if (s_ids[k] < 0) continue;
+            const float* q = pp + (size_t)(k * n + i) * S;
+            float tot = q[0];
+            for (int s = 1; s < S; ++s) tot = __fadd_rn(tot, q[s]);
+            acc = __fadd_rn(acc, __fmul_rn(s_gate[k], tot));
+          }
+          yacc[i] = acc;
+        }
+        __syncwarp();
+        return;
+      }
+      const Seg g = seg_of(mt.seg);
       for (int i = lane; i < mt.nr * M; i += 32) {
         const int r = i / M;
         const int m = i - r * M;
@@ -363,9 +385,40 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       acquired = false;
     };
 
+    if (MODE == kMoeGated && p.packed) {
+      // One stage with every valid segment's rows, completing on one barrier: a
+      // stage costs its round trip through the consumers and the epilogue whatever
+      // its size, and the CTA's segments are only a few rows each.
+      const int n = (int)(u1 - u0);
+      if (acquire()) {
+        const int slot = issued % ns;
+        if (lane == 0) {
+          meta[slot] = StageMeta{-1, 0, p.top_k * n, n};
+          uint32_t bytes = 0;
+          for (int k = 0; k < p.top_k; ++k)
+            if (s_ids[k] >= 0) bytes += (uint32_t)(n * (p.K + nb * 2));
+          const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
+          // With no valid segment (bytes == 0) this arrival alone completes the stage.
+          mbar_arrive_expect_tx(full_bar(slot), bytes);
+          for (int k = 0; k < p.top_k; ++k) {
+            if (s_ids[k] < 0) continue;
+            const int64_t row0 = (int64_t)s_ids[k] * p.N + u0;
+            bulk_g2s_hint(dst + (uint32_t)(k * n) * (uint32_t)p.K, p.wq + row0 * p.K,
+                          (uint32_t)(n * p.K), full_bar(slot), policy);
+            bulk_g2s_hint(dst + p.wd_off + (uint32_t)(k * n * nb * 2), p.wd + row0 * nb,
+                          (uint32_t)(n * nb * 2), full_bar(slot), policy);
+          }
+        }
+        __syncwarp();
+        ++issued;
+        acquired = false;
+      } else {
+        ok = false;
+      }
+    }
     for (;;) {
       StageMeta m;
-      if (!static_next(m)) break;
+      if ((MODE == kMoeGated && p.packed) || !static_next(m)) break;
       if (!acquire()) {
         ok = false;
         break;
@@ -441,7 +494,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       const StageMeta mt = meta[slot];
       if (mt.nr <= 0) break;
       const int nr = mt.nr;
-      const int xrow = mt.xrow;
+      const bool packed_stage = MODE == kMoeGated && mt.seg < 0;  // R == 1 there
       const int groups = (nr + R - 1) / R;
       const int ntasks = groups * S;
       const int t0 =
@@ -455,6 +508,12 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         const int gi = t / S;
         const int s = t - gi * S;
         const int rbase = gi * R;
+        int xrow = mt.xrow;
+        if (packed_stage) {
+          const int k = rbase / mt.xrow;
+          if (s_ids[k] < 0) continue;  // not copied; its partials are never read
+          xrow = p.xpe ? k : 0;
+        }
         const int plo = s_slice[s];
         const int phi = s_slice[s + 1];
         // Per-lane pointers at the task's first block; a part is 1024 bytes on.
@@ -786,6 +845,7 @@ struct TmaTuning {
   size_t ring_budget;     // bytes of ring per CTA
   size_t smem_pair_limit; // shared memory of one CTA when two must fit on an SM
   int ctas_per_sm;
+  size_t packed_max;         // gated routed: largest packed stage (bytes)
   size_t multi_ring_budget;  // M > 1: bytes of ring per CTA (one CTA per SM)
   size_t multi_stage_target; // M > 1: bytes per ring stage
   bool multi_default;        // M > 1 products use this kernel by default
@@ -808,6 +868,7 @@ const TmaTuning& tma_tuning() {
     r.ring_budget = (size_t)env_long("MEMRA_TMA_RING_KB", MEMRA_TMA_RING_KB, 1) * 1024;
     r.smem_pair_limit =
         (size_t)env_long("MEMRA_TMA_SMEM_LIMIT_KB", MEMRA_TMA_SMEM_LIMIT_KB, 1) * 1024;
+    r.packed_max = (size_t)env_long("MEMRA_TMA_PACKED_KB", 48, 0) * 1024;
     r.multi_ring_budget =
         (size_t)env_long("MEMRA_TMA_MULTI_RING_KB", MEMRA_TMA_MULTI_RING_KB, 1) * 1024;
     r.multi_stage_target =
@@ -859,12 +920,19 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   // depth, by what a stage can actually hold.
   rps = (int)std::min<int64_t>(rps, MODE == kMoeUngated ? std::min<int64_t>(maxu, p.N) : maxu);
   rps = std::max(R, rps / R * R);
-  const size_t stage = align_up((size_t)rps * p.K, 128) + align_up((size_t)rps * p.nb * 2, 128);
+  // Gated routed products whose segments are a few rows each pack all of a CTA's
+  // segments into one stage.
+  p.packed = 0;
+  if (MODE == kMoeGated && R == 1 && (size_t)p.top_k * maxu * row_bytes <= tune.packed_max) {
+    p.packed = 1;
+    rps = (int)(p.top_k * maxu);
+  }
+  size_t stage = align_up((size_t)rps * p.K, 128) + align_up((size_t)rps * p.nb * 2, 128);
   const size_t xbytes =
       align_up((size_t)p.xrows * p.K, 128) + align_up((size_t)p.xrows * p.nb * 4, 128);
   const size_t yacc = MODE == kMoeGated ? align_up((size_t)maxu * 4, 16) : 0;
   const size_t fixed = kHeaderBytes + xbytes + yacc + align_up((size_t)(p.S + 1) * 4, 16);
-  const size_t part_per_stage = align_up((size_t)rps * p.S * M * 4, 16);
+  size_t part_per_stage = align_up((size_t)rps * p.S * M * 4, 16);
   // Ring: up to the budget, and within the two-CTAs-per-SM limit when possible.  M > 1
   // products run one CTA per SM (their consumers need more registers) with a deeper
   // ring.
@@ -873,6 +941,19 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   limit = std::min<size_t>(limit, (size_t)info.max_smem_optin);
   const size_t budget = M > 1 ? tune.multi_ring_budget : tune.ring_budget;
   int ns = (int)std::min<size_t>(kMaxStages, std::max<size_t>(2, budget / stage));
+  // A dense product whose CTA share is a little more than the ring holds: stretch the
+  // stages so that the whole share is in flight at once (no stage waits for a slot).
+  if (MODE == kDense && maxu > (int64_t)ns * rps) {
+    const int wide = (int)((maxu + ns - 1) / ns + R - 1) / R * R;
+    const size_t wstage =
+        align_up((size_t)wide * p.K, 128) + align_up((size_t)wide * p.nb * 2, 128);
+    const size_t wpart = align_up((size_t)wide * p.S * M * 4, 16);
+    if (wide <= 2 * rps && fixed + ns * (wstage + wpart) <= limit) {
+      rps = wide;
+      stage = wstage;
+      part_per_stage = wpart;
+    }
+  }
   while (ns > 2 && fixed + ns * (stage + part_per_stage) > limit) --ns;
   if (ns < 2 || fixed + ns * (stage + part_per_stage) > (size_t)info.max_smem_optin) return false;
   p.rps = rps;

@@ -228,6 +228,42 @@ def test_moe_bad_ids_flagged_and_skipped(mem, orc):
     assert_within(np_(yg), yg_ref, 0.5 * terms, "moe bad ids gated")
 
 
+def test_moe_gated_packed_stage_with_bad_ids(mem, orc):
+    """Gated routed products pack all of a CTA's expert segments into one ring stage.
+    Here each CTA owns several rows per segment, one id in the middle is out of range
+    and one is negative (both skipped), and a second call has no valid id at all (its
+    stage carries no bytes; the output must be exact zeros)."""
+    E, N, K = 8, 1000, 512
+    w, wq, wd = make_bank(mem, E, N, K, 41)
+    oq, od = orc.quantize_q8_0(np_(w).reshape(E * N, K))
+    oq = oq.reshape(E, N, K)
+    od = od.reshape(E, N, K // 32)
+    x = synth.activations_bf16(5, K, 42)
+    xq, xd = mem.memra_quantize_q8_1(x.cuda())
+    oxq, oxd = check_acts(orc, x, xq, xd)
+    ids = torch.tensor([3, -1, 5, 99, 0], dtype=torch.int32)
+    gw = torch.tensor([0.3, 0.1, 0.25, 0.15, 0.2], dtype=torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = mem.memra_q8_0_moe_gemv(wq, wd, ids.cuda(), gw.cuda(), xq, xd, True, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    y_ref, bad = orc.moe_gemv(oq, od, np_(ids), np_(gw), oxq, oxd, 1)
+    assert bad == 2
+    terms = np.zeros(N)
+    for k, e in enumerate(np_(ids)):
+        if 0 <= e < E:
+            t = abs_terms(orc.block_dots(oq[e], oxq[k:k + 1]), od[e], oxd[k:k + 1])[0]
+            terms += abs(float(gw[k])) * t
+    assert_within(np_(y), y_ref, terms, "gated packed stage, bad ids")
+    bad_ids = torch.tensor([-4, 8, 1 << 20], dtype=torch.int32, device="cuda")
+    status.zero_()
+    y0 = mem.memra_q8_0_moe_gemv(wq, wd, bad_ids, gw[:3].contiguous().cuda(), xq[:3].contiguous(),
+                                 xd[:3].contiguous(), True, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    assert torch.all(y0 == 0)
+
+
 @pytest.mark.parametrize("R,F", [(8, 768), (1, 32), (3, 2048)])
 def test_swiglu_quantize_bit_exact(mem, orc, R, F):
     gu = synth.normal((R, 2 * F), 41, R, F, std=3.0)
