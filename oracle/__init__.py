@@ -35,6 +35,8 @@ def lib():
         L.oracle_exp_cw.argtypes = [ctypes.c_float]
         L.oracle_exp_cw.restype = ctypes.c_float
         L.oracle_quantize_q8_0.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
+        L.oracle_quantize_q4_0.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
+        L.oracle_unpack_q4_0.argtypes = [_ptr, _i64, _i64, _ptr]
         L.oracle_quantize_q8_1_f32.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         L.oracle_quantize_q8_1_bf16.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         L.oracle_block_dots.argtypes = [_ptr, _i64, _i64, _ptr, _i64, _ptr]
@@ -101,6 +103,31 @@ def quantize_q8_0(w):
     d = np.empty((N, K // 32), np.uint16)
     lib().oracle_quantize_q8_0(_p(w), N, K, _p(q), _p(d))
     return q, d
+
+
+def quantize_q4_0(w):
+    """Weights fp32 [N, K] -> (q4 uint8 [N, K/2] packed codes, wd fp16 bits uint16 [N, K/32])."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert K % 32 == 0
+    q4 = np.empty((N, K // 2), np.uint8)
+    d = np.empty((N, K // 32), np.uint16)
+    lib().oracle_quantize_q4_0(_p(w), N, K, _p(q4), _p(d))
+    return q4, d
+
+
+def unpack_q4_0(q4):
+    """Packed Q4_0 codes uint8 [N, K/2] -> signed int8 values q - 8, [N, K]."""
+    q4 = _c(q4, np.uint8)
+    N, K2 = q4.shape
+    wq = np.empty((N, 2 * K2), np.int8)
+    lib().oracle_unpack_q4_0(_p(q4), N, 2 * K2, _p(wq))
+    return wq
+
+
+def gemm_q4_0(q4, wd, xq, xd, threads=1):
+    """y[M, N] float32 = Q4_0 W times q8_1 x: the Q8_0 product of the unpacked codes."""
+    return gemm(unpack_q4_0(q4), wd, xq, xd, threads=threads)
 
 
 def quantize_q8_1(x):

@@ -154,6 +154,63 @@ void oracle_quantize_q8_0(const float* w, int64_t N, int64_t K, int8_t* q, uint1
 }
 
 // ---------------------------------------------------------------------------
+// Weight ingest to Q4_0 (the pages' other split-plane decode format; memra wiki,
+// feature list: "NVFP4 / Q4_0 / Q8_0 decode -- split-plane repacked matvecs").  The
+// pages name the format and print nothing of it; the reading here is GGUF's Q4_0
+// block restated: 32 consecutive weights of a row share one fp16 scale d and carry
+// unsigned 4-bit codes q in [0, 15] with w ~= d * (q - 8).
+//   m  = the block element of largest magnitude (the first one on a tie);
+//   d  = fp16_rne(m / -8), so that m itself maps to q - 8 = -8 (d = +0 when the
+//        block is all zeros);
+//   q  = clamp(round-half-away(w / float(d)) + 8, 0, 15); d == 0 gives q = 8.
+// Split planes: q4 [N][K/2] bytes and d [N][K/32] fp16 bits.  Byte j < 16 of a
+// block holds element j in its low nibble and element j + 16 in its high nibble.
+// ---------------------------------------------------------------------------
+void oracle_quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* q4, uint16_t* d) {
+  const int64_t nb = K / 32;
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* blk = w + n * K + b * 32;
+      float m = 0.0f;
+      float amax = 0.0f;
+      for (int i = 0; i < 32; ++i) {
+        if (std::fabs(blk[i]) > amax) {
+          amax = std::fabs(blk[i]);
+          m = blk[i];
+        }
+      }
+      const uint16_t d16 = amax == 0.0f ? (uint16_t)0 : f16_rne(m / -8.0f);  // +0 if all zero
+      const float dv = f16_to_f32(d16);
+      d[n * nb + b] = d16;
+      int code[32];
+      for (int i = 0; i < 32; ++i) {
+        if (dv == 0.0f) {
+          code[i] = 8;
+        } else {
+          int c = (int)std::roundf(blk[i] / dv) + 8;
+          code[i] = c < 0 ? 0 : (c > 15 ? 15 : c);
+        }
+      }
+      uint8_t* out = q4 + n * (K / 2) + b * 16;
+      for (int j = 0; j < 16; ++j) out[j] = (uint8_t)(code[j] | (code[j + 16] << 4));
+    }
+  }
+}
+
+// Q4_0 codes as signed int8 values q - 8, row-major [N][K]: the weight operand of
+// the block dot.  With them the Q4_0 product is the Q8_0 product below, term for
+// term: y[m][n] = sum_b (d_w * d_x) * s_b with s_b = sum_i (q_i - 8) * xq_i.
+void oracle_unpack_q4_0(const uint8_t* q4, int64_t N, int64_t K, int8_t* wq) {
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t b = 0; b < K / 32; ++b)
+      for (int j = 0; j < 16; ++j) {
+        const uint8_t byte = q4[n * (K / 2) + b * 16 + j];
+        wq[n * K + b * 32 + j] = (int8_t)((int)(byte & 0x0F) - 8);
+        wq[n * K + b * 32 + j + 16] = (int8_t)((int)(byte >> 4) - 8);
+      }
+}
+
+// ---------------------------------------------------------------------------
 // Activation quantisation ("q8_1" blocks with an fp32 scale).
 // x: [M][K] fp32 or bf16 bits.  q: int8 [M][K].  d: fp32 [M][K/32].
 // Per block: amax = max|x|; d = amax / 127 in fp32; q = clamp(round-half-away(

@@ -42,3 +42,18 @@ def test_small_gemm_fixture(orc):
     assert orc.block_dots(wq, xq).ravel().tolist() == g["block_sums"]
     y = orc.gemm(wq, wd, xq, xd)
     assert np.array_equal(y.view(np.uint32), from_hex(g["y_f32_hex"], (M, N)).view(np.uint32))
+
+
+def test_q4_0_hand_block(orc):
+    g = load("q4_0_hand_block.json")
+    w = np.array(g["w"], np.float32)[None]
+    q4, wd = orc.quantize_q4_0(w)
+    assert q4.ravel().tolist() == g["packed"] and int(wd[0, 0]) == g["wd_f16_bits"]
+    assert (orc.unpack_q4_0(q4).ravel() + 8).tolist() == g["codes"]
+    x = np.array(g["x"], np.float32)[None]
+    xq, xd = orc.quantize_q8_1(x)
+    assert int(orc.block_dots(orc.unpack_q4_0(q4), xq)[0, 0, 0]) == g["block_sum"]
+    assert float(orc.gemm_q4_0(q4, wd, xq, xd)[0, 0]) == g["y"]
+    tq4, twd = orc.quantize_q4_0(np.array(g["tie_w"], np.float32)[None])
+    assert (orc.unpack_q4_0(tq4).ravel() + 8).tolist() == g["tie_codes"]
+    assert int(twd[0, 0]) == g["tie_wd_f16_bits"]

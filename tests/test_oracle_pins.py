@@ -468,3 +468,97 @@ def test_moe_ffn_single_expert_is_dense_ffn(orc):
     h = g_u[:F] / (1 + np.exp(-g_u[:F])) * g_u[F:]
     y64 = wdn[0].astype(np.float64) @ h
     assert np.max(np.abs(y - y64)) < 0.05 * np.max(np.abs(y64)) + 1e-6
+
+
+# ----------------------------------------------------------------------------
+# Q4_0 weights: packing, quantiser invariants and the product.
+# ----------------------------------------------------------------------------
+
+def _np_unpack_q4_0(q4):
+    """Independent numpy unpack: byte j of a block -> element j (low nibble) and
+    element j + 16 (high nibble); values q - 8."""
+    N, K2 = q4.shape
+    b = q4.reshape(N, K2 // 16, 16).astype(np.int16)
+    lo = (b & 0x0F) - 8
+    hi = (b >> 4) - 8
+    return np.concatenate([lo, hi], axis=2).reshape(N, 2 * K2).astype(np.int8)
+
+
+def test_q4_0_unpack_matches_hand_packing(orc):
+    r = rng(40)
+    codes = r.integers(0, 16, size=(5, 96))
+    blocks = codes.reshape(5, 3, 32)
+    packed = (blocks[:, :, :16] | (blocks[:, :, 16:] << 4)).astype(np.uint8).reshape(5, 48)
+    assert np.array_equal(orc.unpack_q4_0(packed), (codes - 8).astype(np.int8))
+
+
+@pytest.mark.parametrize("std", [0.02, 1.0, 300.0])
+def test_q4_0_quant_invariants(orc, std):
+    r = rng(41 + int(std))
+    N, K = 40, 256
+    w = (r.standard_normal((N, K)) * std).astype(np.float32)
+    q4, d = orc.quantize_q4_0(w)
+    v = _np_unpack_q4_0(q4).astype(np.int64)          # q - 8
+    assert v.min() >= -8 and v.max() <= 7
+    dv = d.view(np.float16).astype(np.float64)
+    wb = w.astype(np.float64).reshape(N, K // 32, 32)
+    vb = v.reshape(N, K // 32, 32)
+    # the scale is numpy's fp16 of the first largest-magnitude element over -8
+    first = np.argmax(np.abs(wb), axis=2)
+    m = np.take_along_axis(wb, first[..., None], axis=2)[..., 0]
+    assert np.array_equal(d.view(np.float16), (m / -8.0).astype(np.float32).astype(np.float16))
+    # that element maps to -8
+    assert np.all(np.take_along_axis(vb, first[..., None], axis=2) == -8)
+    # round trip: within d/2 where the quotient is in range, within d where it clamps at +7
+    ratio = wb / dv[..., None]
+    err = np.abs(wb - dv[..., None] * vb)
+    inside = ratio <= 7.5
+    assert np.all(err[inside] <= np.abs(dv[..., None] * 0.5 + 0 * wb)[inside] * (1 + 2 ** -20))
+    assert np.all(vb[~inside] == 7)
+    assert np.all(err[~inside] <= np.abs(dv[..., None] + 0 * wb)[~inside] * (1 + 2 ** -9))
+
+
+def test_q4_0_zero_block_and_sign_and_scaling(orc):
+    r = rng(42)
+    w = (r.standard_normal((3, 128)) * 0.5).astype(np.float32)
+    w[1, 32:64] = 0.0
+    w[2, 64:96] = -0.0
+    q4, d = orc.quantize_q4_0(w)
+    v = _np_unpack_q4_0(q4)
+    assert int(d[1, 1]) == 0 and int(d[2, 2]) == 0          # +0 scale for zero blocks
+    assert np.all(v[1, 32:64] == 0) and np.all(v[2, 64:96] == 0)
+    # -w: the extreme flips sign, so the scale flips sign and every code is unchanged
+    q4n, dn = orc.quantize_q4_0(-w)
+    assert np.array_equal(q4n, q4)
+    nz = d != 0
+    assert np.array_equal(dn[nz], d[nz] ^ 0x8000)
+    # 4w: same codes, scales exactly 4x
+    q4s, ds = orc.quantize_q4_0(4 * w)
+    assert np.array_equal(q4s, q4)
+    assert np.array_equal(ds.view(np.float16).astype(np.float64),
+                          4 * d.view(np.float16).astype(np.float64))
+
+
+@pytest.mark.parametrize("N,K,M", [(7, 32, 1), (33, 544, 1), (16, 5120, 2), (9, 768, 8)])
+def test_q4_0_gemm_within_bound_of_fp64_brute_force(orc, N, K, M):
+    w, x = _case(50 + K, N, K, M)
+    q4, wd = orc.quantize_q4_0(w)
+    xq, xd = orc.quantize_q8_1(x)
+    y = orc.gemm_q4_0(q4, wd, xq, xd)
+    v = _np_unpack_q4_0(q4)
+    Wd = v.astype(np.float64) * np.repeat(wd.view(np.float16).astype(np.float64), 32, axis=1)
+    Xd = xq.astype(np.float64) * np.repeat(xd.astype(np.float64), 32, axis=1)
+    y64 = Xd @ Wd.T
+    nb = K // 32
+    s = np.einsum("mbi,nbi->mnb", xq.astype(np.int64).reshape(M, nb, 32),
+                  v.astype(np.int64).reshape(N, nb, 32)).astype(np.float64)
+    c = wd.view(np.float16).astype(np.float64)[None] * xd.astype(np.float64)[:, None, :]
+    terms = np.abs(c * s).sum(axis=2)
+    gamma = (nb + 2) * U32 / (1 - (nb + 2) * U32)
+    assert np.all(np.abs(y.astype(np.float64) - y64) <= gamma * terms + 1e-30)
+    # against the unquantised product: each weight is within |d|/2 (|d| where it clamps)
+    exact = x.astype(np.float64) @ w.astype(np.float64).T
+    dw = np.abs(np.repeat(wd.view(np.float16).astype(np.float64), 32, axis=1))
+    dx = np.repeat(xd.astype(np.float64), 32, axis=1)
+    qerr = np.abs(Xd) @ dw.T + (dx / 2) @ np.abs(Wd).T + (dx / 2) @ dw.T
+    assert np.all(np.abs(y - exact) <= qerr + 1e-4 * terms + 1e-6)
