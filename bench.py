@@ -39,7 +39,7 @@ METRIC = ("Q8_0 decode GEMV weight-stream GB/s (% of GB300 HBM peak); "
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8", "moe_top8",
-             "stress_lm_head")
+             "stress_lm_head", "dense27b_sweep_q4_0")
 
 
 # ----------------------------------------------------------------------------
@@ -47,10 +47,12 @@ WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8
 # ----------------------------------------------------------------------------
 
 class Gemv:
-    """One Q8_0 product of a step: weights, its bf16 activation(s), q8_1 buffers, y."""
+    """One product of a step: Q8_0 (wq int8 [N, K]) or Q4_0 (wq uint8 [N, K/2]) weights,
+    its bf16 activation(s), q8_1 buffers, y."""
 
     def __init__(self, wq, wd, x, name):
         self.wq, self.wd, self.x, self.name = wq, wd, x, name
+        self.fmt = "q4_0" if wq.dtype == torch.uint8 else "q8_0"
         M, K = x.shape
         N = wq.shape[0]
         dev = wq.device
@@ -60,26 +62,29 @@ class Gemv:
 
     @property
     def weight_bytes(self):
-        return synth.q8_0_bytes(*self.wq.shape)
+        return self.wq.numel() + self.wd.numel() * 2  # quant plane + fp16 scale plane
 
 
-def quantized_weights(mem, N, K, *keys, device, perturb=None):
+def quantized_weights(mem, N, K, *keys, device, perturb=None, fmt="q8_0"):
     w = synth.weights_fp32(N, K, *keys, device=device)
     if perturb:
         synth.perturb_blocks(w, *keys, **perturb)
-    wq, wd = mem.memra_quantize_q8_0(w)
+    if fmt == "q4_0":
+        wq, wd = mem.memra_quantize_q4_0(w)
+    else:
+        wq, wd = mem.memra_quantize_q8_0(w)
     del w
     return wq, wd
 
 
-def build_dense_sweep(mem, device, M=1, layers=None, workload_id=1):
+def build_dense_sweep(mem, device, M=1, layers=None, workload_id=1, fmt="q8_0"):
     """The dense 27B-class sweep: per layer QKV, O, gate+up, down."""
     cfg = synth.DENSE27B
     L = cfg["layers"] if layers is None else layers
     ops = []
     for layer in range(L):
         for t, (name, N, K) in enumerate(cfg["gemvs"]):
-            wq, wd = quantized_weights(mem, N, K, workload_id, layer, t, device=device)
+            wq, wd = quantized_weights(mem, N, K, workload_id, layer, t, device=device, fmt=fmt)
             x = synth.activations_bf16(M, K, workload_id, layer, t, 1000 + M,
                                        outlier_frac=cfg["outlier_frac"],
                                        outlier_scale=cfg["outlier_scale"], device=device)
@@ -148,10 +153,18 @@ def run_gemv_op(mem, op, quantize=True, fused=False):
     """One product of a step: the fused entry point (quantisation in the kernel's
     prologue), or a q8_1 quantise launch followed by the GEMV / verify GEMM."""
     if fused:
+        if op.fmt != "q8_0":
+            raise ValueError("the fused quantise entry point takes Q8_0 weights")
         mem.memra_q8_0_quant_gemm(op.wq, op.wd, op.x, y=op.y)
         return
     if quantize:
         mem.memra_quantize_q8_1(op.x, op.xq, op.xd)
+    if op.fmt == "q4_0":
+        if op.xq.shape[0] == 1:
+            mem.memra_q4_0_gemv(op.wq, op.wd, op.xq[0], op.xd[0], y=op.y[0])
+        else:
+            mem.memra_q4_0_gemm_small_m(op.wq, op.wd, op.xq, op.xd, y=op.y)
+        return
     if op.xq.shape[0] == 1:
         mem.memra_q8_0_gemv(op.wq, op.wd, op.xq[0], op.xd[0], y=op.y[0])
     else:
@@ -171,6 +184,9 @@ class Workload:
         self.ops = []
         if name == "dense27b_sweep":
             self.ops = build_dense_sweep(mem, device, M=1, layers=layers)
+        elif name == "dense27b_sweep_q4_0":
+            self.ops = build_dense_sweep(mem, device, M=1, layers=layers, workload_id=5,
+                                         fmt="q4_0")
         elif name.startswith("verify_m"):
             self.ops = build_dense_sweep(mem, device, M=int(name[len("verify_m"):]),
                                          layers=layers, workload_id=2)
@@ -185,8 +201,9 @@ class Workload:
             raise ValueError(name)
         self._pack_arenas()
         if chain:
-            if self.moe is not None or any(op.x.shape[0] != 1 for op in self.ops):
-                raise ValueError("--chain runs M = 1 dense products only")
+            if self.moe is not None or any(op.x.shape[0] != 1 or op.fmt != "q8_0"
+                                           for op in self.ops):
+                raise ValueError("--chain runs M = 1 dense Q8_0 products only")
             self.chain = mem.GemvChain([(op.wq, op.wd, op.x[0], op.y[0]) for op in self.ops])
         torch.cuda.synchronize(device)
 
@@ -487,10 +504,10 @@ class CpuOracleSample:
 
 def workload_config(name, wl):
     cfg = {"workload": name}
-    if name == "dense27b_sweep" or name.startswith("verify_m"):
+    if name.startswith("dense27b_sweep") or name.startswith("verify_m"):
         cfg.update({"layers": len(wl.ops) // 4, "hidden": synth.DENSE27B["hidden"],
                     "gemvs_per_layer": [[n, N, K] for n, N, K in synth.DENSE27B["gemvs"]],
-                    "M": 1 if name == "dense27b_sweep" else int(name[len("verify_m"):]),
+                    "M": int(name[len("verify_m"):]) if name.startswith("verify_m") else 1,
                     "activations": "bf16 N(0,1), 0.1% of entries x20"})
     elif name == "gemv_4096":
         cfg.update({"N": 4096, "K": 4096, "M": 1, "weight_copies": len(wl.ops)})
@@ -498,7 +515,9 @@ def workload_config(name, wl):
         cfg.update(dict(synth.MOE))
     elif name == "stress_lm_head":
         cfg.update({"shapes": [[n, N, K] for n, N, K in synth.STRESS["shapes"]], "M": [1, 8]})
-    cfg["weights"] = "N(0,0.02) fp32 quantised to Q8_0 (32 int8 + fp16 scale per block)"
+    cfg["weights"] = ("N(0,0.02) fp32 quantised to Q4_0 (32 4-bit codes + fp16 scale per block)"
+                      if name.endswith("q4_0") else
+                      "N(0,0.02) fp32 quantised to Q8_0 (32 int8 + fp16 scale per block)")
     cfg["weight_bytes_per_step"] = wl.weight_bytes
     cfg["l2"] = ("inputs larger than L2: %.2f GB of distinct weights per step vs 129 MB L2"
                  % (wl.weight_bytes / 1e9))
@@ -563,7 +582,8 @@ def run_memra(args):
                             if prof else None),
                 "peak_kind": peak_kind + " copy bandwidth (MEASURED_PEAKS hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "kernel": "Q8_0 product kernel (%s, M=%s)" % (
+                "kernel": "%s product kernel (%s, M=%s)" % (
+                    "Q4_0" if wl.ops and wl.ops[0].fmt == "q4_0" else "Q8_0",
                     "chained, one launch per step" if wl.chain is not None else
                     "routed experts" if wl.moe is not None else
                     ("quantise fused" if wl.fused else "q8_1 input"),
@@ -628,8 +648,8 @@ def run_memra(args):
             "data": "synthetic (seeded N(0,0.02) weights, bf16 N(0,1) activations)",
             "config": cfg,
             "us_per_step": round(ms_per_step * 1e3, 2),
-            "tok_per_s": round(1e3 / ms_per_step, 2) if args.workload in (
-                "dense27b_sweep", "moe_top8") or args.workload.startswith("verify_m") else None,
+            "tok_per_s": round(1e3 / ms_per_step, 2) if args.workload == "moe_top8" or
+            args.workload.startswith(("dense27b_sweep", "verify_m")) else None,
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "hbm_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
             "roofline": roofline,

@@ -50,6 +50,9 @@ _SIGS = {
     "memra_quantize_q8_0": [_p, _i64, _i64, _p, _p, _p],
     "memra_quantize_q8_1": [_p, _i32, _i64, _i64, _p, _p, _p],
     "memra_q8_0_gemv": [_p, _p, _i64, _i64, _p, _p, _p, _p],
+    "memra_quantize_q4_0": [_p, _i64, _i64, _p, _p, _p],
+    "memra_q4_0_gemv": [_p, _p, _i64, _i64, _p, _p, _p, _p],
+    "memra_q4_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
     "memra_q8_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
     "memra_q8_0_quant_gemm": [_p, _p, _i64, _i64, _i64, _p, _i32, _p, _p],
     "memra_q8_0_moe_gemv": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p, _p],
@@ -142,6 +145,22 @@ def memra_quantize_q8_0(w, wq=None, wd=None):
     return wq, wd
 
 
+def memra_quantize_q4_0(w, wq4=None, wd=None):
+    """fp32 weights [N, K] -> (wq4 uint8 [N, K/2] packed 4-bit codes, wd float16 [N, K/32])."""
+    _need(w, "w", torch.float32)
+    N, K = w.shape
+    if wq4 is None:
+        wq4 = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    if wd is None:
+        wd = torch.empty((N, K // 32), dtype=torch.float16, device=w.device)
+    _need(wq4, "wq4", torch.uint8, w.device, (N, K // 2))
+    _need(wd, "wd", torch.float16, w.device, (N, K // 32))
+    with torch.cuda.device(w.device):
+        _check("memra_quantize_q4_0",
+               lib().memra_quantize_q4_0(_ptr(w), N, K, _ptr(wq4), _ptr(wd), _stream(w)))
+    return wq4, wd
+
+
 def memra_quantize_q8_1(x, xq=None, xd=None):
     """Activations [M, K] (bf16 or fp32) -> (xq int8 [M, K], xd float32 [M, K/32])."""
     if x.dtype == torch.bfloat16:
@@ -225,6 +244,46 @@ def memra_q8_0_gemv(wq, wd, xq, xd, y=None):
         _check("memra_q8_0_gemv",
                lib().memra_q8_0_gemv(_ptr(wq), _ptr(wd), N, K, _ptr(xq), _ptr(xd), _ptr(y),
                                      _stream(wq)))
+    return y
+
+
+def memra_q4_0_gemm_small_m(wq4, wd, xq, xd, y=None):
+    """y [M, N] = W (Q4_0: wq4 uint8 [N, K/2], wd float16 [N, K/32]) x (q8_1), M <= 8."""
+    _need(wq4, "wq4", torch.uint8)
+    N, K2 = wq4.shape
+    K = 2 * K2
+    dev = wq4.device
+    _need(wd, "wd", torch.float16, dev, (N, K // 32))
+    _need(xq, "xq", torch.int8, dev)
+    M = xq.shape[0]
+    _need(xq, "xq", torch.int8, dev, (M, K))
+    _need(xd, "xd", torch.float32, dev, (M, K // 32))
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, (M, N))
+    with torch.cuda.device(dev):
+        _check("memra_q4_0_gemm_small_m",
+               lib().memra_q4_0_gemm_small_m(_ptr(wq4), _ptr(wd), N, K, M, _ptr(xq), _ptr(xd),
+                                             _ptr(y), _stream(wq4)))
+    return y
+
+
+def memra_q4_0_gemv(wq4, wd, xq, xd, y=None):
+    """y [N] = W (Q4_0) x (q8_1) for one activation row (xq [K], xd [K/32])."""
+    _need(wq4, "wq4", torch.uint8)
+    N, K2 = wq4.shape
+    K = 2 * K2
+    dev = wq4.device
+    _need(wd, "wd", torch.float16, dev, (N, K // 32))
+    _need(xq, "xq", torch.int8, dev, (K,))
+    _need(xd, "xd", torch.float32, dev, (K // 32,))
+    if y is None:
+        y = torch.empty((N,), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, (N,))
+    with torch.cuda.device(dev):
+        _check("memra_q4_0_gemv",
+               lib().memra_q4_0_gemv(_ptr(wq4), _ptr(wd), N, K, _ptr(xq), _ptr(xd), _ptr(y),
+                                     _stream(wq4)))
     return y
 
 

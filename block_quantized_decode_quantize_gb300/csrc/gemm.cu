@@ -80,6 +80,18 @@ constexpr int kMaxTopK = MEMRA_MAX_TOP_K;
 
 enum Mode { kDense = 0, kMoeUngated = 1, kMoeGated = 2 };
 
+// Weight formats: Q8_0 (32 int8 quants a block, K bytes a row) and Q4_0 (32 4-bit
+// codes a block, K/2 bytes a row; byte j of a block holds elements j and j+16).
+enum Fmt { kQ8 = 0, kQ4 = 1 };
+
+// dp4a with unsigned bytes in a and signed bytes in b (the Q4_0 codes against q8_1
+// activations): exact int32.
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // ----------------------------------------------------------------------------
 // Work description shared by both kernels: a CTA's rows come as segments, each a
 // contiguous run of weight rows multiplied by one activation row set.
@@ -89,6 +101,7 @@ struct Params {
   const uint16_t* wd;
   int64_t N;               // rows of one weight matrix
   int64_t K;
+  int64_t qrow;            // bytes of one row of the quant plane (K, or K/2 for Q4_0)
   int nb, cpr, S;
   const int8_t* xq;
   const float* xd;
@@ -115,6 +128,7 @@ struct Params {
   uint32_t stage_bytes;    // bytes per stage (quants, then scales at wd_off)
   uint32_t wd_off;
   uint32_t off_x, off_xd, off_ring, off_part, off_yacc, off_slice;
+  uint32_t off_xsum;       // Q4_0: int32 per-block sums of the activation quants
   // register kernel layout
   int tile_rows;
 };
@@ -219,7 +233,7 @@ struct StageMeta {
   int xrow;
 };
 
-template <int M, int R, int MODE, int XIN>
+template <int M, int R, int MODE, int XIN, int FMT = kQ8>
 __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS : 1)
     q8_tma_kernel(const Params p) {
   constexpr int kConsumerWarps = tma_consumer_warps(M);
@@ -369,11 +383,11 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         if (m) {
           meta[slot] = *m;
           const Seg g = seg_of(m->seg);
-          const uint32_t qb = (uint32_t)(m->nr * p.K);
+          const uint32_t qb = (uint32_t)(m->nr * p.qrow);
           const uint32_t db = (uint32_t)(m->nr * nb * 2);
           const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
           mbar_arrive_expect_tx(full_bar(slot), qb + db);
-          bulk_g2s_hint(dst, p.wq + (g.row0 + m->r0) * p.K, qb, full_bar(slot), policy);
+          bulk_g2s_hint(dst, p.wq + (g.row0 + m->r0) * p.qrow, qb, full_bar(slot), policy);
           bulk_g2s_hint(dst + p.wd_off, p.wd + (g.row0 + m->r0) * nb, db, full_bar(slot), policy);
         } else {
           meta[slot] = StageMeta{0, 0, 0, 0};  // sentinel: no more stages
@@ -396,15 +410,15 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
           meta[slot] = StageMeta{-1, 0, p.top_k * n, n};
           uint32_t bytes = 0;
           for (int k = 0; k < p.top_k; ++k)
-            if (s_ids[k] >= 0) bytes += (uint32_t)(n * (p.K + nb * 2));
+            if (s_ids[k] >= 0) bytes += (uint32_t)(n * (p.qrow + nb * 2));
           const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
           // With no valid segment (bytes == 0) this arrival alone completes the stage.
           mbar_arrive_expect_tx(full_bar(slot), bytes);
           for (int k = 0; k < p.top_k; ++k) {
             if (s_ids[k] < 0) continue;
             const int64_t row0 = (int64_t)s_ids[k] * p.N + u0;
-            bulk_g2s_hint(dst + (uint32_t)(k * n) * (uint32_t)p.K, p.wq + row0 * p.K,
-                          (uint32_t)(n * p.K), full_bar(slot), policy);
+            bulk_g2s_hint(dst + (uint32_t)(k * n) * (uint32_t)p.qrow, p.wq + row0 * p.qrow,
+                          (uint32_t)(n * p.qrow), full_bar(slot), policy);
             bulk_g2s_hint(dst + p.wd_off + (uint32_t)(k * n * nb * 2), p.wd + row0 * nb,
                           (uint32_t)(n * nb * 2), full_bar(slot), policy);
           }
@@ -485,6 +499,29 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       quantize_rows_to_smem<XIN>(p.xin, p.xrows, (int)p.K, xs, xds, cw, kConsumerWarps, lane);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    // Q4_0: s_b = sum_i (c_i - 8) x_i = (sum_i c_i x_i) - 8 sum_i x_i, with the
+    // activation's per-block sums taken once here.
+    int32_t* xsum = reinterpret_cast<int32_t*>(smem + p.off_xsum);
+    if (FMT == kQ4) {
+      for (int i = threadIdx.x - 32; i < p.xrows * nb; i += kConsumerWarps * 32) {
+        const uint4 a = *reinterpret_cast<const uint4*>(xs + (size_t)i * 32);
+        const uint4 b = *reinterpret_cast<const uint4*>(xs + (size_t)i * 32 + 16);
+        const int ones = 0x01010101;
+        int t = __dp4a(ones, (int)a.x, 0);
+        t = __dp4a(ones, (int)a.y, t);
+        t = __dp4a(ones, (int)a.z, t);
+        t = __dp4a(ones, (int)a.w, t);
+        t = __dp4a(ones, (int)b.x, t);
+        t = __dp4a(ones, (int)b.y, t);
+        t = __dp4a(ones, (int)b.z, t);
+        xsum[i] = __dp4a(ones, (int)b.w, t);
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    }
+    // Bytes of one block and of one 32-block part in the ring's quant rows.
+    constexpr int kBlockBytes = FMT == kQ4 ? 16 : 32;
+    constexpr int kPartBytes = 32 * kBlockBytes;
+    const int Qrow = (int)p.qrow;
     uint32_t tbase = 0;  // tasks in all earlier stages: deals tasks round-robin over warps
     for (uint32_t it = 0;; ++it) {
       const int slot = it % ns;
@@ -516,14 +553,14 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         }
         const int plo = s_slice[s];
         const int phi = s_slice[s + 1];
-        // Per-lane pointers at the task's first block; a part is 1024 bytes on.
+        // Per-lane pointers at the task's first block; a part is kPartBytes on.
         const int8_t* wl[R];
         const uint16_t* dl[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           // Rows past the stage's end reuse a valid row; their sums are dropped.
           const int row = rbase + r < nr ? rbase + r : rbase;
-          wl[r] = ws + row * Ki + (plo * 32 + lane) * 32 + h1 * 16;
+          wl[r] = ws + row * Qrow + (plo * 32 + lane) * kBlockBytes + (FMT == kQ4 ? 0 : h1 * 16);
           dl[r] = ds + row * nb + plo * 32 + lane;
         }
         const int8_t* xl = xs + (size_t)xrow * Ki + (plo * 32 + lane) * 32 + h1 * 16;
@@ -540,9 +577,11 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
             uint16_t dw[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-              // The two halves in this lane quad's order (see the file comment).
-              w0[r] = *reinterpret_cast<const uint4*>(wl[r] + q * 1024);
-              w1[r] = *reinterpret_cast<const uint4*>(wl[r] + q * 1024 + 16 - 32 * h1);
+              // Q8_0: the two halves in this lane quad's order (see the file comment).
+              // Q4_0: the block's 16 bytes of codes in one load.
+              w0[r] = *reinterpret_cast<const uint4*>(wl[r] + q * kPartBytes);
+              if (FMT == kQ8)
+                w1[r] = *reinterpret_cast<const uint4*>(wl[r] + q * kPartBytes + 16 - 32 * h1);
               dw[r] = dl[r][q * 32];
             }
 #pragma unroll
@@ -551,10 +590,30 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
               const uint4 x0 = *reinterpret_cast<const uint4*>(xm);
               const uint4 x1 = *reinterpret_cast<const uint4*>(xm + 16 - 32 * h1);
               const float dx = xdl[(size_t)m * nb + q * 32];
+              if (FMT == kQ4) {
+                // x0 holds half h1 of the block, x1 the other half.
+                const uint4 xa = h1 ? x1 : x0;  // elements 0..15
+                const uint4 xb = h1 ? x0 : x1;  // elements 16..31
+                const int sx = xsum[(size_t)(xrow + m) * nb + pt * 32 + lane];
 #pragma unroll
-              for (int r = 0; r < R; ++r) {
-                const int sb = dot_halves(w0[r], w1[r], x0, x1);
-                acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, sb);
+                for (int r = 0; r < R; ++r) {
+                  const uint4 c = w0[r];
+                  int t = dp4a_us(c.x & 0x0F0F0F0Fu, (int)xa.x, 0);
+                  t = dp4a_us(c.y & 0x0F0F0F0Fu, (int)xa.y, t);
+                  t = dp4a_us(c.z & 0x0F0F0F0Fu, (int)xa.z, t);
+                  t = dp4a_us(c.w & 0x0F0F0F0Fu, (int)xa.w, t);
+                  t = dp4a_us((c.x >> 4) & 0x0F0F0F0Fu, (int)xb.x, t);
+                  t = dp4a_us((c.y >> 4) & 0x0F0F0F0Fu, (int)xb.y, t);
+                  t = dp4a_us((c.z >> 4) & 0x0F0F0F0Fu, (int)xb.z, t);
+                  t = dp4a_us((c.w >> 4) & 0x0F0F0F0Fu, (int)xb.w, t);
+                  acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, t - 8 * sx);
+                }
+              } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                  const int sb = dot_halves(w0[r], w1[r], x0, x1);
+                  acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, sb);
+                }
               }
             }
           }
@@ -900,18 +959,19 @@ int gemv_path_override() {
 
 int64_t max_units_per_cta(int64_t units, int64_t grid) { return (units + grid - 1) / grid; }
 
-template <int M, int R, int MODE, int XIN>
+template <int M, int R, int MODE, int XIN, int FMT = kQ8>
 bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out) {
   const int path = gemv_path_override();
   const TmaTuning& tune = tma_tuning();
-  if (path == 1 || (path == 0 && M > 1 && !tune.multi_default)) return false;
+  if (FMT == kQ8 && (path == 1 || (path == 0 && M > 1 && !tune.multi_default))) return false;
   // Per-shape dispatch: below a few tens of MB of weights the register kernel's
   // faster start wins over the deeper bulk-copy stream (measured on GB300).
-  if (path == 0 && MODE == kDense && p.units * p.K < tune.dense_min_bytes) return false;
+  if (FMT == kQ8 && path == 0 && MODE == kDense && p.units * p.K < tune.dense_min_bytes)
+    return false;
   if (p.K % 256 != 0) return false;
   if (!aligned(p.wd, 16) || !aligned(p.wq, 16)) return false;
   if (XIN == kXq8 && (!aligned(p.xd, 16) || !aligned(p.xq, 16))) return false;
-  const size_t row_bytes = (size_t)p.K + (size_t)p.nb * 2;
+  const size_t row_bytes = (size_t)p.qrow + (size_t)p.nb * 2;
   const int64_t maxu = max_units_per_cta(p.units, grid);
   int rps = (int)std::max<size_t>(1, (M > 1 ? tune.multi_stage_target : tune.stage_target) /
                                           row_bytes);
@@ -927,9 +987,10 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
     p.packed = 1;
     rps = (int)(p.top_k * maxu);
   }
-  size_t stage = align_up((size_t)rps * p.K, 128) + align_up((size_t)rps * p.nb * 2, 128);
-  const size_t xbytes =
-      align_up((size_t)p.xrows * p.K, 128) + align_up((size_t)p.xrows * p.nb * 4, 128);
+  size_t stage = align_up((size_t)rps * p.qrow, 128) + align_up((size_t)rps * p.nb * 2, 128);
+  const size_t xsum_bytes = FMT == kQ4 ? align_up((size_t)p.xrows * p.nb * 4, 128) : 0;
+  const size_t xbytes = align_up((size_t)p.xrows * p.K, 128) +
+                        align_up((size_t)p.xrows * p.nb * 4, 128) + xsum_bytes;
   const size_t yacc = MODE == kMoeGated ? align_up((size_t)maxu * 4, 16) : 0;
   const size_t fixed = kHeaderBytes + xbytes + yacc + align_up((size_t)(p.S + 1) * 4, 16);
   size_t part_per_stage = align_up((size_t)rps * p.S * M * 4, 16);
@@ -946,7 +1007,7 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   if (MODE == kDense && maxu > (int64_t)ns * rps) {
     const int wide = (int)((maxu + ns - 1) / ns + R - 1) / R * R;
     const size_t wstage =
-        align_up((size_t)wide * p.K, 128) + align_up((size_t)wide * p.nb * 2, 128);
+        align_up((size_t)wide * p.qrow, 128) + align_up((size_t)wide * p.nb * 2, 128);
     const size_t wpart = align_up((size_t)wide * p.S * M * 4, 16);
     if (wide <= 2 * rps && fixed + ns * (wstage + wpart) <= limit) {
       rps = wide;
@@ -959,10 +1020,11 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   p.rps = rps;
   p.ns = ns;
   p.stage_bytes = (uint32_t)stage;
-  p.wd_off = (uint32_t)align_up((size_t)rps * p.K, 128);
+  p.wd_off = (uint32_t)align_up((size_t)rps * p.qrow, 128);
   size_t off = kHeaderBytes;
   p.off_x = (uint32_t)off;
   p.off_xd = (uint32_t)(off + align_up((size_t)p.xrows * p.K, 128));
+  p.off_xsum = (uint32_t)(p.off_xd + align_up((size_t)p.xrows * p.nb * 4, 128));
   off += xbytes;
   p.off_ring = (uint32_t)off;
   off += (size_t)ns * stage;
@@ -1020,26 +1082,44 @@ int reg_grid_ctas_per_sm(int M) {
   return v > 0 && v < built ? (int)v : built;
 }
 
-template <int M, int R, int MODE, int XIN>
+template <int M, int R, int MODE, int XIN, int FMT = kQ8>
 memra_status run_product(Params p, cudaStream_t stream) {
   DeviceInfo info;
   if (!device_info(&info)) return MEMRA_ERR_CUDA;
+  p.qrow = FMT == kQ4 ? p.K / 2 : p.K;
   p.nb = (int)(p.K / 32);
   p.cpr = (p.nb + 31) / 32;
   p.S = slices_for(p.cpr);
   int64_t grid = std::min<int64_t>(p.units, (int64_t)info.sms * (M > 1 ? 1 : tma_tuning().ctas_per_sm));
   size_t smem = 0;
-  if (plan_tma<M, R, MODE, XIN>(p, info, grid, &smem)) {
+  if (plan_tma<M, R, MODE, XIN, FMT>(p, info, grid, &smem)) {
     if (grid > info.sms && smem > tma_tuning().smem_pair_limit) {
       // Only one such CTA fits per SM: one per SM, so the grid stays a single wave.
       grid = std::min<int64_t>(p.units, info.sms);
-      if (!plan_tma<M, R, MODE, XIN>(p, info, grid, &smem)) return MEMRA_ERR_UNSUPPORTED;
+      if (!plan_tma<M, R, MODE, XIN, FMT>(p, info, grid, &smem)) return MEMRA_ERR_UNSUPPORTED;
     }
-    return launch(q8_tma_kernel<M, R, MODE, XIN>, grid, tma_threads(M), smem, stream, p);
+    return launch(q8_tma_kernel<M, R, MODE, XIN, FMT>, grid, tma_threads(M), smem, stream, p);
   }
+  if (FMT == kQ4) return MEMRA_ERR_UNSUPPORTED;  // Q4_0 runs on the bulk-copy kernel only
   grid = std::min<int64_t>(p.units, (int64_t)info.sms * reg_grid_ctas_per_sm(M));
   if (plan_reg<M, R, MODE, XIN>(p, info, grid, &smem))
     return launch(q8_reg_kernel<M, R, MODE, XIN>, grid, kRegThreads, smem, stream, p);
+  return MEMRA_ERR_UNSUPPORTED;
+}
+
+// Q4_0 products (dense, q8_1 input).  M = 8 takes 2-row tasks: with K = 17408 the
+// activation planes and their block sums leave room for 2-row stages only.
+memra_status dispatch_m_q4(const Params& p, int M, cudaStream_t s) {
+  switch (M) {
+    case 1: return run_product<1, 1, kDense, kXq8, kQ4>(p, s);
+    case 2: return run_product<2, 1, kDense, kXq8, kQ4>(p, s);
+    case 3: return run_product<3, 1, kDense, kXq8, kQ4>(p, s);
+    case 4: return run_product<4, 2, kDense, kXq8, kQ4>(p, s);
+    case 5: return run_product<5, 2, kDense, kXq8, kQ4>(p, s);
+    case 6: return run_product<6, 2, kDense, kXq8, kQ4>(p, s);
+    case 7: return run_product<7, 2, kDense, kXq8, kQ4>(p, s);
+    case 8: return run_product<8, 2, kDense, kXq8, kQ4>(p, s);
+  }
   return MEMRA_ERR_UNSUPPORTED;
 }
 
@@ -1105,6 +1185,40 @@ extern "C" memra_status memra_q8_0_gemv(const int8_t* wq, const uint16_t* wd, in
                                         const int8_t* xq, const float* xd, float* y,
                                         cudaStream_t stream) {
   return memra_q8_0_gemm_small_m(wq, wd, N, K, 1, xq, xd, y, stream);
+}
+
+extern "C" memra_status memra_q4_0_gemm_small_m(const uint8_t* wq4, const uint16_t* wd, int64_t N,
+                                                int64_t K, int64_t M, const int8_t* xq,
+                                                const float* xd, float* y, cudaStream_t stream) {
+  if (N < 0 || K < 0 || M < 0 || K % 32 != 0) return MEMRA_ERR_INVALID_ARG;
+  if (M > MEMRA_MAX_M) return MEMRA_ERR_UNSUPPORTED;
+  if (N > INT32_MAX || K > INT32_MAX) return MEMRA_ERR_UNSUPPORTED;
+  if (N == 0 || M == 0) return MEMRA_OK;
+  if (!y) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(y, 4)) return MEMRA_ERR_ALIGNMENT;
+  if (K == 0) return zero_fill(y, M * N, stream);
+  if (!wq4 || !wd || !xq || !xd) return MEMRA_ERR_INVALID_ARG;
+  if (K % 256 != 0) return MEMRA_ERR_UNSUPPORTED;
+  if (!aligned(wq4, 16) || !aligned(wd, 16) || !aligned(xq, 16) || !aligned(xd, 16))
+    return MEMRA_ERR_ALIGNMENT;
+  if (!x_fits(M, K)) return MEMRA_ERR_UNSUPPORTED;
+  Params p{};
+  p.wq = reinterpret_cast<const int8_t*>(wq4);
+  p.wd = wd;
+  p.N = N;
+  p.K = K;
+  p.xq = xq;
+  p.xd = xd;
+  p.xrows = (int)M;
+  p.y = y;
+  p.units = N;
+  return dispatch_m_q4(p, (int)M, stream);
+}
+
+extern "C" memra_status memra_q4_0_gemv(const uint8_t* wq4, const uint16_t* wd, int64_t N, int64_t K,
+                                        const int8_t* xq, const float* xd, float* y,
+                                        cudaStream_t stream) {
+  return memra_q4_0_gemm_small_m(wq4, wd, N, K, 1, xq, xd, y, stream);
 }
 
 extern "C" memra_status memra_q8_0_quant_gemm(const int8_t* wq, const uint16_t* wd, int64_t N,

@@ -92,6 +92,75 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
+// Weights to Q4_0: per 32-block m = the element of largest |w| (the first one on a
+// tie), d16 = fp16_rne(m / -8) (+0 for an all-zero block), code = clamp(round-half-
+// away(w / float(d16)) + 8, 0, 15).  Packed split plane: byte j < 16 of a block holds
+// element j's code in its low nibble and element j+16's in its high nibble.  Four
+// lanes own a block (8 values each); like the Q8_0 ingest this kernel does not let
+// its dependents start early.
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_q4_0_kernel(const float* __restrict__ w, int64_t groups, uint8_t* __restrict__ q4,
+                         uint16_t* __restrict__ d) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < groups;
+       base += stride) {
+    const int64_t g = base + lane;
+    const bool valid = g < groups;
+    float v[8];
+    if (valid) {
+      load8(w + g * 8, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+    // The lane's first largest-magnitude value, then the block's: a larger
+    // magnitude wins, an equal one from the lower lane (earlier elements) wins.
+    float am = 0.0f, m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (fabsf(v[i]) > am) {
+        am = fabsf(v[i]);
+        m = v[i];
+      }
+    }
+#pragma unroll
+    for (int mask = 1; mask <= 2; mask <<= 1) {
+      const float om = __shfl_xor_sync(kFullMask, m, mask);
+      const float oam = fabsf(om);
+      const bool other_first = (lane & mask) != 0;
+      if (oam > am || (oam == am && other_first)) {
+        am = oam;
+        m = om;
+      }
+    }
+    const uint16_t d16 = am == 0.0f ? (uint16_t)0 : __half_as_ushort(__float2half_rn(m / -8.0f));
+    const float dv = __half2float(__ushort_as_half(d16));
+    const float inv = dv == 0.0f ? 0.0f : 1.0f / dv;
+    int qv[8];
+    quant8_fast(v, dv, inv, qv);  // clamp(round-half-away(v / dv), +-127), exactly
+    int c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = min(max(qv[i] + 8, 0), 15);
+    uint2 own;
+    own.x = pack4(c[0], c[1], c[2], c[3]);
+    own.y = pack4(c[4], c[5], c[6], c[7]);
+    // Lanes 0 and 1 of the block (elements 0..15) take the codes of lanes 2 and 3
+    // (elements 16..31) as their high nibbles.
+    uint2 high;
+    high.x = __shfl_xor_sync(kFullMask, own.x, 2);
+    high.y = __shfl_xor_sync(kFullMask, own.y, 2);
+    if (valid && (lane & 2) == 0) {
+      uint2 out;
+      out.x = own.x | (high.x << 4);
+      out.y = own.y | (high.y << 4);
+      *reinterpret_cast<uint2*>(q4 + (g >> 2) * 16 + (lane & 1) * 8) = out;
+    }
+    if (valid && (lane & 3) == 0) d[g >> 2] = d16;
+  }
+}
+
 // h = (g / (1 + exp(-g))) * u, one rounding per operation, then q8_1 of h.
 // gu: [R][2F] (gate columns first), F % 32 == 0, so a thread's 8 values never
 // straddle a row.
@@ -148,6 +217,21 @@ extern "C" memra_status memra_quantize_q8_0(const float* w, int64_t N, int64_t K
   const int64_t groups = N * K / 8;
   cudaError_t e = launch_kernel(quantize_q8_0_kernel, dim3(quant_grid(groups, info)),
                                 dim3(kQuantThreads), 0, stream, w, groups, wq, wd);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MEMRA_OK;
+}
+
+extern "C" memra_status memra_quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* wq4,
+                                            uint16_t* wd, cudaStream_t stream) {
+  if (N < 0 || K < 0 || K % 32 != 0) return MEMRA_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return MEMRA_OK;
+  if (!w || !wq4 || !wd) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(wq4, 16) || !aligned(wd, 2)) return MEMRA_ERR_ALIGNMENT;
+  DeviceInfo info;
+  if (!device_info(&info)) return MEMRA_ERR_CUDA;
+  const int64_t groups = N * K / 8;
+  cudaError_t e = launch_kernel(quantize_q4_0_kernel, dim3(quant_grid(groups, info)),
+                                dim3(kQuantThreads), 0, stream, w, groups, wq4, wd);
   if (e != cudaSuccess) return cuda_fail(e);
   return MEMRA_OK;
 }

@@ -111,6 +111,37 @@ memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t* wd, int64
                                      cudaStream_t stream);
 
 /*
+ * Q4_0 weights, the pages' other split-plane decode format (memra wiki, feature
+ * list: "NVFP4 / Q4_0 / Q8_0 decode -- split-plane repacked matvecs").  The pages
+ * print nothing of it; this library's reading is GGUF's Q4_0 block: 32 consecutive
+ * weights of a row share one fp16 scale d and carry 4-bit codes c in [0, 15] with
+ * w ~= d * (c - 8).
+ *   Planes: wq4 uint8 [N][K/2] and wd fp16 [N][K/32].  Byte j < 16 of a block holds
+ *   element j's code in its low nibble and element j+16's in its high nibble.
+ *   Quantisation: m = the element of largest |w| (the first one on a tie);
+ *   d = fp16_rne(m / -8) (+0 for an all-zero block); c = clamp(round_half_away(
+ *   w / float(d)) + 8, 0, 15).  w: fp32 [N][K], 16-byte aligned; wq4 16-byte aligned.
+ */
+memra_status memra_quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* wq4, uint16_t* wd,
+                                 cudaStream_t stream);
+
+/*
+ * Q4_0 x q8_1 products: y[m][n] = sum_b (d_w[n][b] * d_x[m][b]) * s_b with the exact
+ * int32 block sum s_b = sum_i (c_i - 8) * xq_i, in the same fp32 summation order as
+ * the Q8_0 products (so the result equals the Q8_0 product of the unpacked codes,
+ * bit for bit).  M in [0, 8]; xq [M][K], xd [M][K/32], y fp32 [M][N].
+ * K must be a multiple of 256 (MEMRA_ERR_UNSUPPORTED otherwise); wq4, wd, xq and xd
+ * 16-byte aligned.
+ */
+memra_status memra_q4_0_gemm_small_m(const uint8_t* wq4, const uint16_t* wd, int64_t N, int64_t K,
+                                     int64_t M, const int8_t* xq, const float* xd, float* y,
+                                     cudaStream_t stream);
+
+/* The decode GEMV on Q4_0 weights: memra_q4_0_gemm_small_m with M = 1, y fp32 [N]. */
+memra_status memra_q4_0_gemv(const uint8_t* wq4, const uint16_t* wd, int64_t N, int64_t K,
+                             const int8_t* xq, const float* xd, float* y, cudaStream_t stream);
+
+/*
  * The verify GEMM (or, with M = 1, the decode GEMV) with the activation's q8_1
  * quantisation done in the kernel's prologue: each CTA quantises x [M][K] (bf16
  * bits or fp32, 16-byte aligned) into on-chip memory while the weight stream is

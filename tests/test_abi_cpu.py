@@ -87,6 +87,22 @@ def test_quantizer_argument_errors(L):
     assert L.memra_swiglu_quantize_q8_1(A256 + 4, 2, 64, A256, A256, None) == 2
 
 
+def test_q4_0_argument_errors(L):
+    f = L.memra_q4_0_gemm_small_m
+    assert f(A256, A256, 64, 48, 1, A256, A256, A256, None) == 1      # K % 32 != 0
+    assert f(A256, A256, 64, 256, 9, A256, A256, A256, None) == 3     # M > 8
+    assert f(A256, A256, 64, 96, 1, A256, A256, A256, None) == 3      # K % 256 != 0
+    assert f(A256 + 8, A256, 64, 256, 1, A256, A256, A256, None) == 2  # wq4 not 16-aligned
+    assert f(A256, A256 + 2, 64, 256, 1, A256, A256, A256, None) == 2  # wd not 16-aligned
+    assert f(A256, A256, 64, 256, 1, A256, A256 + 4, A256, None) == 2  # xd not 16-aligned
+    assert f(None, A256, 64, 256, 1, A256, A256, A256, None) == 1     # null weights
+    assert f(None, None, 0, 256, 1, None, None, None, None) == 0       # empty: no work
+    assert L.memra_q4_0_gemv(A256, A256, 64, 33, A256, A256, A256, None) == 1
+    assert L.memra_quantize_q4_0(A256, 4, 48, A256, A256, None) == 1
+    assert L.memra_quantize_q4_0(A256, 4, 64, A256 + 8, A256, None) == 2
+    assert L.memra_quantize_q4_0(None, 0, 64, None, None, None) == 0
+
+
 def test_moe_argument_errors(L):
     f = L.memra_q8_0_moe_gemv
     args = dict(wq=A256, wd=A256, E=4, N=16, K=64, ids=A256, gw=None, top_k=2, xq=A256,

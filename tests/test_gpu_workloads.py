@@ -80,6 +80,33 @@ def test_dense27b_layer_sampled(mem, orc, layer, M):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("layer", [0, 63])
+def test_dense27b_q4_0_layer_sampled(mem, orc, layer):
+    """The Q4_0 sweep as bench.py builds it: sampled rows against the oracle."""
+    cfg = synth.DENSE27B
+    for t, (name, N, K) in enumerate(cfg["gemvs"]):
+        wq4, wd = bench.quantized_weights(mem, N, K, 5, layer, t, device="cuda", fmt="q4_0")
+        x = synth.activations_bf16(1, K, 5, layer, t, 1001, outlier_frac=cfg["outlier_frac"],
+                                   outlier_scale=cfg["outlier_scale"], device="cuda")
+        op = bench.Gemv(wq4, wd, x, name)
+        assert op.fmt == "q4_0" and op.weight_bytes == N * K // 2 + N * (K // 32) * 2
+        bench.run_gemv_op(mem, op)
+        torch.cuda.synchronize()
+        rows = sample_rows(N, seed=500 + layer * 10 + t)
+        w = synth.weights_fp32(N, K, 5, layer, t, device="cuda")
+        w_rows = w[torch.as_tensor(rows, device="cuda")].cpu().numpy()
+        oq4, od = orc.quantize_q4_0(w_rows)
+        idx = torch.as_tensor(rows, device="cuda")
+        assert np.array_equal(np_(wq4[idx]), oq4), name + ": packed codes"
+        assert np.array_equal(wd_bits(wd[idx]), od), name + ": scales"
+        oxq, oxd = orc.quantize_q8_1(bf16_bits_np(x.cpu()))
+        y_ref = orc.gemm_q4_0(oq4, od, oxq, oxd)
+        terms = abs_terms(orc.block_dots(orc.unpack_q4_0(oq4), oxq), od, oxd)
+        assert_within(np_(op.y)[:, rows], y_ref, terms, "q4_0 L%d %s" % (layer, name))
+        del w, wq4, wd, op
+    torch.cuda.empty_cache()
+
+
 def test_moe_layer_full_size(mem, orc):
     """One routed layer of the 128-expert MoE (hidden 2048, expert FFN 768, top-8)."""
     c = synth.MOE
