@@ -522,6 +522,10 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
     constexpr int kBlockBytes = FMT == kQ4 ? 16 : 32;
     constexpr int kPartBytes = 32 * kBlockBytes;
     const int Qrow = (int)p.qrow;
+    // Q4_0 nibble masks and shifts of this lane (see the block dot below).
+    const uint32_t q4m0 = h1 ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+    const uint32_t q4m1 = ~q4m0;
+    const int q4s0 = h1 ? 4 : 0;
     uint32_t tbase = 0;  // tasks in all earlier stages: deals tasks round-robin over warps
     for (uint32_t it = 0;; ++it) {
       const int slot = it % ns;
@@ -591,22 +595,25 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
               const uint4 x1 = *reinterpret_cast<const uint4*>(xm + 16 - 32 * h1);
               const float dx = xdl[(size_t)m * nb + q * 32];
               if (FMT == kQ4) {
-                // x0 holds half h1 of the block, x1 the other half.
-                const uint4 xa = h1 ? x1 : x0;  // elements 0..15
-                const uint4 xb = h1 ? x0 : x1;  // elements 16..31
+                // x0 holds half h1 of the block (elements 16*h1 ..), x1 the other half.
+                // The lane pairs x0 with the nibbles of half h1 (mask m0) and x1 with the
+                // other nibbles (m1).  A high-nibble mask leaves 16 times the codes in
+                // place, which makes that dp4a exactly 16 times the half's dot (a
+                // multiple of 16 below 2^19), undone by the shift.
                 const int sx = xsum[(size_t)(xrow + m) * nb + pt * 32 + lane];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                   const uint4 c = w0[r];
-                  int t = dp4a_us(c.x & 0x0F0F0F0Fu, (int)xa.x, 0);
-                  t = dp4a_us(c.y & 0x0F0F0F0Fu, (int)xa.y, t);
-                  t = dp4a_us(c.z & 0x0F0F0F0Fu, (int)xa.z, t);
-                  t = dp4a_us(c.w & 0x0F0F0F0Fu, (int)xa.w, t);
-                  t = dp4a_us((c.x >> 4) & 0x0F0F0F0Fu, (int)xb.x, t);
-                  t = dp4a_us((c.y >> 4) & 0x0F0F0F0Fu, (int)xb.y, t);
-                  t = dp4a_us((c.z >> 4) & 0x0F0F0F0Fu, (int)xb.z, t);
-                  t = dp4a_us((c.w >> 4) & 0x0F0F0F0Fu, (int)xb.w, t);
-                  acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, t - 8 * sx);
+                  int a = dp4a_us(c.x & q4m0, (int)x0.x, 0);
+                  a = dp4a_us(c.y & q4m0, (int)x0.y, a);
+                  a = dp4a_us(c.z & q4m0, (int)x0.z, a);
+                  a = dp4a_us(c.w & q4m0, (int)x0.w, a);
+                  int b = dp4a_us(c.x & q4m1, (int)x1.x, 0);
+                  b = dp4a_us(c.y & q4m1, (int)x1.y, b);
+                  b = dp4a_us(c.z & q4m1, (int)x1.z, b);
+                  b = dp4a_us(c.w & q4m1, (int)x1.w, b);
+                  const int dot = (a >> q4s0) + (b >> (4 - q4s0));
+                  acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, dot - 8 * sx);
                 }
               } else {
 #pragma unroll
@@ -1107,11 +1114,15 @@ memra_status run_product(Params p, cudaStream_t stream) {
   return MEMRA_ERR_UNSUPPORTED;
 }
 
-// Q4_0 products (dense, q8_1 input).  M = 8 takes 2-row tasks: with K = 17408 the
-// activation planes and their block sums leave room for 2-row stages only.
+// Q4_0 products (dense, q8_1 input).  A Q4_0 block costs as many dp4a as a Q8_0 block
+// in half the bytes, so the consumers, not the stream, set the pace: M = 1 takes
+// 2-row tasks, which share each block's activation loads between two rows (measured
+// on the 64-layer sweep: 3.44 ms per token with 1-row tasks, 3.16 with 2, 3.32 with
+// 4).  M = 8 takes 2-row tasks too: with K = 17408 the activation planes and their
+// block sums leave room for 2-row stages only.
 memra_status dispatch_m_q4(const Params& p, int M, cudaStream_t s) {
   switch (M) {
-    case 1: return run_product<1, 1, kDense, kXq8, kQ4>(p, s);
+    case 1: return run_product<1, 2, kDense, kXq8, kQ4>(p, s);
     case 2: return run_product<2, 1, kDense, kXq8, kQ4>(p, s);
     case 3: return run_product<3, 1, kDense, kXq8, kQ4>(p, s);
     case 4: return run_product<4, 2, kDense, kXq8, kQ4>(p, s);
