@@ -39,7 +39,7 @@ METRIC = ("Q8_0 decode GEMV weight-stream GB/s (% of GB300 HBM peak); "
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8", "moe_top8",
-             "stress_lm_head", "dense27b_sweep_q4_0")
+             "stress_lm_head", "dense27b_sweep_q4_0", "moe_top8_q4_0")
 
 
 # ----------------------------------------------------------------------------
@@ -117,13 +117,15 @@ def build_stress(mem, device, M):
 
 
 class MoeLayer:
-    def __init__(self, mem, layer, device):
+    def __init__(self, mem, layer, device, fmt="q8_0"):
         c = synth.MOE
         E, H, F, k = c["experts"], c["hidden"], c["ffn"], c["top_k"]
-        gq, gd = quantized_weights(mem, E * 2 * F, H, 3, layer, 0, device=device)
-        dq, dd = quantized_weights(mem, E * H, F, 3, layer, 1, device=device)
-        self.gq, self.gd = gq.view(E, 2 * F, H), gd.view(E, 2 * F, H // 32)
-        self.dq, self.dd = dq.view(E, H, F), dd.view(E, H, F // 32)
+        self.fmt = fmt
+        kdiv = 2 if fmt == "q4_0" else 1  # quant bytes per weight: 1/2 for Q4_0
+        gq, gd = quantized_weights(mem, E * 2 * F, H, 3, layer, 0, device=device, fmt=fmt)
+        dq, dd = quantized_weights(mem, E * H, F, 3, layer, 1, device=device, fmt=fmt)
+        self.gq, self.gd = gq.view(E, 2 * F, H // kdiv), gd.view(E, 2 * F, H // 32)
+        self.dq, self.dd = dq.view(E, H, F // kdiv), dd.view(E, H, F // 32)
         self.ids, self.gw = synth.routing(E, k, 3, layer, 2, device=device)
         self.x = synth.activations_bf16(1, H, 3, layer, 3, device=device)
         self.xq = torch.empty((1, H), dtype=torch.int8, device=device)
@@ -133,20 +135,29 @@ class MoeLayer:
         self.hd = torch.empty((k, F // 32), dtype=torch.float32, device=device)
         self.y = torch.empty((H,), dtype=torch.float32, device=device)
         self.status = torch.zeros((1,), dtype=torch.int32, device=device)
-        self.weight_bytes = k * (synth.q8_0_bytes(2 * F, H) + synth.q8_0_bytes(H, F))
+        # the selected experts' quant and scale planes, read once per token
+        self.weight_bytes = k * (self.gq[0].numel() + self.gd[0].numel() * 2 +
+                                 self.dq[0].numel() + self.dd[0].numel() * 2)
+
+    def gemv(self, mem, *args, **kw):
+        if self.fmt == "q4_0":
+            return mem.memra_q4_0_moe_gemv(*args, **kw)
+        return mem.memra_q8_0_moe_gemv(*args, **kw)
 
     def run(self, mem, fused=False):
         if fused:
+            if self.fmt != "q8_0":
+                raise ValueError("the two-kernel routed FFN takes Q8_0 banks")
             mem.memra_q8_0_moe_ffn(self.gq, self.gd, self.dq, self.dd, self.ids, self.gw,
                                    self.x[0], y=self.y, workspace=self.ygu,
                                    dev_status=self.status)
             return
         mem.memra_quantize_q8_1(self.x, self.xq, self.xd)
-        mem.memra_q8_0_moe_gemv(self.gq, self.gd, self.ids, None, self.xq[0], self.xd[0], False,
-                                y=self.ygu, dev_status=self.status)
+        self.gemv(mem, self.gq, self.gd, self.ids, None, self.xq[0], self.xd[0], False,
+                  y=self.ygu, dev_status=self.status)
         mem.memra_swiglu_quantize_q8_1(self.ygu, self.hq, self.hd)
-        mem.memra_q8_0_moe_gemv(self.dq, self.dd, self.ids, self.gw, self.hq, self.hd, True,
-                                y=self.y, dev_status=self.status)
+        self.gemv(mem, self.dq, self.dd, self.ids, self.gw, self.hq, self.hd, True,
+                  y=self.y, dev_status=self.status)
 
 
 def run_gemv_op(mem, op, quantize=True, fused=False):
@@ -194,9 +205,10 @@ class Workload:
             self.ops = build_gemv_4096(mem, device)
         elif name == "stress_lm_head":
             self.ops = build_stress(mem, device, M=1) + build_stress(mem, device, M=8)
-        elif name == "moe_top8":
+        elif name in ("moe_top8", "moe_top8_q4_0"):
             n = synth.MOE["layers"] if layers is None else layers
-            self.moe = [MoeLayer(mem, layer, device) for layer in range(n)]
+            fmt = "q4_0" if name.endswith("q4_0") else "q8_0"
+            self.moe = [MoeLayer(mem, layer, device, fmt=fmt) for layer in range(n)]
         else:
             raise ValueError(name)
         self._pack_arenas()
@@ -279,10 +291,10 @@ class Workload:
             self.step()  # both launches of the fused layer stream weights
         elif self.moe is not None:
             for m in self.moe:
-                self.mem.memra_q8_0_moe_gemv(m.gq, m.gd, m.ids, None, m.xq[0], m.xd[0], False,
-                                             y=m.ygu, dev_status=m.status)
-                self.mem.memra_q8_0_moe_gemv(m.dq, m.dd, m.ids, m.gw, m.hq, m.hd, True,
-                                             y=m.y, dev_status=m.status)
+                m.gemv(self.mem, m.gq, m.gd, m.ids, None, m.xq[0], m.xd[0], False,
+                       y=m.ygu, dev_status=m.status)
+                m.gemv(self.mem, m.dq, m.dd, m.ids, m.gw, m.hq, m.hd, True,
+                       y=m.y, dev_status=m.status)
         else:
             for op in self.ops:
                 run_gemv_op(self.mem, op, quantize=False, fused=self.fused)
@@ -511,7 +523,7 @@ def workload_config(name, wl):
                     "activations": "bf16 N(0,1), 0.1% of entries x20"})
     elif name == "gemv_4096":
         cfg.update({"N": 4096, "K": 4096, "M": 1, "weight_copies": len(wl.ops)})
-    elif name == "moe_top8":
+    elif name.startswith("moe_top8"):
         cfg.update(dict(synth.MOE))
     elif name == "stress_lm_head":
         cfg.update({"shapes": [[n, N, K] for n, N, K in synth.STRESS["shapes"]], "M": [1, 8]})
@@ -648,7 +660,7 @@ def run_memra(args):
             "data": "synthetic (seeded N(0,0.02) weights, bf16 N(0,1) activations)",
             "config": cfg,
             "us_per_step": round(ms_per_step * 1e3, 2),
-            "tok_per_s": round(1e3 / ms_per_step, 2) if args.workload == "moe_top8" or
+            "tok_per_s": round(1e3 / ms_per_step, 2) if args.workload.startswith("moe_top8") or
             args.workload.startswith(("dense27b_sweep", "verify_m")) else None,
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "hbm_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),

@@ -53,6 +53,7 @@ _SIGS = {
     "memra_quantize_q4_0": [_p, _i64, _i64, _p, _p, _p],
     "memra_q4_0_gemv": [_p, _p, _i64, _i64, _p, _p, _p, _p],
     "memra_q4_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
+    "memra_q4_0_moe_gemv": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p, _p],
     "memra_q8_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
     "memra_q8_0_quant_gemm": [_p, _p, _i64, _i64, _i64, _p, _i32, _p, _p],
     "memra_q8_0_moe_gemv": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p, _p],
@@ -287,14 +288,11 @@ def memra_q4_0_gemv(wq4, wd, xq, xd, y=None):
     return y
 
 
-def memra_q8_0_moe_gemv(wq_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert, y=None,
-                        dev_status=None):
-    """Routed-expert GEMV.  wq_bank int8 [E, N, K], wd_bank float16 [E, N, K/32],
-    ids int32 [top_k], gate_w float32 [top_k] or None.  x_per_expert=False: xq [K],
-    xd [K/32]; True: xq [top_k, K], xd [top_k, K/32].  Returns y [top_k, N] without
-    gate weights, [N] with them."""
-    _need(wq_bank, "wq_bank", torch.int8)
-    E, N, K = wq_bank.shape
+def _moe_gemv(fn, wq_bank, qdtype, kmul, wd_bank, ids, gate_w, xq, xd, x_per_expert, y,
+              dev_status):
+    _need(wq_bank, "wq_bank", qdtype)
+    E, N, Kq = wq_bank.shape
+    K = Kq * kmul
     dev = wq_bank.device
     _need(wd_bank, "wd_bank", torch.float16, dev, (E, N, K // 32))
     _need(ids, "ids", torch.int32, dev)
@@ -315,11 +313,28 @@ def memra_q8_0_moe_gemv(wq_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert, y=N
     if dev_status is not None:
         _need(dev_status, "dev_status", torch.int32, dev, (1,))
     with torch.cuda.device(dev):
-        _check("memra_q8_0_moe_gemv",
-               lib().memra_q8_0_moe_gemv(_ptr(wq_bank), _ptr(wd_bank), E, N, K, _ptr(ids),
-                                         _ptr(gate_w), top_k, _ptr(xq), _ptr(xd), xpe, _ptr(y),
-                                         _ptr(dev_status), _stream(wq_bank)))
+        _check(fn, getattr(lib(), fn)(_ptr(wq_bank), _ptr(wd_bank), E, N, K, _ptr(ids),
+                                      _ptr(gate_w), top_k, _ptr(xq), _ptr(xd), xpe, _ptr(y),
+                                      _ptr(dev_status), _stream(wq_bank)))
     return y
+
+
+def memra_q8_0_moe_gemv(wq_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert, y=None,
+                        dev_status=None):
+    """Routed-expert GEMV.  wq_bank int8 [E, N, K], wd_bank float16 [E, N, K/32],
+    ids int32 [top_k], gate_w float32 [top_k] or None.  x_per_expert=False: xq [K],
+    xd [K/32]; True: xq [top_k, K], xd [top_k, K/32].  Returns y [top_k, N] without
+    gate weights, [N] with them."""
+    return _moe_gemv("memra_q8_0_moe_gemv", wq_bank, torch.int8, 1, wd_bank, ids, gate_w, xq,
+                     xd, x_per_expert, y, dev_status)
+
+
+def memra_q4_0_moe_gemv(wq4_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert, y=None,
+                        dev_status=None):
+    """memra_q8_0_moe_gemv on a Q4_0 bank: wq4_bank uint8 [E, N, K/2] (packed codes),
+    wd_bank float16 [E, N, K/32]."""
+    return _moe_gemv("memra_q4_0_moe_gemv", wq4_bank, torch.uint8, 2, wd_bank, ids, gate_w, xq,
+                     xd, x_per_expert, y, dev_status)
 
 
 def memra_q8_0_moe_ffn(gu_q, gu_d, dn_q, dn_d, ids, gate_w, x, y=None, workspace=None,

@@ -1259,11 +1259,15 @@ extern "C" memra_status memra_q8_0_quant_gemm(const int8_t* wq, const uint16_t* 
   return dispatch_m<kDense, kXf32>(p, (int)M, stream);
 }
 
-extern "C" memra_status memra_q8_0_moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank,
-                                            int64_t E, int64_t N, int64_t K, const int32_t* ids,
-                                            const float* gate_w, int64_t top_k, const int8_t* xq,
-                                            const float* xd, int32_t x_per_expert, float* y,
-                                            int32_t* dev_status, cudaStream_t stream) {
+namespace memra {
+namespace {
+// The routed-expert GEMV for either weight format (wq_bank: int8 [E][N][K] for Q8_0,
+// packed uint8 [E][N][K/2] for Q4_0).
+template <int FMT>
+memra_status moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank, int64_t E, int64_t N,
+                      int64_t K, const int32_t* ids, const float* gate_w, int64_t top_k,
+                      const int8_t* xq, const float* xd, int32_t x_per_expert, float* y,
+                      int32_t* dev_status, cudaStream_t stream) {
   if (E < 1 || N < 0 || K < 0 || K % 32 != 0 || top_k < 1) return MEMRA_ERR_INVALID_ARG;
   if (x_per_expert != 0 && x_per_expert != 1) return MEMRA_ERR_INVALID_ARG;
   if (top_k > MEMRA_MAX_TOP_K) return MEMRA_ERR_UNSUPPORTED;
@@ -1275,8 +1279,14 @@ extern "C" memra_status memra_q8_0_moe_gemv(const int8_t* wq_bank, const uint16_
     return MEMRA_ERR_ALIGNMENT;
   if (K == 0) return zero_fill(y, gate_w ? N : top_k * N, stream);
   if (!wq_bank || !wd_bank || !xq || !xd) return MEMRA_ERR_INVALID_ARG;
-  if (!aligned(wq_bank, 32) || !aligned(wd_bank, 2) || !aligned(xq, 16) || !aligned(xd, 4))
+  if (FMT == kQ4) {
+    if (K % 256 != 0) return MEMRA_ERR_UNSUPPORTED;
+    if (!aligned(wq_bank, 16) || !aligned(wd_bank, 16) || !aligned(xq, 16) || !aligned(xd, 16))
+      return MEMRA_ERR_ALIGNMENT;
+  } else if (!aligned(wq_bank, 32) || !aligned(wd_bank, 2) || !aligned(xq, 16) ||
+             !aligned(xd, 4)) {
     return MEMRA_ERR_ALIGNMENT;
+  }
   const int64_t xrows = x_per_expert ? top_k : 1;
   if (!x_fits(xrows, K)) return MEMRA_ERR_UNSUPPORTED;
   Params p{};
@@ -1296,10 +1306,30 @@ extern "C" memra_status memra_q8_0_moe_gemv(const int8_t* wq_bank, const uint16_
   p.status = dev_status;
   if (gate_w) {
     p.units = N;
-    return run_product<1, 1, kMoeGated, kXq8>(p, stream);
+    return run_product<1, 1, kMoeGated, kXq8, FMT>(p, stream);
   }
   p.units = top_k * N;
-  return run_product<1, 1, kMoeUngated, kXq8>(p, stream);
+  return run_product<1, 1, kMoeUngated, kXq8, FMT>(p, stream);
+}
+}  // namespace
+}  // namespace memra
+
+extern "C" memra_status memra_q8_0_moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank,
+                                            int64_t E, int64_t N, int64_t K, const int32_t* ids,
+                                            const float* gate_w, int64_t top_k, const int8_t* xq,
+                                            const float* xd, int32_t x_per_expert, float* y,
+                                            int32_t* dev_status, cudaStream_t stream) {
+  return moe_gemv<kQ8>(wq_bank, wd_bank, E, N, K, ids, gate_w, top_k, xq, xd, x_per_expert, y,
+                       dev_status, stream);
+}
+
+extern "C" memra_status memra_q4_0_moe_gemv(const uint8_t* wq4_bank, const uint16_t* wd_bank,
+                                            int64_t E, int64_t N, int64_t K, const int32_t* ids,
+                                            const float* gate_w, int64_t top_k, const int8_t* xq,
+                                            const float* xd, int32_t x_per_expert, float* y,
+                                            int32_t* dev_status, cudaStream_t stream) {
+  return moe_gemv<kQ4>(reinterpret_cast<const int8_t*>(wq4_bank), wd_bank, E, N, K, ids, gate_w,
+                       top_k, xq, xd, x_per_expert, y, dev_status, stream);
 }
 
 extern "C" memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* gu_d,

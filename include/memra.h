@@ -221,6 +221,21 @@ memra_status memra_q8_0_moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank,
                                  cudaStream_t stream);
 
 /*
+ * memra_q8_0_moe_gemv on a Q4_0 expert bank (the pages credit wide loads of Q4_0
+ * expert weights for part of their MoE margins: memra performance, docs/
+ * PERFORMANCE.md, Gemma-4 QAT Q4_0 board; memra wiki, the same board): wq4_bank uint8 [E][N][K/2]
+ * packed as memra_quantize_q4_0 packs a weight matrix, wd_bank fp16 [E][N][K/32].
+ * Same arguments, outputs, id handling and dev_status as memra_q8_0_moe_gemv; the
+ * block sums are those of memra_q4_0_gemm_small_m.  K must be a multiple of 256
+ * (MEMRA_ERR_UNSUPPORTED otherwise); wq4_bank, wd_bank, xq and xd 16-byte aligned.
+ */
+memra_status memra_q4_0_moe_gemv(const uint8_t* wq4_bank, const uint16_t* wd_bank, int64_t E,
+                                 int64_t N, int64_t K, const int32_t* ids, const float* gate_w,
+                                 int64_t top_k, const int8_t* xq, const float* xd,
+                                 int32_t x_per_expert, float* y, int32_t* dev_status,
+                                 cudaStream_t stream);
+
+/*
  * SwiGLU between the routed gate/up and down projections, followed by q8_1
  * quantisation (the MoE FFN's activation; the pages put the routed experts in the
  * qwen/silu MoE class: memra performance, "Shipped on the sm_90a build").  The

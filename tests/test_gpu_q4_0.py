@@ -103,3 +103,38 @@ def test_q4_0_rejects_k_not_multiple_of_256(mem):
     with pytest.raises(mem.MemraError) as e:
         mem.memra_q4_0_gemm_small_m(wq4, wd, xq, xd)
     assert e.value.status == 3
+
+
+@pytest.mark.parametrize("gated,per_expert", [(False, False), (True, True), (True, False)])
+def test_q4_0_moe_gemv_parity(mem, orc, gated, per_expert):
+    """Routed experts on a Q4_0 bank: against the oracle's routed product of the unpacked
+    codes, and bit for bit the Q8_0 routed product of the same codes."""
+    E, N, K, top_k = 12, 200, 768, 8
+    w = torch.stack([synth.weights_fp32(N, K, 61, e) for e in range(E)])
+    wq4, wd, oq4, od = check_q4_weights(orc, mem, w.view(E * N, K))
+    bank4, bankd = wq4.view(E, N, K // 2), wd.view(E, N, K // 32)
+    ids = torch.tensor([3, 11, 0, 7, 3, 5, 9, 1], dtype=torch.int32)
+    gw = torch.tensor([0.2, 0.15, 0.1, 0.1, 0.15, 0.1, 0.1, 0.1], dtype=torch.float32)
+    x = synth.activations_bf16(top_k if per_expert else 1, K, 62)
+    xq, xd = mem.memra_quantize_q8_1(x.cuda())
+    oxq, oxd = orc.quantize_q8_1(bf16_bits_np(x))
+    assert np.array_equal(np_(xq), oxq)
+    xq_in, xd_in = (xq, xd) if per_expert else (xq[0], xd[0])
+    gw_in = gw.cuda() if gated else None
+    y = mem.memra_q4_0_moe_gemv(bank4, bankd, ids.cuda(), gw_in, xq_in, xd_in, per_expert)
+    bank8 = unpack_torch(wq4).view(E, N, K)
+    y8 = mem.memra_q8_0_moe_gemv(bank8, bankd, ids.cuda(), gw_in, xq_in, xd_in, per_expert)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), y8.view(torch.int32))
+    o8 = orc.unpack_q4_0(oq4).reshape(E, N, K)
+    odb = od.reshape(E, N, K // 32)
+    y_ref, bad = orc.moe_gemv(o8, odb, np_(ids), np_(gw) if gated else None, oxq, oxd,
+                              1 if per_expert else 0)
+    assert bad == 0
+    terms = np.stack([abs_terms(orc.block_dots(o8[e], oxq[k:k + 1] if per_expert else oxq),
+                                odb[e], oxd[k:k + 1] if per_expert else oxd)[0]
+                      for k, e in enumerate(np_(ids))])
+    if gated:
+        assert_within(np_(y), y_ref, (np_(gw)[:, None] * terms).sum(axis=0), "q4_0 moe gated")
+    else:
+        assert_within(np_(y), y_ref, terms, "q4_0 moe")
