@@ -494,8 +494,7 @@ extern "C" memra_status memra_q8_0_gemv_chain(const memra_q8_0_step* steps,
   p.off_slice = (uint32_t)off;
   // Every CTA must be resident at once (the grid barrier waits for all of them):
   // a cooperative launch of as many CTAs as fit, up to two per SM.
-  cudaError_t e = cudaFuncSetAttribute(q8_chain_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_dynamic_smem(q8_chain_kernel, smem, info);
   if (e != cudaSuccess) return cuda_fail(e);
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q8_chain_kernel, kChainThreads,

@@ -307,6 +307,18 @@ memra_status check_launch();
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
+// Let `kernel` take more than 48 KB of dynamic shared memory.  The attribute goes to
+// the device's opt-in maximum, never to one launch's size: a CUDA graph captured
+// earlier can hold launches of the same kernel with larger sizes, and lowering the
+// attribute would make those launches invalid wherever they are checked again (a
+// profiler re-issues graph nodes as single launches).
+template <typename Kern>
+cudaError_t allow_dynamic_smem(Kern kernel, size_t smem, const DeviceInfo& info) {
+  if (smem <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              info.max_smem_optin);
+}
+
 // Programmatic dependent launch is on unless the environment sets MEMRA_PDL=0
 // (read once per process).
 bool pdl_enabled();

@@ -1070,13 +1070,10 @@ bool plan_reg(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
 
 template <typename Kern>
 memra_status launch(Kern kernel, int64_t grid, int threads, size_t smem, cudaStream_t stream,
-                    const Params& p) {
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e);
-  }
-  cudaError_t e = launch_kernel(kernel, dim3((unsigned)grid), dim3(threads), smem, stream, p);
+                    const DeviceInfo& info, const Params& p) {
+  cudaError_t e = allow_dynamic_smem(kernel, smem, info);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch_kernel(kernel, dim3((unsigned)grid), dim3(threads), smem, stream, p);
   if (e != cudaSuccess) return cuda_fail(e);
   return MEMRA_OK;
 }
@@ -1105,12 +1102,13 @@ memra_status run_product(Params p, cudaStream_t stream) {
       grid = std::min<int64_t>(p.units, info.sms);
       if (!plan_tma<M, R, MODE, XIN, FMT>(p, info, grid, &smem)) return MEMRA_ERR_UNSUPPORTED;
     }
-    return launch(q8_tma_kernel<M, R, MODE, XIN, FMT>, grid, tma_threads(M), smem, stream, p);
+    return launch(q8_tma_kernel<M, R, MODE, XIN, FMT>, grid, tma_threads(M), smem, stream, info,
+                  p);
   }
   if (FMT == kQ4) return MEMRA_ERR_UNSUPPORTED;  // Q4_0 runs on the bulk-copy kernel only
   grid = std::min<int64_t>(p.units, (int64_t)info.sms * reg_grid_ctas_per_sm(M));
   if (plan_reg<M, R, MODE, XIN>(p, info, grid, &smem))
-    return launch(q8_reg_kernel<M, R, MODE, XIN>, grid, kRegThreads, smem, stream, p);
+    return launch(q8_reg_kernel<M, R, MODE, XIN>, grid, kRegThreads, smem, stream, info, p);
   return MEMRA_ERR_UNSUPPORTED;
 }
 
