@@ -37,6 +37,8 @@ def lib():
         L.oracle_quantize_q8_0.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         L.oracle_quantize_q4_0.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         L.oracle_unpack_q4_0.argtypes = [_ptr, _i64, _i64, _ptr]
+        L.oracle_repack_q8_0.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
+        L.oracle_repack_q4_0.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         L.oracle_quantize_q8_1_f32.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         L.oracle_quantize_q8_1_bf16.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         L.oracle_block_dots.argtypes = [_ptr, _i64, _i64, _ptr, _i64, _ptr]
@@ -123,6 +125,26 @@ def unpack_q4_0(q4):
     wq = np.empty((N, 2 * K2), np.int8)
     lib().oracle_unpack_q4_0(_p(q4), N, 2 * K2, _p(wq))
     return wq
+
+
+def repack_q8_0(blocks, N, K):
+    """GGUF Q8_0 block bytes uint8 [N * K/32 * 34] -> (wq int8 [N, K], wd fp16 bits [N, K/32])."""
+    blocks = _c(np.asarray(blocks).reshape(-1), np.uint8)
+    assert K % 32 == 0 and blocks.size == N * (K // 32) * 34
+    q = np.empty((N, K), np.int8)
+    d = np.empty((N, K // 32), np.uint16)
+    lib().oracle_repack_q8_0(_p(blocks), N, K, _p(q), _p(d))
+    return q, d
+
+
+def repack_q4_0(blocks, N, K):
+    """GGUF Q4_0 block bytes uint8 [N * K/32 * 18] -> (q4 uint8 [N, K/2], wd fp16 bits [N, K/32])."""
+    blocks = _c(np.asarray(blocks).reshape(-1), np.uint8)
+    assert K % 32 == 0 and blocks.size == N * (K // 32) * 18
+    q4 = np.empty((N, K // 2), np.uint8)
+    d = np.empty((N, K // 32), np.uint16)
+    lib().oracle_repack_q4_0(_p(blocks), N, K, _p(q4), _p(d))
+    return q4, d
 
 
 def gemm_q4_0(q4, wd, xq, xd, threads=1):

@@ -211,6 +211,39 @@ void oracle_unpack_q4_0(const uint8_t* q4, int64_t N, int64_t K, int8_t* wq) {
 }
 
 // ---------------------------------------------------------------------------
+// Repack from GGUF's interleaved block arrays to the two planes (the pages' "split-
+// plane repacked" matvecs: memra wiki, feature list).  The pages print neither
+// layout; the reading is GGUF's:
+//   Q8_0 block, 34 bytes: the fp16 scale (little-endian), then the 32 int8 quants;
+//   Q4_0 block, 18 bytes: the fp16 scale (little-endian), then 16 bytes whose byte j
+//        holds element j's code in its low nibble and element j+16's in its high one.
+// A row of K weights is K/32 consecutive blocks, rows one after another.  The
+// repack is byte for byte: no value is changed.
+// ---------------------------------------------------------------------------
+void oracle_repack_q8_0(const uint8_t* blocks, int64_t N, int64_t K, int8_t* q, uint16_t* d) {
+  const int64_t nb = K / 32;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t* blk = blocks + (n * nb + b) * 34;
+      d[n * nb + b] = (uint16_t)(blk[0] | (blk[1] << 8));
+      for (int i = 0; i < 32; ++i) {
+        const int v = blk[2 + i];
+        q[n * K + b * 32 + i] = (int8_t)(v < 128 ? v : v - 256);
+      }
+    }
+}
+
+void oracle_repack_q4_0(const uint8_t* blocks, int64_t N, int64_t K, uint8_t* q4, uint16_t* d) {
+  const int64_t nb = K / 32;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t* blk = blocks + (n * nb + b) * 18;
+      d[n * nb + b] = (uint16_t)(blk[0] | (blk[1] << 8));
+      for (int j = 0; j < 16; ++j) q4[n * (K / 2) + b * 16 + j] = blk[2 + j];
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Activation quantisation ("q8_1" blocks with an fp32 scale).
 // x: [M][K] fp32 or bf16 bits.  q: int8 [M][K].  d: fp32 [M][K/32].
 // Per block: amax = max|x|; d = amax / 127 in fp32; q = clamp(round-half-away(

@@ -57,3 +57,27 @@ def test_q4_0_hand_block(orc):
     tq4, twd = orc.quantize_q4_0(np.array(g["tie_w"], np.float32)[None])
     assert (orc.unpack_q4_0(tq4).ravel() + 8).tolist() == g["tie_codes"]
     assert int(twd[0, 0]) == g["tie_wd_f16_bits"]
+
+
+def test_gguf_q8_0_blocks_repack(orc):
+    g = load("gguf_blocks.json")["q8_0"]
+    N, K = g["N"], g["K"]
+    blocks = np.frombuffer(bytes.fromhex(g["bytes_hex"]), np.uint8)
+    wq, wd = orc.repack_q8_0(blocks, N, K)
+    assert wq.ravel().tolist() == g["wq"]
+    assert wd.ravel().tolist() == g["wd_f16_bits"]
+    assert orc.f16_bits_to_f32(wd).ravel().tolist() == g["wd_values"]
+
+
+def test_gguf_q4_0_blocks_repack(orc):
+    g = load("gguf_blocks.json")["q4_0"]
+    N, K = g["N"], g["K"]
+    blocks = np.frombuffer(bytes.fromhex(g["bytes_hex"]), np.uint8)
+    q4, wd = orc.repack_q4_0(blocks, N, K)
+    assert q4.tolist() == g["q4"]
+    assert wd.ravel().tolist() == g["wd_f16_bits"]
+    assert orc.f16_bits_to_f32(wd).ravel().tolist() == g["wd_values"]
+    # The repacked codes are the hand-quantised block's, and row 1 is all zeros.
+    vals = orc.unpack_q4_0(q4)
+    assert (vals[0].astype(int) + 8).tolist() == g["codes_row0"]
+    assert not vals[1].any()

@@ -562,3 +562,65 @@ def test_q4_0_gemm_within_bound_of_fp64_brute_force(orc, N, K, M):
     dx = np.repeat(xd.astype(np.float64), 32, axis=1)
     qerr = np.abs(Xd) @ dw.T + (dx / 2) @ np.abs(Wd).T + (dx / 2) @ dw.T
     assert np.all(np.abs(y - exact) <= qerr + 1e-4 * terms + 1e-6)
+
+
+# ----------------------------------------------------------------------------
+# GGUF block arrays -> planes.  numpy's packed structured dtypes lay the blocks out
+# independently of the oracle: fp16 scale little-endian, then the quants.
+# ----------------------------------------------------------------------------
+
+Q8_0_BLOCK = np.dtype([("d", "<u2"), ("qs", "i1", (32,))])
+Q4_0_BLOCK = np.dtype([("d", "<u2"), ("qs", "u1", (16,))])
+
+
+def test_gguf_block_dtypes_are_packed():
+    assert Q8_0_BLOCK.itemsize == 34 and Q4_0_BLOCK.itemsize == 18
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (7, 96), (33, 512)])
+def test_repack_q8_0_round_trip(orc, N, K):
+    r = rng(60 + N)
+    w = (r.standard_normal((N, K)) * 0.02).astype(np.float32)
+    wq, wd = orc.quantize_q8_0(w)
+    aos = np.empty((N, K // 32), Q8_0_BLOCK)
+    aos["d"] = wd
+    aos["qs"] = wq.reshape(N, K // 32, 32)
+    q2, d2 = orc.repack_q8_0(aos.view(np.uint8), N, K)
+    assert np.array_equal(q2, wq) and np.array_equal(d2, wd)
+    # The dequantised weights by the block definition (d * q, scale from the block's
+    # first two bytes) equal those of the planes.
+    raw = aos.view(np.uint8).reshape(N, K // 32, 34)
+    d_blk = (raw[:, :, 0].astype(np.uint16) | (raw[:, :, 1].astype(np.uint16) << 8))
+    deq_blk = d_blk.view(np.float16).astype(np.float64)[:, :, None] * \
+        raw[:, :, 2:].view(np.int8).astype(np.float64)
+    deq_pl = orc.f16_bits_to_f32(d2).astype(np.float64)[:, :, None] * \
+        q2.reshape(N, K // 32, 32).astype(np.float64)
+    assert np.array_equal(deq_blk, deq_pl)
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (5, 256), (17, 1024)])
+def test_repack_q4_0_round_trip(orc, N, K):
+    r = rng(70 + N)
+    w = (r.standard_normal((N, K)) * 0.02).astype(np.float32)
+    q4, wd = orc.quantize_q4_0(w)
+    aos = np.empty((N, K // 32), Q4_0_BLOCK)
+    aos["d"] = wd
+    aos["qs"] = q4.reshape(N, K // 32, 16)
+    q2, d2 = orc.repack_q4_0(aos.view(np.uint8), N, K)
+    assert np.array_equal(q2, q4) and np.array_equal(d2, wd)
+    # Element j of a block is byte j's low nibble, element j + 16 its high nibble.
+    raw = aos.view(np.uint8).reshape(N, K // 32, 18)[:, :, 2:].astype(np.int16)
+    vals = np.concatenate([(raw & 15) - 8, (raw >> 4) - 8], axis=2).reshape(N, K)
+    assert np.array_equal(orc.unpack_q4_0(q2), vals.astype(np.int8))
+
+
+def test_repack_is_a_byte_permutation(orc):
+    """Every input byte lands in exactly one output byte, unchanged: repack a block array
+    whose bytes are all distinct positions' indices (mod 256, per byte plane)."""
+    N, K = 3, 64
+    nblk = N * K // 32
+    raw = (np.arange(nblk * 34) % 251).astype(np.uint8)
+    q, d = orc.repack_q8_0(raw, N, K)
+    blk = raw.reshape(nblk, 34)
+    assert np.array_equal(q.view(np.uint8).reshape(nblk, 32), blk[:, 2:])
+    assert np.array_equal(d.reshape(nblk).view(np.uint8).reshape(nblk, 2), blk[:, :2])
