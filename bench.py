@@ -15,7 +15,8 @@ peak; ``cpu_baseline`` is the CPU oracle on the host cores over a bounded sample
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl memra|reference]
                   [--workload dense27b_sweep|gemv_4096|verify_m2|verify_m4|verify_m8|
-                              moe_top8|stress_lm_head]
+                              batch_m16|moe_top8|stress_lm_head|dense27b_sweep_q4_0|
+                              moe_top8_q4_0]
 """
 import argparse
 import hashlib
@@ -38,7 +39,8 @@ METRIC = ("Q8_0 decode GEMV weight-stream GB/s (% of GB300 HBM peak); "
           "µs per 27B layer sweep")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8", "moe_top8",
+WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8", "batch_m16",
+             "moe_top8",
              "stress_lm_head", "dense27b_sweep_q4_0", "moe_top8_q4_0")
 
 
@@ -75,6 +77,15 @@ def quantized_weights(mem, N, K, *keys, device, perturb=None, fmt="q8_0"):
         wq, wd = mem.memra_quantize_q8_0(w)
     del w
     return wq, wd
+
+
+def rows_of(name):
+    """Activation rows of a dense-sweep workload: verify_mM and batch_mM have M, the
+    plain sweeps 1."""
+    for prefix in ("verify_m", "batch_m"):
+        if name.startswith(prefix):
+            return int(name[len(prefix):])
+    return 1
 
 
 def build_dense_sweep(mem, device, M=1, layers=None, workload_id=1, fmt="q8_0"):
@@ -198,8 +209,8 @@ class Workload:
         elif name == "dense27b_sweep_q4_0":
             self.ops = build_dense_sweep(mem, device, M=1, layers=layers, workload_id=5,
                                          fmt="q4_0")
-        elif name.startswith("verify_m"):
-            self.ops = build_dense_sweep(mem, device, M=int(name[len("verify_m"):]),
+        elif name.startswith(("verify_m", "batch_m")):
+            self.ops = build_dense_sweep(mem, device, M=rows_of(name),
                                          layers=layers, workload_id=2)
         elif name == "gemv_4096":
             self.ops = build_gemv_4096(mem, device)
@@ -257,12 +268,19 @@ class Workload:
                 op.x, op.y = new_in[id(op.x)], y
 
     @property
+    def passes(self):
+        """Product launches per dense product: batches above 8 rows take two passes."""
+        if self.moe is not None or self.chain is not None:
+            return 1
+        return 2 if self.ops[0].xq.shape[0] > 8 else 1
+
+    @property
     def launches_per_step(self):
         if self.chain is not None:
             return 1
         if self.moe is not None:
             return (2 if self.fused else 4) * len(self.moe)
-        return (1 if self.fused else 2) * len(self.ops)
+        return (self.passes + (0 if self.fused else 1)) * len(self.ops)
 
     @property
     def gemv_launches_per_step(self):
@@ -270,7 +288,7 @@ class Workload:
             return 1
         if self.moe is not None:
             return 2 * len(self.moe)
-        return len(self.ops)
+        return self.passes * len(self.ops)
 
     def step(self):
         if self.chain is not None:
@@ -516,11 +534,14 @@ class CpuOracleSample:
 
 def workload_config(name, wl):
     cfg = {"workload": name}
-    if name.startswith("dense27b_sweep") or name.startswith("verify_m"):
+    if name.startswith(("dense27b_sweep", "verify_m", "batch_m")):
         cfg.update({"layers": len(wl.ops) // 4, "hidden": synth.DENSE27B["hidden"],
                     "gemvs_per_layer": [[n, N, K] for n, N, K in synth.DENSE27B["gemvs"]],
-                    "M": int(name[len("verify_m"):]) if name.startswith("verify_m") else 1,
+                    "M": rows_of(name),
                     "activations": "bf16 N(0,1), 0.1% of entries x20"})
+        if name.startswith("batch_m"):
+            cfg["sequences"] = rows_of(name)
+            cfg["passes_per_product"] = 2 if rows_of(name) > 8 else 1
     elif name == "gemv_4096":
         cfg.update({"N": 4096, "K": 4096, "M": 1, "weight_copies": len(wl.ops)})
     elif name.startswith("moe_top8"):
@@ -583,7 +604,8 @@ def run_memra(args):
     g_elapsed = time_graph(gemv_graph, args.steps, stream)
     n_gemv = wl.gemv_launches_per_step * args.steps
     gemv_avg_s = g_elapsed / n_gemv
-    bytes_per_launch = bytes_step / wl.gemv_launches_per_step
+    # Each launch streams its product's weights once (a two-pass batch streams them twice).
+    bytes_per_launch = bytes_step * wl.passes / wl.gemv_launches_per_step
     achieved = bytes_per_launch / gemv_avg_s / 1e9
     peak, peak_kind = measured_peaks()
     prof = profile_traffic(kernel_source_hash())
@@ -599,7 +621,9 @@ def run_memra(args):
                     "chained, one launch per step" if wl.chain is not None else
                     "routed experts" if wl.moe is not None else
                     ("quantise fused" if wl.fused else "q8_1 input"),
-                    1 if wl.moe is not None else wl.ops[0].xq.shape[0]),
+                    1 if wl.moe is not None else "%d%s" % (
+                        wl.ops[0].xq.shape[0],
+                        " in 2 passes" if wl.passes == 2 else "")),
                 "avg_launch_us": round(gemv_avg_s * 1e6, 3),
                 "bytes_per_launch": int(bytes_per_launch),
                 "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
@@ -660,8 +684,9 @@ def run_memra(args):
             "data": "synthetic (seeded N(0,0.02) weights, bf16 N(0,1) activations)",
             "config": cfg,
             "us_per_step": round(ms_per_step * 1e3, 2),
-            "tok_per_s": round(1e3 / ms_per_step, 2) if args.workload.startswith("moe_top8") or
-            args.workload.startswith(("dense27b_sweep", "verify_m")) else None,
+            "tok_per_s": round(1e3 * (rows_of(args.workload) if args.workload.startswith(
+                "batch_m") else 1) / ms_per_step, 2) if args.workload.startswith(
+                ("moe_top8", "dense27b_sweep", "verify_m", "batch_m")) else None,
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "hbm_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
             "roofline": roofline,

@@ -22,7 +22,7 @@ from . import build as _build
 MEMRA_OK = 0
 MEMRA_BF16 = 0
 MEMRA_F32 = 1
-MAX_M = 8
+MAX_M = 16
 MAX_TOP_K = 64
 MOE_NOALLOC_SCRATCH_FLOATS = 65536
 
@@ -51,6 +51,8 @@ _SIGS = {
     "memra_quantize_q8_1": [_p, _i32, _i64, _i64, _p, _p, _p],
     "memra_q8_0_gemv": [_p, _p, _i64, _i64, _p, _p, _p, _p],
     "memra_quantize_q4_0": [_p, _i64, _i64, _p, _p, _p],
+    "memra_repack_q8_0": [_p, _i64, _i64, _p, _p, _p],
+    "memra_repack_q4_0": [_p, _i64, _i64, _p, _p, _p],
     "memra_q4_0_gemv": [_p, _p, _i64, _i64, _p, _p, _p, _p],
     "memra_q4_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
     "memra_q4_0_moe_gemv": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p, _p],
@@ -162,6 +164,43 @@ def memra_quantize_q4_0(w, wq4=None, wd=None):
     return wq4, wd
 
 
+def _blocks(blocks, N, K, block_bytes):
+    _need(blocks, "blocks", torch.uint8)
+    if K % 32 != 0 or blocks.numel() != N * (K // 32) * block_bytes:
+        raise ValueError("blocks must hold N * K/32 blocks of %d bytes (N=%d, K=%d), got %d bytes"
+                         % (block_bytes, N, K, blocks.numel()))
+
+
+def memra_repack_q8_0(blocks, N, K, wq=None, wd=None):
+    """GGUF Q8_0 block bytes (uint8, N * K/32 * 34) -> (wq int8 [N, K], wd float16 [N, K/32])."""
+    _blocks(blocks, N, K, 34)
+    if wq is None:
+        wq = torch.empty((N, K), dtype=torch.int8, device=blocks.device)
+    if wd is None:
+        wd = torch.empty((N, K // 32), dtype=torch.float16, device=blocks.device)
+    _need(wq, "wq", torch.int8, blocks.device, (N, K))
+    _need(wd, "wd", torch.float16, blocks.device, (N, K // 32))
+    with torch.cuda.device(blocks.device):
+        _check("memra_repack_q8_0",
+               lib().memra_repack_q8_0(_ptr(blocks), N, K, _ptr(wq), _ptr(wd), _stream(blocks)))
+    return wq, wd
+
+
+def memra_repack_q4_0(blocks, N, K, wq4=None, wd=None):
+    """GGUF Q4_0 block bytes (uint8, N * K/32 * 18) -> (wq4 uint8 [N, K/2], wd float16 [N, K/32])."""
+    _blocks(blocks, N, K, 18)
+    if wq4 is None:
+        wq4 = torch.empty((N, K // 2), dtype=torch.uint8, device=blocks.device)
+    if wd is None:
+        wd = torch.empty((N, K // 32), dtype=torch.float16, device=blocks.device)
+    _need(wq4, "wq4", torch.uint8, blocks.device, (N, K // 2))
+    _need(wd, "wd", torch.float16, blocks.device, (N, K // 32))
+    with torch.cuda.device(blocks.device):
+        _check("memra_repack_q4_0",
+               lib().memra_repack_q4_0(_ptr(blocks), N, K, _ptr(wq4), _ptr(wd), _stream(blocks)))
+    return wq4, wd
+
+
 def memra_quantize_q8_1(x, xq=None, xd=None):
     """Activations [M, K] (bf16 or fp32) -> (xq int8 [M, K], xd float32 [M, K/32])."""
     if x.dtype == torch.bfloat16:
@@ -185,7 +224,7 @@ def memra_quantize_q8_1(x, xq=None, xd=None):
 
 
 def memra_q8_0_gemm_small_m(wq, wd, xq, xd, y=None):
-    """y [M, N] = W (Q8_0) x (q8_1) for M <= 8 activation rows."""
+    """y [M, N] = W (Q8_0) x (q8_1) for M <= 16 activation rows (two weight passes above 8)."""
     _need(wq, "wq", torch.int8)
     N, K = wq.shape
     dev = wq.device
@@ -249,7 +288,7 @@ def memra_q8_0_gemv(wq, wd, xq, xd, y=None):
 
 
 def memra_q4_0_gemm_small_m(wq4, wd, xq, xd, y=None):
-    """y [M, N] = W (Q4_0: wq4 uint8 [N, K/2], wd float16 [N, K/32]) x (q8_1), M <= 8."""
+    """y [M, N] = W (Q4_0: wq4 uint8 [N, K/2], wd float16 [N, K/32]) x (q8_1), M <= 16."""
     _need(wq4, "wq4", torch.uint8)
     N, K2 = wq4.shape
     K = 2 * K2

@@ -1158,6 +1158,26 @@ bool x_fits(int64_t xrows, int64_t K) {
   return xrows * K + xrows * (K / 32) * 4 <= MEMRA_MAX_X_BYTES;
 }
 
+// A batch of up to MEMRA_MAX_M activation rows runs as passes over the weights of at
+// most kPassRows rows each: one pass up to kPassRows, else ceil(M/2) then floor(M/2)
+// rows.  Every row's arithmetic is the M = 1 arithmetic, so the split changes no bit
+// of y.  From M = 8 on the dp4a issue rate, not the weight stream, sets a pass's time
+// (the 27B verify sweep: 4.33 ms per token at M = 1, 6.85 ms at M = 8), so a second
+// stream of the weights costs little next to the block dots.
+constexpr int64_t kPassRows = 8;
+static_assert(MEMRA_MAX_M <= 2 * kPassRows, "two passes at most");
+
+int64_t pass_rows(int64_t M) { return M <= kPassRows ? M : (M + 1) / 2; }
+
+template <typename Pass>
+memra_status in_passes(int64_t M, Pass&& pass) {
+  if (M <= kPassRows) return pass(0, M);
+  const int64_t m1 = (M + 1) / 2;
+  const memra_status st = pass(0, m1);
+  if (st != MEMRA_OK) return st;
+  return pass(m1, M - m1);
+}
+
 }  // namespace
 }  // namespace memra
 
@@ -1176,18 +1196,20 @@ extern "C" memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t
   if (!wq || !wd || !xq || !xd) return MEMRA_ERR_INVALID_ARG;
   if (!aligned(wq, 32) || !aligned(wd, 2) || !aligned(xq, 16) || !aligned(xd, 4))
     return MEMRA_ERR_ALIGNMENT;
-  if (!x_fits(M, K)) return MEMRA_ERR_UNSUPPORTED;
-  Params p{};
-  p.wq = wq;
-  p.wd = wd;
-  p.N = N;
-  p.K = K;
-  p.xq = xq;
-  p.xd = xd;
-  p.xrows = (int)M;
-  p.y = y;
-  p.units = N;
-  return dispatch_m<kDense, kXq8>(p, (int)M, stream);
+  if (!x_fits(pass_rows(M), K)) return MEMRA_ERR_UNSUPPORTED;
+  return in_passes(M, [&](int64_t m0, int64_t rows) {
+    Params p{};
+    p.wq = wq;
+    p.wd = wd;
+    p.N = N;
+    p.K = K;
+    p.xq = xq + m0 * K;
+    p.xd = xd + m0 * (K / 32);
+    p.xrows = (int)rows;
+    p.y = y + m0 * N;
+    p.units = N;
+    return dispatch_m<kDense, kXq8>(p, (int)rows, stream);
+  });
 }
 
 extern "C" memra_status memra_q8_0_gemv(const int8_t* wq, const uint16_t* wd, int64_t N, int64_t K,
@@ -1210,18 +1232,20 @@ extern "C" memra_status memra_q4_0_gemm_small_m(const uint8_t* wq4, const uint16
   if (K % 256 != 0) return MEMRA_ERR_UNSUPPORTED;
   if (!aligned(wq4, 16) || !aligned(wd, 16) || !aligned(xq, 16) || !aligned(xd, 16))
     return MEMRA_ERR_ALIGNMENT;
-  if (!x_fits(M, K)) return MEMRA_ERR_UNSUPPORTED;
-  Params p{};
-  p.wq = reinterpret_cast<const int8_t*>(wq4);
-  p.wd = wd;
-  p.N = N;
-  p.K = K;
-  p.xq = xq;
-  p.xd = xd;
-  p.xrows = (int)M;
-  p.y = y;
-  p.units = N;
-  return dispatch_m_q4(p, (int)M, stream);
+  if (!x_fits(pass_rows(M), K)) return MEMRA_ERR_UNSUPPORTED;
+  return in_passes(M, [&](int64_t m0, int64_t rows) {
+    Params p{};
+    p.wq = reinterpret_cast<const int8_t*>(wq4);
+    p.wd = wd;
+    p.N = N;
+    p.K = K;
+    p.xq = xq + m0 * K;
+    p.xd = xd + m0 * (K / 32);
+    p.xrows = (int)rows;
+    p.y = y + m0 * N;
+    p.units = N;
+    return dispatch_m_q4(p, (int)rows, stream);
+  });
 }
 
 extern "C" memra_status memra_q4_0_gemv(const uint8_t* wq4, const uint16_t* wd, int64_t N, int64_t K,
@@ -1243,18 +1267,21 @@ extern "C" memra_status memra_q8_0_quant_gemm(const int8_t* wq, const uint16_t* 
   if (K == 0) return zero_fill(y, M * N, stream);
   if (!wq || !wd || !x) return MEMRA_ERR_INVALID_ARG;
   if (!aligned(wq, 32) || !aligned(wd, 2) || !aligned(x, 16)) return MEMRA_ERR_ALIGNMENT;
-  if (!x_fits(M, K)) return MEMRA_ERR_UNSUPPORTED;
-  Params p{};
-  p.wq = wq;
-  p.wd = wd;
-  p.N = N;
-  p.K = K;
-  p.xin = x;
-  p.xrows = (int)M;
-  p.y = y;
-  p.units = N;
-  if (dtype == MEMRA_BF16) return dispatch_m<kDense, kXbf16>(p, (int)M, stream);
-  return dispatch_m<kDense, kXf32>(p, (int)M, stream);
+  if (!x_fits(pass_rows(M), K)) return MEMRA_ERR_UNSUPPORTED;
+  const int64_t x_row_bytes = K * (dtype == MEMRA_BF16 ? 2 : 4);
+  return in_passes(M, [&](int64_t m0, int64_t rows) {
+    Params p{};
+    p.wq = wq;
+    p.wd = wd;
+    p.N = N;
+    p.K = K;
+    p.xin = static_cast<const char*>(x) + m0 * x_row_bytes;
+    p.xrows = (int)rows;
+    p.y = y + m0 * N;
+    p.units = N;
+    if (dtype == MEMRA_BF16) return dispatch_m<kDense, kXbf16>(p, (int)rows, stream);
+    return dispatch_m<kDense, kXf32>(p, (int)rows, stream);
+  });
 }
 
 namespace memra {

@@ -194,6 +194,49 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
+// GGUF block arrays -> planes, one thread per block.  A block starts on a 2-byte
+// boundary only (34 or 18 bytes long), so it is read as 16-bit words; word 0 is the
+// fp16 scale (little-endian, as on the device) and the quant bytes follow in order.
+// The quants leave in 16-byte stores: block i of the flattened [N][K/32] array is
+// bytes [32 i, 32 i + 32) of the Q8_0 plane and [16 i, 16 i + 16) of the Q4_0 plane.
+// Like the weight quantisers, these kernels let no dependent start early.
+template <int WORDS>
+__device__ __forceinline__ void load_block_words(const uint16_t* blk, uint32_t* w) {
+#pragma unroll
+  for (int j = 0; j < WORDS / 2; ++j)
+    w[j] = (uint32_t)blk[1 + 2 * j] | ((uint32_t)blk[2 + 2 * j] << 16);
+}
+
+__global__ void __launch_bounds__(kQuantThreads)
+    repack_q8_0_kernel(const uint16_t* __restrict__ blocks, int64_t nblk,
+                       int8_t* __restrict__ q, uint16_t* __restrict__ d) {
+  pdl_wait();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblk; i += stride) {
+    const uint16_t* blk = blocks + i * 17;
+    uint32_t w[8];
+    load_block_words<16>(blk, w);
+    uint4* dst = reinterpret_cast<uint4*>(q + i * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    d[i] = blk[0];
+  }
+}
+
+__global__ void __launch_bounds__(kQuantThreads)
+    repack_q4_0_kernel(const uint16_t* __restrict__ blocks, int64_t nblk,
+                       uint8_t* __restrict__ q4, uint16_t* __restrict__ d) {
+  pdl_wait();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblk; i += stride) {
+    const uint16_t* blk = blocks + i * 9;
+    uint32_t w[4];
+    load_block_words<8>(blk, w);
+    *reinterpret_cast<uint4*>(q4 + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    d[i] = blk[0];
+  }
+}
+
 int quant_grid(int64_t groups, const DeviceInfo& info) {
   const int64_t warps = (groups + 31) / 32;
   const int64_t blocks = (warps * 32 + kQuantThreads - 1) / kQuantThreads;
@@ -232,6 +275,47 @@ extern "C" memra_status memra_quantize_q4_0(const float* w, int64_t N, int64_t K
   const int64_t groups = N * K / 8;
   cudaError_t e = launch_kernel(quantize_q4_0_kernel, dim3(quant_grid(groups, info)),
                                 dim3(kQuantThreads), 0, stream, w, groups, wq4, wd);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MEMRA_OK;
+}
+
+// Shared argument checks of the two repacks; *nblk receives N * K / 32.
+static memra_status repack_args(const void* blocks, int64_t N, int64_t K, const void* q,
+                                const void* d, int64_t block_bytes, int64_t* nblk) {
+  *nblk = 0;
+  if (N < 0 || K < 0 || K % 32 != 0) return MEMRA_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return MEMRA_OK;
+  if (!blocks || !q || !d) return MEMRA_ERR_INVALID_ARG;
+  if (N > INT64_MAX / block_bytes / (K / 32)) return MEMRA_ERR_UNSUPPORTED;
+  if (!aligned(blocks, 2) || !aligned(q, 16) || !aligned(d, 2)) return MEMRA_ERR_ALIGNMENT;
+  *nblk = N * (K / 32);
+  return MEMRA_OK;
+}
+
+extern "C" memra_status memra_repack_q8_0(const void* blocks, int64_t N, int64_t K, int8_t* wq,
+                                          uint16_t* wd, cudaStream_t stream) {
+  int64_t nblk;
+  memra_status st = repack_args(blocks, N, K, wq, wd, 34, &nblk);
+  if (st != MEMRA_OK || nblk == 0) return st;
+  DeviceInfo info;
+  if (!device_info(&info)) return MEMRA_ERR_CUDA;
+  cudaError_t e = launch_kernel(repack_q8_0_kernel, dim3(quant_grid(nblk, info)),
+                                dim3(kQuantThreads), 0, stream,
+                                static_cast<const uint16_t*>(blocks), nblk, wq, wd);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MEMRA_OK;
+}
+
+extern "C" memra_status memra_repack_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* wq4,
+                                          uint16_t* wd, cudaStream_t stream) {
+  int64_t nblk;
+  memra_status st = repack_args(blocks, N, K, wq4, wd, 18, &nblk);
+  if (st != MEMRA_OK || nblk == 0) return st;
+  DeviceInfo info;
+  if (!device_info(&info)) return MEMRA_ERR_CUDA;
+  cudaError_t e = launch_kernel(repack_q4_0_kernel, dim3(quant_grid(nblk, info)),
+                                dim3(kQuantThreads), 0, stream,
+                                static_cast<const uint16_t*>(blocks), nblk, wq4, wd);
   if (e != cudaSuccess) return cuda_fail(e);
   return MEMRA_OK;
 }

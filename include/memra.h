@@ -2,8 +2,8 @@
  * memra.h -- C ABI of the GB300 (sm_103a) Q8_0 decode library.
  *
  * The single-user decode step of an LLM streams block-quantised weights through
- * a fused dequantise matrix-vector (M = 1) or skinny matrix (M <= 8, speculative
- * verify) product, plus a routed-expert (MoE) variant.  The memra pages name this
+ * a fused dequantise matrix-vector (M = 1) or skinny matrix (M <= 16: speculative
+ * verify, batched decode) product, plus a routed-expert (MoE) variant.  The memra pages name this
  * path: Q8_0 decode through split-plane repacked matvecs with warp-level dp4a and
  * per-shape dispatch (memra wiki, github.com/avifenesh/memra/wiki, feature list);
  * one batched K+1 verify for MTP speculative decoding (same list); routed MoE
@@ -62,16 +62,18 @@ typedef enum memra_status {
   MEMRA_OK = 0,
   MEMRA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, K % 32 != 0, bad enum */
   MEMRA_ERR_ALIGNMENT = 2,     /* a pointer violates the alignment above */
-  MEMRA_ERR_UNSUPPORTED = 3,   /* a size beyond the documented limits (M > 8, ...) */
+  MEMRA_ERR_UNSUPPORTED = 3,   /* a size beyond the documented limits (M > 16, ...) */
   MEMRA_ERR_CUDA = 4           /* the CUDA runtime reported an error */
 } memra_status;
 
 typedef enum memra_dtype { MEMRA_BF16 = 0, MEMRA_F32 = 1 } memra_dtype;
 
 /* Limits. */
-#define MEMRA_MAX_M 8            /* activation rows per small-M call */
+#define MEMRA_MAX_M 16           /* activation rows per small-M call */
 #define MEMRA_MAX_TOP_K 64       /* experts per routed call */
-#define MEMRA_MAX_X_BYTES 196608 /* M*K*(1 + 4/32) bytes of q8_1 activation per call */
+/* Bytes of q8_1 activation a pass over the weights holds on chip: P*K*(1 + 4/32)
+ * with P the rows of one pass (M up to 8, else ceil(M/2)). */
+#define MEMRA_MAX_X_BYTES 196608
 
 /*
  * Weight ingest: fp32 W [N][K] -> Q8_0 planes wq [N][K], wd [N][K/32].
@@ -101,10 +103,13 @@ memra_status memra_q8_0_gemv(const int8_t* wq, const uint16_t* wd, int64_t N, in
                              const int8_t* xq, const float* xd, float* y, cudaStream_t stream);
 
 /*
- * Speculative / MTP verify skinny GEMM: M in [0, 8] activation rows share one
- * pass over the weights (memra wiki, feature list: one batched K+1 verify).
+ * Speculative / MTP verify skinny GEMM and batched decode: M in [0, 16] activation
+ * rows (memra wiki, feature list: one batched K+1 verify; memra performance,
+ * "Serving performance": batched decode in 16-wide chunks on a kernel class whose
+ * 16-batch results are bit-exact).  Up to 8 rows share one pass over the weights;
+ * 9..16 rows take two passes, of ceil(M/2) and floor(M/2) rows.
  * xq [M][K], xd [M][K/32], y fp32 [M][N].  Row m of y equals, bit for bit, the
- * memra_q8_0_gemv result for activation row m.
+ * memra_q8_0_gemv result for activation row m, whatever M.
  */
 memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t* wd, int64_t N, int64_t K,
                                      int64_t M, const int8_t* xq, const float* xd, float* y,
@@ -112,8 +117,8 @@ memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t* wd, int64
 
 /*
  * Q4_0 weights, the pages' other split-plane decode format (memra wiki, feature
- * list: "NVFP4 / Q4_0 / Q8_0 decode -- split-plane repacked matvecs").  The pages
- * print nothing of it; this library's reading is GGUF's Q4_0 block: 32 consecutive
+ * list, which names NVFP4, Q4_0 and Q8_0 decode through split-plane matvecs).  The
+ * pages print nothing of it; this library's reading is GGUF's Q4_0 block: 32 consecutive
  * weights of a row share one fp16 scale d and carry 4-bit codes c in [0, 15] with
  * w ~= d * (c - 8).
  *   Planes: wq4 uint8 [N][K/2] and wd fp16 [N][K/32].  Byte j < 16 of a block holds
@@ -126,10 +131,31 @@ memra_status memra_quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* 
                                  cudaStream_t stream);
 
 /*
+ * Repack from GGUF's interleaved block arrays into the split planes (memra wiki,
+ * feature list: decode runs on split-plane repacked weights).  The pages print no
+ * block layout; the reading is GGUF's:
+ *   Q8_0 block, 34 bytes: fp16 scale (little-endian), then 32 int8 quants;
+ *   Q4_0 block, 18 bytes: fp16 scale (little-endian), then 16 bytes, byte j holding
+ *   element j's code in its low nibble and element j+16's in its high nibble (the
+ *   same byte layout as this library's Q4_0 plane).
+ * blocks: N * K/32 blocks, row after row (device memory, 2-byte aligned).  Outputs:
+ * wq int8 [N][K] or wq4 uint8 [N][K/2] (16-byte aligned) and wd fp16 bits [N][K/32]
+ * (2-byte aligned), all allocated by the caller.  Byte for byte: no value changes.
+ * Errors: K % 32 != 0 or a null pointer -> MEMRA_ERR_INVALID_ARG; misaligned
+ * pointers -> MEMRA_ERR_ALIGNMENT; N * K/32 * block bytes beyond int64 ->
+ * MEMRA_ERR_UNSUPPORTED.  N == 0 or K == 0 launches nothing.
+ */
+memra_status memra_repack_q8_0(const void* blocks, int64_t N, int64_t K, int8_t* wq,
+                               uint16_t* wd, cudaStream_t stream);
+memra_status memra_repack_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* wq4,
+                               uint16_t* wd, cudaStream_t stream);
+
+/*
  * Q4_0 x q8_1 products: y[m][n] = sum_b (d_w[n][b] * d_x[m][b]) * s_b with the exact
  * int32 block sum s_b = sum_i (c_i - 8) * xq_i, in the same fp32 summation order as
  * the Q8_0 products (so the result equals the Q8_0 product of the unpacked codes,
- * bit for bit).  M in [0, 8]; xq [M][K], xd [M][K/32], y fp32 [M][N].
+ * bit for bit).  M in [0, 16], in passes as for memra_q8_0_gemm_small_m; xq [M][K],
+ * xd [M][K/32], y fp32 [M][N].
  * K must be a multiple of 256 (MEMRA_ERR_UNSUPPORTED otherwise); wq4, wd, xq and xd
  * 16-byte aligned.
  */

@@ -155,9 +155,9 @@ void oracle_quantize_q8_0(const float* w, int64_t N, int64_t K, int8_t* q, uint1
 
 // ---------------------------------------------------------------------------
 // Weight ingest to Q4_0 (the pages' other split-plane decode format; memra wiki,
-// feature list: "NVFP4 / Q4_0 / Q8_0 decode -- split-plane repacked matvecs").  The
-// pages name the format and print nothing of it; the reading here is GGUF's Q4_0
-// block restated: 32 consecutive weights of a row share one fp16 scale d and carry
+// feature list, which names NVFP4, Q4_0 and Q8_0 decode through split-plane
+// matvecs).  The pages name the format and print nothing of it; the reading here is
+// GGUF's Q4_0 block restated: 32 consecutive weights of a row share one fp16 scale d and carry
 // unsigned 4-bit codes q in [0, 15] with w ~= d * (q - 8).
 //   m  = the block element of largest magnitude (the first one on a tie);
 //   d  = fp16_rne(m / -8), so that m itself maps to q - 8 = -8 (d = +0 when the

@@ -55,7 +55,7 @@ def test_gemv_argument_errors(L):
     f = L.memra_q8_0_gemm_small_m
     assert f(A256, A256, 64, 48, 1, A256, A256, A256, None) == 1      # K % 32 != 0
     assert f(A256, A256, -1, 64, 1, A256, A256, A256, None) == 1      # negative N
-    assert f(A256, A256, 64, 64, 9, A256, A256, A256, None) == 3      # M > 8
+    assert f(A256, A256, 64, 64, 17, A256, A256, A256, None) == 3     # M > 16
     assert f(None, A256, 64, 64, 1, A256, A256, A256, None) == 1      # null weights
     assert f(A256 + 16, A256, 64, 64, 1, A256, A256, A256, None) == 2  # wq not 32-aligned
     assert f(A256, A256 + 1, 64, 64, 1, A256, A256, A256, None) == 2   # wd not 2-aligned
@@ -70,7 +70,7 @@ def test_fused_argument_errors(L):
     f = L.memra_q8_0_quant_gemm
     assert f(A256, A256, 64, 48, 1, A256, 0, A256, None) == 1       # K % 32
     assert f(A256, A256, 64, 64, 1, A256, 5, A256, None) == 1       # dtype
-    assert f(A256, A256, 64, 64, 9, A256, 0, A256, None) == 3       # M > 8
+    assert f(A256, A256, 64, 64, 17, A256, 0, A256, None) == 3      # M > 16
     assert f(A256, A256, 64, 64, 1, A256 + 8, 0, A256, None) == 2   # x not 16-aligned
     assert f(A256 + 16, A256, 64, 64, 1, A256, 0, A256, None) == 2  # wq not 32-aligned
     assert f(None, None, 0, 64, 1, None, 0, None, None) == 0
@@ -90,7 +90,7 @@ def test_quantizer_argument_errors(L):
 def test_q4_0_argument_errors(L):
     f = L.memra_q4_0_gemm_small_m
     assert f(A256, A256, 64, 48, 1, A256, A256, A256, None) == 1      # K % 32 != 0
-    assert f(A256, A256, 64, 256, 9, A256, A256, A256, None) == 3     # M > 8
+    assert f(A256, A256, 64, 256, 17, A256, A256, A256, None) == 3    # M > 16
     assert f(A256, A256, 64, 96, 1, A256, A256, A256, None) == 3      # K % 256 != 0
     assert f(A256 + 8, A256, 64, 256, 1, A256, A256, A256, None) == 2  # wq4 not 16-aligned
     assert f(A256, A256 + 2, 64, 256, 1, A256, A256, A256, None) == 2  # wd not 16-aligned
@@ -101,6 +101,20 @@ def test_q4_0_argument_errors(L):
     assert L.memra_quantize_q4_0(A256, 4, 48, A256, A256, None) == 1
     assert L.memra_quantize_q4_0(A256, 4, 64, A256 + 8, A256, None) == 2
     assert L.memra_quantize_q4_0(None, 0, 64, None, None, None) == 0
+
+
+def test_repack_argument_errors(L):
+    for f, _ in ((L.memra_repack_q8_0, 34), (L.memra_repack_q4_0, 18)):
+        assert f(A256, 4, 48, A256, A256, None) == 1           # K % 32 != 0
+        assert f(A256, -1, 64, A256, A256, None) == 1          # N < 0
+        assert f(None, 4, 64, A256, A256, None) == 1           # null blocks
+        assert f(A256, 4, 64, None, A256, None) == 1           # null quants
+        assert f(A256 + 1, 4, 64, A256, A256, None) == 2       # blocks not 2-aligned
+        assert f(A256, 4, 64, A256 + 8, A256, None) == 2       # quants not 16-aligned
+        assert f(A256, 4, 64, A256, A256 + 1, None) == 2       # scales not 2-aligned
+        assert f(A256, 1 << 62, 64, A256, A256, None) == 3     # bytes beyond int64
+        assert f(None, 0, 64, None, None, None) == 0           # empty: no work
+        assert f(None, 4, 0, None, None, None) == 0
 
 
 def test_moe_argument_errors(L):

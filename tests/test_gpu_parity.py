@@ -138,6 +138,37 @@ def test_rows_do_not_depend_on_m(mem, orc):
         assert torch.equal(yM.view(torch.int32), y8[:M].view(torch.int32)), M
 
 
+@pytest.mark.parametrize("N,K", [(1003, 1184), (257, 17408), (4096, 4096), (130, 768)])
+@pytest.mark.parametrize("M", [9, 12, 16])
+def test_batched_decode_parity(mem, orc, N, K, M):
+    """M = 9..16 rows (two passes over the weights): against the oracle, and every row
+    bit for bit the M = 1 product of that row."""
+    (wq, wd, xq, xd), (oq, od, oxq, oxd) = run_pair(mem, orc, N, K, M, seed=N * 17 + K + M)
+    y = Guarded((M, N), torch.float32)
+    mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd, y=y.view)
+    torch.cuda.synchronize()
+    assert y.intact()
+    assert_within(np_(y.view), orc.gemm(oq, od, oxq, oxd),
+                  abs_terms(orc.block_dots(oq, oxq), od, oxd), "batch N=%d K=%d M=%d" % (N, K, M))
+    for m in range(M):
+        y1 = mem.memra_q8_0_gemv(wq, wd, xq[m], xd[m])
+        assert torch.equal(y1.view(torch.int32), y.view[m].view(torch.int32)), m
+
+
+def test_batched_decode_limits(mem):
+    K = 17408
+    wq = torch.zeros((64, K), dtype=torch.int8, device="cuda")
+    wd = torch.zeros((64, K // 32), dtype=torch.float16, device="cuda")
+    xq = torch.zeros((17, K), dtype=torch.int8, device="cuda")
+    xd = torch.zeros((17, K // 32), dtype=torch.float32, device="cuda")
+    with pytest.raises(mem.MemraError) as e:
+        mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd)        # M = 17
+    assert e.value.status == 3
+    y = mem.memra_q8_0_gemm_small_m(wq, wd, xq[:16], xd[:16])  # two passes of 8 rows
+    torch.cuda.synchronize()
+    assert not y.any()
+
+
 def test_deterministic_repeat(mem, orc):
     (wq, wd, xq, xd), _ = run_pair(mem, orc, 2048, 5120, 4, seed=3)
     a = mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd)
@@ -351,9 +382,9 @@ def test_misaligned_views_are_rejected(mem):
     assert torch.all(y == 3.0)                          # nothing launched
     with pytest.raises(mem.MemraError) as ei:
         mem.memra_q8_0_gemm_small_m(torch.zeros((N, K), dtype=torch.int8, device=dev), wd,
-                                    torch.zeros((9, K), dtype=torch.int8, device=dev),
-                                    torch.zeros((9, K // 32), dtype=torch.float32, device=dev))
-    assert ei.value.status == 3
+                                    torch.zeros((17, K), dtype=torch.int8, device=dev),
+                                    torch.zeros((17, K // 32), dtype=torch.float32, device=dev))
+    assert ei.value.status == 3                         # M > 16
 
 
 # ----------------------------------------------------------------------------
@@ -362,7 +393,7 @@ def test_misaligned_views_are_rejected(mem):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("N,K,M", [(1003, 1184, 1), (4096, 4096, 1), (257, 17408, 1),
-                                   (513, 5120, 3), (130, 768, 8), (64, 32, 2)])
+                                   (513, 5120, 3), (130, 768, 8), (64, 32, 2), (300, 5120, 13)])
 def test_fused_quant_gemm_matches_two_step(mem, orc, dtype, N, K, M):
     w = synth.weights_fp32(N, K, 80, N, K)
     x = synth.activations_fp32(M, K, 81, N, K, M, outlier_frac=0.001).to(dtype).cuda()

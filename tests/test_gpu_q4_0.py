@@ -67,7 +67,8 @@ def test_quantize_q4_0_special_blocks(mem, orc):
 
 @pytest.mark.parametrize("N,K,M", [(1003, 4096, 1), (777, 5120, 1), (300, 5120, 8),
                                    (64, 17408, 1), (130, 17408, 8), (12289, 4096, 2),
-                                   (5120, 17408, 1), (513, 2048, 4), (1, 256, 3)])
+                                   (5120, 17408, 1), (513, 2048, 4), (1, 256, 3), (700, 5120, 16),
+                                   (129, 17408, 11)])
 def test_q4_0_gemm_parity(mem, orc, N, K, M):
     seed = N * 31 + K + M
     w = synth.weights_fp32(N, K, seed, 502)
