@@ -59,6 +59,12 @@ _SIGS = {
     "memra_q8_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
     "memra_q8_0_quant_gemm": [_p, _p, _i64, _i64, _i64, _p, _i32, _p, _p],
     "memra_q8_0_moe_gemv": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p, _p],
+    "memra_q8_0_moe_gemv_tokens": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _i64, _p, _p, _i32,
+                                   _p, _p, _p, _p],
+    "memra_q4_0_moe_gemv_tokens": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _i64, _p, _p, _i32,
+                                   _p, _p, _p, _p],
+    "memra_q8_0_moe_ffn_tokens": [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _i64, _p, _i32,
+                                  _p, _p, _p, _p],
     "memra_swiglu_quantize_q8_1": [_p, _i64, _i64, _p, _p, _p],
     "memra_q8_0_moe_ffn": [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _i32, _p, _p, _p,
                            _p],
@@ -374,6 +380,95 @@ def memra_q4_0_moe_gemv(wq4_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert, y=
     wd_bank float16 [E, N, K/32]."""
     return _moe_gemv("memra_q4_0_moe_gemv", wq4_bank, torch.uint8, 2, wd_bank, ids, gate_w, xq,
                      xd, x_per_expert, y, dev_status)
+
+
+def _moe_gemv_tokens(fn, wq_bank, qdtype, kmul, wd_bank, ids, gate_w, xq, xd, x_per_expert,
+                     y, workspace, dev_status):
+    _need(wq_bank, "wq_bank", qdtype)
+    E, N, Kq = wq_bank.shape
+    K = Kq * kmul
+    dev = wq_bank.device
+    _need(wd_bank, "wd_bank", torch.float16, dev, (E, N, K // 32))
+    _need(ids, "ids", torch.int32, dev)
+    T, top_k = ids.shape
+    if gate_w is not None:
+        _need(gate_w, "gate_w", torch.float32, dev, (T, top_k))
+    xpe = 1 if x_per_expert else 0
+    rows = (T, top_k) if xpe else (T,)
+    _need(xq, "xq", torch.int8, dev, rows + (K,))
+    _need(xd, "xd", torch.float32, dev, rows + (K // 32,))
+    yshape = (T, N) if gate_w is not None else (T, top_k, N)
+    if y is None:
+        y = torch.empty(yshape, dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, yshape)
+    if gate_w is not None:
+        if workspace is None:
+            workspace = torch.empty((T, top_k, N), dtype=torch.float32, device=dev)
+        _need(workspace, "workspace", torch.float32, dev, (T, top_k, N))
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    with torch.cuda.device(dev):
+        _check(fn, getattr(lib(), fn)(_ptr(wq_bank), _ptr(wd_bank), E, N, K, _ptr(ids),
+                                      _ptr(gate_w), T, top_k, _ptr(xq), _ptr(xd), xpe, _ptr(y),
+                                      _ptr(workspace), _ptr(dev_status), _stream(wq_bank)))
+    return y
+
+
+def memra_q8_0_moe_gemv_tokens(wq_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert, y=None,
+                               workspace=None, dev_status=None):
+    """Routed experts for a batch of tokens.  ids int32 [T, top_k], gate_w float32
+    [T, top_k] or None.  x_per_expert=False: xq [T, K], xd [T, K/32]; True: xq
+    [T, top_k, K], xd [T, top_k, K/32].  Returns y [T, top_k, N] without gate weights,
+    [T, N] with them (`workspace` float32 [T, top_k, N] then holds the per-pair rows)."""
+    return _moe_gemv_tokens("memra_q8_0_moe_gemv_tokens", wq_bank, torch.int8, 1, wd_bank, ids,
+                            gate_w, xq, xd, x_per_expert, y, workspace, dev_status)
+
+
+def memra_q4_0_moe_gemv_tokens(wq4_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert, y=None,
+                               workspace=None, dev_status=None):
+    """memra_q8_0_moe_gemv_tokens on a Q4_0 bank (wq4_bank uint8 [E, N, K/2])."""
+    return _moe_gemv_tokens("memra_q4_0_moe_gemv_tokens", wq4_bank, torch.uint8, 2, wd_bank,
+                            ids, gate_w, xq, xd, x_per_expert, y, workspace, dev_status)
+
+
+def memra_q8_0_moe_ffn_tokens(gu_q, gu_d, dn_q, dn_d, ids, gate_w, x, y=None, workspace=None,
+                              dev_status=None):
+    """memra_q8_0_moe_ffn for a batch: ids int32 [T, top_k], gate_w float32 [T, top_k],
+    x [T, H] (bf16 or fp32).  Returns y float32 [T, H].  `workspace` float32
+    [T * top_k * (2F + H)] holds the pairs' gate|up rows, then their down rows."""
+    _need(gu_q, "gu_q", torch.int8)
+    E, F2, H = gu_q.shape
+    F = F2 // 2
+    dev = gu_q.device
+    _need(gu_d, "gu_d", torch.float16, dev, (E, F2, H // 32))
+    _need(dn_q, "dn_q", torch.int8, dev, (E, H, F))
+    _need(dn_d, "dn_d", torch.float16, dev, (E, H, F // 32))
+    _need(ids, "ids", torch.int32, dev)
+    T, top_k = ids.shape
+    _need(gate_w, "gate_w", torch.float32, dev, (T, top_k))
+    if x.dtype == torch.bfloat16:
+        dt = MEMRA_BF16
+    elif x.dtype == torch.float32:
+        dt = MEMRA_F32
+    else:
+        raise TypeError("x must be bfloat16 or float32")
+    _need(x, "x", x.dtype, dev, (T, H))
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, (T, H))
+    ws = T * top_k * (F2 + H)
+    if workspace is None:
+        workspace = torch.empty((ws,), dtype=torch.float32, device=dev)
+    _need(workspace, "workspace", torch.float32, dev, (ws,))
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    with torch.cuda.device(dev):
+        _check("memra_q8_0_moe_ffn_tokens",
+               lib().memra_q8_0_moe_ffn_tokens(_ptr(gu_q), _ptr(gu_d), _ptr(dn_q), _ptr(dn_d), E,
+                                               H, F, _ptr(ids), _ptr(gate_w), T, top_k, _ptr(x),
+                                               dt, _ptr(y), _ptr(workspace), _ptr(dev_status),
+                                               _stream(gu_q)))
+    return y
 
 
 def memra_q8_0_moe_ffn(gu_q, gu_d, dn_q, dn_d, ids, gate_w, x, y=None, workspace=None,

@@ -76,7 +76,9 @@
 namespace memra {
 namespace {
 
-constexpr int kMaxTopK = MEMRA_MAX_TOP_K;
+// Routed slots one launch holds in shared memory: a batch's tokens x top_k.
+constexpr int kMaxTopK = MEMRA_MAX_PAIRS;
+static_assert(MEMRA_MAX_TOP_K <= MEMRA_MAX_PAIRS, "a single token's slots fit");
 
 enum Mode { kDense = 0, kMoeUngated = 1, kMoeGated = 2 };
 
@@ -114,7 +116,14 @@ struct Params {
   const float* gate_w;
   int top_k;
   int64_t E;
-  int xpe;                 // one activation row per expert
+  int xpe;                 // one activation row per expert (per routed slot)
+  // Routed slots that share one activation row (xpe): slot k reads row k / xdiv.  A
+  // batch of tokens routes top_k slots each and shares each token's row among them.
+  int xdiv;
+  // Slots of a batched routed product (> 0): the grid gives every slot the same
+  // number of CTAs at the same row offsets, so that slots routed to the same expert
+  // stream its rows at the same time and the repeats are served from L2.
+  int lockstep;
   int32_t* status;
   // The routing was already waited for by the preceding kernel of the same call, and
   // that kernel let this one launch only after its own wait: read it at once.
@@ -132,6 +141,14 @@ struct Params {
   // register kernel layout
   int tile_rows;
 };
+
+// Unquantised activation row `row` (K values; SwiGLU input rows hold gate|up, 2K).
+template <int XIN>
+__device__ __forceinline__ const void* xin_row(const void* xin, int64_t row, int64_t K) {
+  if (XIN == kXbf16) return static_cast<const uint16_t*>(xin) + row * K;
+  if (XIN == kXf32) return static_cast<const float*>(xin) + row * K;
+  return static_cast<const float*>(xin) + row * 2 * K;
+}
 
 struct Seg {
   int64_t row0;   // first weight row (absolute row index into the plane)
@@ -177,7 +194,7 @@ __device__ __forceinline__ Seg get_seg(const Params& p, int64_t u0, int64_t u1, 
     g.valid = e >= 0;
     g.row0 = (int64_t)(e < 0 ? 0 : e) * p.N + lo;
     g.nrows = (int)(hi - lo);
-    g.xrow = p.xpe ? (int)k : 0;
+    g.xrow = p.xpe ? (int)(p.xdiv > 1 ? k / p.xdiv : k) : 0;
     g.out0 = k * p.N + lo;
   }
   return g;
@@ -258,6 +275,14 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
   const int ns = p.ns;
   const int64_t u0 = p.units * blockIdx.x / gridDim.x;
   const int64_t u1 = p.units * (blockIdx.x + 1) / gridDim.x;
+  // Activation rows this CTA stages: [xlo, xlo + nxr).  An ungated routed product
+  // with an activation row per slot group stages only the rows of its own segments.
+  int xlo = 0, nxr = p.xrows;
+  if (MODE == kMoeUngated && p.xpe) {
+    const int64_t d = p.xdiv > 1 ? p.xdiv : 1;
+    xlo = (int)((u0 / p.N) / d);
+    nxr = (int)(((u1 - 1) / p.N) / d) - xlo + 1;
+  }
   auto full_bar = [&](int i) { return smem_addr(bars + i); };
   auto empty_bar = [&](int i) { return smem_addr(bars + kMaxStages + i); };
 
@@ -319,7 +344,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         m.seg = cur_si;
         m.r0 = cur_r0;
         m.nr = min(p.rps, g.nrows - cur_r0);
-        m.xrow = g.xrow;
+        m.xrow = g.xrow - xlo;
         cur_r0 += p.rps;
         return true;
       }
@@ -493,17 +518,18 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
     // and land only after all of them.
     pdl_wait();
     if (XIN == kXq8) {
-      copy_x_to_smem<4>(p.xq, p.xd, p.xrows * Ki, p.xrows * nb * 4, xs, xds, threadIdx.x - 32,
-                        kConsumerWarps * 32);
+      copy_x_to_smem<4>(p.xq + (size_t)xlo * Ki, p.xd + (size_t)xlo * nb, nxr * Ki, nxr * nb * 4,
+                        xs, xds, threadIdx.x - 32, kConsumerWarps * 32);
     } else {
-      quantize_rows_to_smem<XIN>(p.xin, p.xrows, (int)p.K, xs, xds, cw, kConsumerWarps, lane);
+      quantize_rows_to_smem<XIN>(xin_row<XIN>(p.xin, xlo, p.K), nxr, (int)p.K, xs, xds, cw,
+                                 kConsumerWarps, lane);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     // Q4_0: s_b = sum_i (c_i - 8) x_i = (sum_i c_i x_i) - 8 sum_i x_i, with the
     // activation's per-block sums taken once here.
     int32_t* xsum = reinterpret_cast<int32_t*>(smem + p.off_xsum);
     if (FMT == kQ4) {
-      for (int i = threadIdx.x - 32; i < p.xrows * nb; i += kConsumerWarps * 32) {
+      for (int i = threadIdx.x - 32; i < nxr * nb; i += kConsumerWarps * 32) {
         const uint4 a = *reinterpret_cast<const uint4*>(xs + (size_t)i * 32);
         const uint4 b = *reinterpret_cast<const uint4*>(xs + (size_t)i * 32 + 16);
         const int ones = 0x01010101;
@@ -897,6 +923,32 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Gated sum of a batch's routed slots: y[t][n] = sum over the valid slots k of token
+// t, in ascending k, of gate[t][k] * yp[t][k][n], from 0 with one rounding per
+// multiply and per add.  That is the gated routed product's own order, so token t's
+// row equals, bit for bit, the gated product of that token alone.
+__global__ void __launch_bounds__(256)
+    moe_combine_kernel(const float* __restrict__ yp, const int32_t* __restrict__ ids,
+                       const float* __restrict__ gate_w, int64_t T, int top_k, int64_t N,
+                       int64_t E, float* __restrict__ y) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t total = T * N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / N;
+    const int64_t n = i - t * N;
+    float acc = 0.0f;
+    for (int k = 0; k < top_k; ++k) {
+      const int64_t slot = t * top_k + k;
+      const int32_t e = __ldcg(ids + slot);
+      if (e < 0 || e >= E) continue;
+      acc = __fadd_rn(acc, __fmul_rn(__ldcg(gate_w + slot), yp[slot * N + n]));
+    }
+    y[i] = acc;
+  }
+}
+
 // ----------------------------------------------------------------------------
 // Host dispatch.
 // ----------------------------------------------------------------------------
@@ -995,9 +1047,14 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
     rps = (int)(p.top_k * maxu);
   }
   size_t stage = align_up((size_t)rps * p.qrow, 128) + align_up((size_t)rps * p.nb * 2, 128);
-  const size_t xsum_bytes = FMT == kQ4 ? align_up((size_t)p.xrows * p.nb * 4, 128) : 0;
-  const size_t xbytes = align_up((size_t)p.xrows * p.K, 128) +
-                        align_up((size_t)p.xrows * p.nb * 4, 128) + xsum_bytes;
+  // Activation rows a CTA stages: an ungated routed product with a row per slot group
+  // needs only those of the slots its unit range touches (at most ceil(maxu/N) + 1).
+  const int64_t xr = MODE == kMoeUngated && p.xpe
+                         ? std::min<int64_t>(p.xrows, (maxu + p.N - 1) / p.N + 1)
+                         : p.xrows;
+  const size_t xsum_bytes = FMT == kQ4 ? align_up((size_t)xr * p.nb * 4, 128) : 0;
+  const size_t xbytes = align_up((size_t)xr * p.K, 128) + align_up((size_t)xr * p.nb * 4, 128) +
+                        xsum_bytes;
   const size_t yacc = MODE == kMoeGated ? align_up((size_t)maxu * 4, 16) : 0;
   const size_t fixed = kHeaderBytes + xbytes + yacc + align_up((size_t)(p.S + 1) * 4, 16);
   size_t part_per_stage = align_up((size_t)rps * p.S * M * 4, 16);
@@ -1030,8 +1087,8 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   p.wd_off = (uint32_t)align_up((size_t)rps * p.qrow, 128);
   size_t off = kHeaderBytes;
   p.off_x = (uint32_t)off;
-  p.off_xd = (uint32_t)(off + align_up((size_t)p.xrows * p.K, 128));
-  p.off_xsum = (uint32_t)(p.off_xd + align_up((size_t)p.xrows * p.nb * 4, 128));
+  p.off_xd = (uint32_t)(off + align_up((size_t)xr * p.K, 128));
+  p.off_xsum = (uint32_t)(p.off_xd + align_up((size_t)xr * p.nb * 4, 128));
   off += xbytes;
   p.off_ring = (uint32_t)off;
   off += (size_t)ns * stage;
@@ -1094,12 +1151,18 @@ memra_status run_product(Params p, cudaStream_t stream) {
   p.nb = (int)(p.K / 32);
   p.cpr = (p.nb + 31) / 32;
   p.S = slices_for(p.cpr);
-  int64_t grid = std::min<int64_t>(p.units, (int64_t)info.sms * (M > 1 ? 1 : tma_tuning().ctas_per_sm));
+  // A single wave of `slots` CTAs; a batched routed product takes a multiple of its
+  // slot count, so that every slot's rows split at the same offsets.
+  auto wave = [&](int64_t slots) {
+    if (p.lockstep > 0 && p.lockstep <= slots) slots = slots / p.lockstep * p.lockstep;
+    return std::min<int64_t>(p.units, slots);
+  };
+  int64_t grid = wave((int64_t)info.sms * (M > 1 ? 1 : tma_tuning().ctas_per_sm));
   size_t smem = 0;
   if (plan_tma<M, R, MODE, XIN, FMT>(p, info, grid, &smem)) {
     if (grid > info.sms && smem > tma_tuning().smem_pair_limit) {
       // Only one such CTA fits per SM: one per SM, so the grid stays a single wave.
-      grid = std::min<int64_t>(p.units, info.sms);
+      grid = wave(info.sms);
       if (!plan_tma<M, R, MODE, XIN, FMT>(p, info, grid, &smem)) return MEMRA_ERR_UNSUPPORTED;
     }
     return launch(q8_tma_kernel<M, R, MODE, XIN, FMT>, grid, tma_threads(M), smem, stream, info,
@@ -1336,6 +1399,71 @@ memra_status moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank, int64_t E,
   p.units = top_k * N;
   return run_product<1, 1, kMoeUngated, kXq8, FMT>(p, stream);
 }
+
+memra_status launch_combine(const float* yp, const int32_t* ids, const float* gate_w, int64_t T,
+                            int64_t top_k, int64_t N, int64_t E, float* y, cudaStream_t stream) {
+  DeviceInfo info;
+  if (!device_info(&info)) return MEMRA_ERR_CUDA;
+  const int64_t blocks = std::min<int64_t>((T * N + 255) / 256, (int64_t)info.sms * 8);
+  const cudaError_t e = launch_kernel(moe_combine_kernel, dim3((unsigned)blocks), dim3(256), 0,
+                                      stream, yp, ids, gate_w, T, (int)top_k, N, E, y);
+  return e == cudaSuccess ? MEMRA_OK : cuda_fail(e);
+}
+
+// Routed experts for a batch of T tokens, top_k slots each: every (token, slot) pair is
+// one segment of the ungated routed product (the single-token arithmetic), and the
+// grid gives every pair the same row split (lockstep), so that pairs routed to the
+// same expert read its rows from HBM once and from L2 after.
+template <int FMT>
+memra_status moe_gemv_tokens(const int8_t* wq_bank, const uint16_t* wd_bank, int64_t E,
+                             int64_t N, int64_t K, const int32_t* ids, const float* gate_w,
+                             int64_t T, int64_t top_k, const int8_t* xq, const float* xd,
+                             int32_t x_per_expert, float* y, float* workspace,
+                             int32_t* dev_status, cudaStream_t stream) {
+  if (E < 1 || N < 0 || K < 0 || K % 32 != 0 || top_k < 1 || T < 0) return MEMRA_ERR_INVALID_ARG;
+  if (x_per_expert != 0 && x_per_expert != 1) return MEMRA_ERR_INVALID_ARG;
+  if (top_k > MEMRA_MAX_TOP_K || T > MEMRA_MAX_PAIRS || T * top_k > MEMRA_MAX_PAIRS)
+    return MEMRA_ERR_UNSUPPORTED;
+  if (N > INT32_MAX || K > INT32_MAX || E > INT32_MAX) return MEMRA_ERR_UNSUPPORTED;
+  if (N == 0 || T == 0) return MEMRA_OK;
+  if (!y || !ids || (gate_w && !workspace)) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(y, 4) || !aligned(ids, 4) || (gate_w && !aligned(gate_w, 4)) ||
+      (gate_w && !aligned(workspace, 4)) || (dev_status && !aligned(dev_status, 4)))
+    return MEMRA_ERR_ALIGNMENT;
+  const int64_t P = T * top_k;
+  if (K == 0) return zero_fill(y, gate_w ? T * N : P * N, stream);
+  if (!wq_bank || !wd_bank || !xq || !xd) return MEMRA_ERR_INVALID_ARG;
+  if (FMT == kQ4) {
+    if (K % 256 != 0) return MEMRA_ERR_UNSUPPORTED;
+    if (!aligned(wq_bank, 16) || !aligned(wd_bank, 16) || !aligned(xq, 16) || !aligned(xd, 16))
+      return MEMRA_ERR_ALIGNMENT;
+  } else if (!aligned(wq_bank, 32) || !aligned(wd_bank, 2) || !aligned(xq, 16) ||
+             !aligned(xd, 4)) {
+    return MEMRA_ERR_ALIGNMENT;
+  }
+  const int64_t xrows = x_per_expert ? P : T;
+  if (!x_fits(xrows, K)) return MEMRA_ERR_UNSUPPORTED;
+  Params p{};
+  p.wq = wq_bank;
+  p.wd = wd_bank;
+  p.N = N;
+  p.K = K;
+  p.xq = xq;
+  p.xd = xd;
+  p.xrows = (int)xrows;
+  p.y = gate_w ? workspace : y;
+  p.ids = ids;
+  p.top_k = (int)P;
+  p.E = E;
+  p.xpe = 1;
+  p.xdiv = x_per_expert ? 1 : (int)top_k;
+  p.lockstep = (int)P;
+  p.status = dev_status;
+  p.units = P * N;
+  const memra_status st = run_product<1, 1, kMoeUngated, kXq8, FMT>(p, stream);
+  if (st != MEMRA_OK || !gate_w) return st;
+  return launch_combine(workspace, ids, gate_w, T, top_k, N, E, y, stream);
+}
 }  // namespace
 }  // namespace memra
 
@@ -1355,6 +1483,100 @@ extern "C" memra_status memra_q4_0_moe_gemv(const uint8_t* wq4_bank, const uint1
                                             int32_t* dev_status, cudaStream_t stream) {
   return moe_gemv<kQ4>(reinterpret_cast<const int8_t*>(wq4_bank), wd_bank, E, N, K, ids, gate_w,
                        top_k, xq, xd, x_per_expert, y, dev_status, stream);
+}
+
+extern "C" memra_status memra_q8_0_moe_gemv_tokens(const int8_t* wq_bank, const uint16_t* wd_bank,
+                                                   int64_t E, int64_t N, int64_t K,
+                                                   const int32_t* ids, const float* gate_w,
+                                                   int64_t T, int64_t top_k, const int8_t* xq,
+                                                   const float* xd, int32_t x_per_expert,
+                                                   float* y, float* workspace,
+                                                   int32_t* dev_status, cudaStream_t stream) {
+  return moe_gemv_tokens<kQ8>(wq_bank, wd_bank, E, N, K, ids, gate_w, T, top_k, xq, xd,
+                              x_per_expert, y, workspace, dev_status, stream);
+}
+
+extern "C" memra_status memra_q4_0_moe_gemv_tokens(const uint8_t* wq4_bank,
+                                                   const uint16_t* wd_bank, int64_t E, int64_t N,
+                                                   int64_t K, const int32_t* ids,
+                                                   const float* gate_w, int64_t T, int64_t top_k,
+                                                   const int8_t* xq, const float* xd,
+                                                   int32_t x_per_expert, float* y,
+                                                   float* workspace, int32_t* dev_status,
+                                                   cudaStream_t stream) {
+  return moe_gemv_tokens<kQ4>(reinterpret_cast<const int8_t*>(wq4_bank), wd_bank, E, N, K, ids,
+                              gate_w, T, top_k, xq, xd, x_per_expert, y, workspace, dev_status,
+                              stream);
+}
+
+extern "C" memra_status memra_q8_0_moe_ffn_tokens(const int8_t* gu_q, const uint16_t* gu_d,
+                                                  const int8_t* dn_q, const uint16_t* dn_d,
+                                                  int64_t E, int64_t H, int64_t F,
+                                                  const int32_t* ids, const float* gate_w,
+                                                  int64_t T, int64_t top_k, const void* x,
+                                                  int32_t dtype, float* y, float* workspace,
+                                                  int32_t* dev_status, cudaStream_t stream) {
+  if (E < 1 || H < 0 || F < 0 || H % 32 != 0 || F % 32 != 0 || top_k < 1 || T < 0)
+    return MEMRA_ERR_INVALID_ARG;
+  if (dtype != MEMRA_BF16 && dtype != MEMRA_F32) return MEMRA_ERR_INVALID_ARG;
+  if (top_k > MEMRA_MAX_TOP_K || T > MEMRA_MAX_PAIRS || T * top_k > MEMRA_MAX_PAIRS)
+    return MEMRA_ERR_UNSUPPORTED;
+  if (H > INT32_MAX / 2 || F > INT32_MAX / 2 || E > INT32_MAX) return MEMRA_ERR_UNSUPPORTED;
+  if (H == 0 || T == 0) return MEMRA_OK;
+  if (!y || !ids || !gate_w) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(y, 4) || !aligned(ids, 4) || !aligned(gate_w, 4) ||
+      (dev_status && !aligned(dev_status, 4)))
+    return MEMRA_ERR_ALIGNMENT;
+  if (F == 0) return zero_fill(y, T * H, stream);
+  if (!gu_q || !gu_d || !dn_q || !dn_d || !x || !workspace) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(gu_q, 32) || !aligned(gu_d, 2) || !aligned(dn_q, 32) || !aligned(dn_d, 2) ||
+      !aligned(x, 16) || !aligned(workspace, 16))
+    return MEMRA_ERR_ALIGNMENT;
+  const int64_t P = T * top_k;
+  if (!x_fits(T, H) || !x_fits(P, F)) return MEMRA_ERR_UNSUPPORTED;
+  float* gu = workspace;              // [P][2F]: gate|up rows of every (token, slot)
+  float* yp = workspace + P * 2 * F;  // [P][H]: down rows of every (token, slot)
+  // gate|up, with each token's row quantised in the prologue.
+  Params a{};
+  a.wq = gu_q;
+  a.wd = gu_d;
+  a.N = 2 * F;
+  a.K = H;
+  a.xin = x;
+  a.xrows = (int)T;
+  a.y = gu;
+  a.ids = ids;
+  a.top_k = (int)P;
+  a.E = E;
+  a.xpe = 1;
+  a.xdiv = (int)top_k;
+  a.lockstep = (int)P;
+  a.status = dev_status;
+  a.units = P * 2 * F;
+  memra_status st = dtype == MEMRA_BF16 ? run_product<1, 1, kMoeUngated, kXbf16>(a, stream)
+                                        : run_product<1, 1, kMoeUngated, kXf32>(a, stream);
+  if (st != MEMRA_OK) return st;
+  // down, with SwiGLU + q8_1 of each pair's gate|up row in the prologue.
+  Params b{};
+  b.wq = dn_q;
+  b.wd = dn_d;
+  b.N = H;
+  b.K = F;
+  b.xin = gu;
+  b.xrows = (int)P;
+  b.y = yp;
+  b.ids = ids;
+  b.top_k = (int)P;
+  b.E = E;
+  b.xpe = 1;
+  b.xdiv = 1;
+  b.lockstep = (int)P;
+  b.status = dev_status;
+  b.routing_ready = 1;  // the gate|up kernel above waited for the routing
+  b.units = P * H;
+  st = run_product<1, 1, kMoeUngated, kXswiglu>(b, stream);
+  if (st != MEMRA_OK) return st;
+  return launch_combine(yp, ids, gate_w, T, top_k, H, E, y, stream);
 }
 
 extern "C" memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* gu_d,

@@ -70,7 +70,8 @@ typedef enum memra_dtype { MEMRA_BF16 = 0, MEMRA_F32 = 1 } memra_dtype;
 
 /* Limits. */
 #define MEMRA_MAX_M 16           /* activation rows per small-M call */
-#define MEMRA_MAX_TOP_K 64       /* experts per routed call */
+#define MEMRA_MAX_TOP_K 64       /* experts per routed call (per token) */
+#define MEMRA_MAX_PAIRS 128      /* (token, slot) pairs per batched routed call */
 /* Bytes of q8_1 activation a pass over the weights holds on chip: P*K*(1 + 4/32)
  * with P the rows of one pass (M up to 8, else ceil(M/2)). */
 #define MEMRA_MAX_X_BYTES 196608
@@ -296,6 +297,58 @@ memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* gu_d, const 
                                 const int32_t* ids, const float* gate_w, int64_t top_k,
                                 const void* x, int32_t dtype, float* y, float* workspace,
                                 int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Routed experts for a batch of T tokens (the pages' expert-major MoE batching,
+ * memra wiki, feature list; here for speculative verify or batched decode of
+ * routed layers).  Token t routes ids[t][0..top_k) with gates gate_w[t][..].
+ * Every (token, slot) pair is computed with the single-token arithmetic, and pairs
+ * that route to the same expert stream its rows at the same time, so the expert's
+ * weights come from HBM once and from L2 after (not a guarantee: a timing effect).
+ *   ids: device int32 [T][top_k]; gate_w: device fp32 [T][top_k] or NULL.
+ *   x_per_expert == 0: xq [T][K], xd [T][K/32], one row per token;
+ *   x_per_expert == 1: xq [T][top_k][K], xd [T][top_k][K/32], one row per pair.
+ *   gate_w == NULL: y fp32 [T][top_k][N], y[t][k] = W[ids[t][k]] x; workspace unused.
+ *   gate_w given:   y fp32 [T][N], y[t] = sum_k gate_w[t][k] y[t][k] in ascending k;
+ *                   workspace: caller-allocated fp32 [T][top_k][N] (4-byte aligned),
+ *                   which keeps the per-pair rows after the call.
+ * Row t of the result equals, bit for bit, memra_q8_0_moe_gemv on token t alone.
+ * Limits: top_k <= MEMRA_MAX_TOP_K, T * top_k <= MEMRA_MAX_PAIRS, and the
+ * activation rows (T, or T * top_k per pair) within MEMRA_MAX_X_BYTES.  Bad ids,
+ * alignment and dev_status as memra_q8_0_moe_gemv.  T == 0 or N == 0 launches nothing.
+ */
+memra_status memra_q8_0_moe_gemv_tokens(const int8_t* wq_bank, const uint16_t* wd_bank, int64_t E,
+                                        int64_t N, int64_t K, const int32_t* ids,
+                                        const float* gate_w, int64_t T, int64_t top_k,
+                                        const int8_t* xq, const float* xd, int32_t x_per_expert,
+                                        float* y, float* workspace, int32_t* dev_status,
+                                        cudaStream_t stream);
+
+/* memra_q8_0_moe_gemv_tokens on a Q4_0 expert bank (layout and limits as
+ * memra_q4_0_moe_gemv). */
+memra_status memra_q4_0_moe_gemv_tokens(const uint8_t* wq4_bank, const uint16_t* wd_bank,
+                                        int64_t E, int64_t N, int64_t K, const int32_t* ids,
+                                        const float* gate_w, int64_t T, int64_t top_k,
+                                        const int8_t* xq, const float* xd, int32_t x_per_expert,
+                                        float* y, float* workspace, int32_t* dev_status,
+                                        cudaStream_t stream);
+
+/*
+ * memra_q8_0_moe_ffn for a batch of T tokens, in three kernels: gate|up of every
+ * (token, slot) pair with each token's row quantised in the prologue, down of every
+ * pair with its SwiGLU + q8_1 in the prologue, and the gated sum per token.
+ *   x [T][H] (bf16 bits or fp32, 16-byte aligned); ids, gate_w [T][top_k]; y fp32 [T][H].
+ *   workspace: caller-allocated device fp32 [T * top_k * (2F + H)], 16-byte aligned:
+ *   the pairs' gate|up rows [T][top_k][2F], then their down rows [T][top_k][H].
+ * Row t of y equals, bit for bit, memra_q8_0_moe_ffn on token t alone.  Limits as
+ * memra_q8_0_moe_gemv_tokens (x: T rows of H; h: T * top_k rows of F).
+ */
+memra_status memra_q8_0_moe_ffn_tokens(const int8_t* gu_q, const uint16_t* gu_d,
+                                       const int8_t* dn_q, const uint16_t* dn_d, int64_t E,
+                                       int64_t H, int64_t F, const int32_t* ids,
+                                       const float* gate_w, int64_t T, int64_t top_k,
+                                       const void* x, int32_t dtype, float* y, float* workspace,
+                                       int32_t* dev_status, cudaStream_t stream);
 
 /*
  * memra_q8_0_moe_ffn without caller memory.  The pages have no counterpart: this

@@ -264,5 +264,31 @@ def moe_ffn(x, gu_q, gu_d, dn_q, dn_d, ids, gate_w):
     return y, bad
 
 
+def moe_gemv_tokens(wq_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert):
+    """Routed experts for a batch of tokens: each token's routed product on its own (the
+    pages' batching changes which weights are read together, not what a token gets).
+    ids [T, top_k], gate_w [T, top_k] or None; xq/xd [T, K] or [T, top_k, K].  Returns
+    (y, n_bad): y [T, top_k, N] without gate weights, [T, N] with them."""
+    ids = np.asarray(ids)
+    ys, bad = [], 0
+    for t in range(ids.shape[0]):
+        y, b = moe_gemv(wq_bank, wd_bank, ids[t], None if gate_w is None else gate_w[t],
+                        xq[t], xd[t], x_per_expert)
+        ys.append(y)
+        bad += b
+    return np.stack(ys), bad
+
+
+def moe_ffn_tokens(x, gu_q, gu_d, dn_q, dn_d, ids, gate_w):
+    """The routed FFN layer for a batch of tokens, each on its own.  x fp32 [T, K],
+    ids and gate_w [T, top_k]; returns (y [T, N_out], n_bad)."""
+    ys, bad = [], 0
+    for t in range(np.asarray(ids).shape[0]):
+        y, b = moe_ffn(x[t], gu_q, gu_d, dn_q, dn_d, ids[t], gate_w[t])
+        ys.append(y)
+        bad += b
+    return np.stack(ys), bad
+
+
 def max_threads():
     return int(lib().oracle_openmp_max_threads())

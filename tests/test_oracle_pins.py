@@ -624,3 +624,53 @@ def test_repack_is_a_byte_permutation(orc):
     blk = raw.reshape(nblk, 34)
     assert np.array_equal(q.view(np.uint8).reshape(nblk, 32), blk[:, 2:])
     assert np.array_equal(d.reshape(nblk).view(np.uint8).reshape(nblk, 2), blk[:, :2])
+
+
+# ----------------------------------------------------------------------------
+# Routed experts for a batch of tokens: each token on its own.
+# ----------------------------------------------------------------------------
+
+def _quant_bank(orc, seed, E, N, K):
+    w, wq, wd = _bank(seed, E, N, K)
+    for e in range(E):
+        wq[e], wd[e] = orc.quantize_q8_0(w[e])
+    return wq, wd
+
+
+def test_moe_gemv_tokens_single_token_and_shared_expert(orc):
+    E, N, K, T, top_k = 6, 16, 96, 3, 2
+    wq, wd = _quant_bank(orc, 30, E, N, K)
+    x = rng(31).standard_normal((T, K)).astype(np.float32)
+    xq, xd = orc.quantize_q8_1(x)
+    # tokens 0 and 2 both route to expert 4, in different slots
+    ids = np.array([[4, 1], [0, 5], [2, 4]], np.int32)
+    gw = np.array([[0.7, 0.3], [0.5, 0.5], [0.25, 0.75]], np.float32)
+    y, bad = orc.moe_gemv_tokens(wq, wd, ids, None, xq, xd, 0)
+    assert bad == 0 and y.shape == (T, top_k, N)
+    # pair (t, k) is expert ids[t, k] applied to token t's row, by the plain GEMV
+    for t in range(T):
+        for k in range(top_k):
+            e = ids[t, k]
+            assert np.array_equal(y[t, k], orc.gemm(wq[e], wd[e], xq[t:t + 1], xd[t:t + 1])[0])
+    yg, _ = orc.moe_gemv_tokens(wq, wd, ids, gw, xq, xd, 0)
+    # the gated row is the gated product of that token alone, with its own gates
+    for t in range(T):
+        one, _ = orc.moe_gemv(wq, wd, ids[t], gw[t], xq[t:t + 1], xd[t:t + 1], 0)
+        assert np.array_equal(yg[t], one)
+    # swapping two tokens swaps their rows
+    perm = [2, 0, 1]
+    yp, _ = orc.moe_gemv_tokens(wq, wd, ids[perm], gw[perm], xq[perm], xd[perm], 0)
+    assert np.array_equal(yp, yg[perm])
+
+
+def test_moe_gemv_tokens_per_pair_rows(orc):
+    E, N, K, T, top_k = 4, 8, 64, 2, 3
+    wq, wd = _quant_bank(orc, 32, E, N, K)
+    x = rng(33).standard_normal((T, top_k, K)).astype(np.float32)
+    xq, xd = orc.quantize_q8_1(x.reshape(T * top_k, K))
+    xq, xd = xq.reshape(T, top_k, K), xd.reshape(T, top_k, K // 32)
+    ids = np.array([[3, 0, 3], [1, 2, -1]], np.int32)
+    y, bad = orc.moe_gemv_tokens(wq, wd, ids, None, xq, xd, 1)
+    assert bad == 1 and not y[1, 2].any()
+    assert np.array_equal(y[0, 2], orc.gemm(wq[3], wd[3], xq[0, 2:3], xd[0, 2:3])[0])
+    assert np.array_equal(y[1, 0], orc.gemm(wq[1], wd[1], xq[1, 0:1], xd[1, 0:1])[0])
