@@ -16,7 +16,7 @@ peak; ``cpu_baseline`` is the CPU oracle on the host cores over a bounded sample
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl memra|reference]
                   [--workload dense27b_sweep|gemv_4096|verify_m2|verify_m4|verify_m8|
                               batch_m16|moe_top8|stress_lm_head|dense27b_sweep_q4_0|
-                              moe_top8_q4_0]
+                              moe_top8_q4_0|moe_top8_tokens8]
 """
 import argparse
 import hashlib
@@ -41,7 +41,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8", "batch_m16",
              "moe_top8",
-             "stress_lm_head", "dense27b_sweep_q4_0", "moe_top8_q4_0")
+             "stress_lm_head", "dense27b_sweep_q4_0", "moe_top8_q4_0", "moe_top8_tokens8")
 
 
 # ----------------------------------------------------------------------------
@@ -77,6 +77,15 @@ def quantized_weights(mem, N, K, *keys, device, perturb=None, fmt="q8_0"):
         wq, wd = mem.memra_quantize_q8_0(w)
     del w
     return wq, wd
+
+
+def tokens_of(name):
+    """Tokens one step decodes: a batch of sequences or of routed tokens, else 1."""
+    if name.startswith("batch_m"):
+        return rows_of(name)
+    if name.endswith("tokens8"):
+        return 8
+    return 1
 
 
 def rows_of(name):
@@ -128,15 +137,24 @@ def build_stress(mem, device, M):
 
 
 class MoeLayer:
-    def __init__(self, mem, layer, device, fmt="q8_0"):
+    """One routed FFN layer for one token, or (tokens > 1) for a batch of tokens with
+    their own routings through the batched entry points."""
+
+    def __init__(self, mem, layer, device, fmt="q8_0", tokens=1):
         c = synth.MOE
         E, H, F, k = c["experts"], c["hidden"], c["ffn"], c["top_k"]
         self.fmt = fmt
+        self.tokens = tokens
         kdiv = 2 if fmt == "q4_0" else 1  # quant bytes per weight: 1/2 for Q4_0
         gq, gd = quantized_weights(mem, E * 2 * F, H, 3, layer, 0, device=device, fmt=fmt)
         dq, dd = quantized_weights(mem, E * H, F, 3, layer, 1, device=device, fmt=fmt)
         self.gq, self.gd = gq.view(E, 2 * F, H // kdiv), gd.view(E, 2 * F, H // 32)
         self.dq, self.dd = dq.view(E, H, F // kdiv), dd.view(E, H, F // 32)
+        if tokens > 1:
+            if fmt != "q8_0":
+                raise ValueError("the batched routed FFN takes Q8_0 banks")
+            self._init_tokens(layer, device, E, H, F, k, tokens)
+            return
         self.ids, self.gw = synth.routing(E, k, 3, layer, 2, device=device)
         self.x = synth.activations_bf16(1, H, 3, layer, 3, device=device)
         self.xq = torch.empty((1, H), dtype=torch.int8, device=device)
@@ -150,12 +168,37 @@ class MoeLayer:
         self.weight_bytes = k * (self.gq[0].numel() + self.gd[0].numel() * 2 +
                                  self.dq[0].numel() + self.dd[0].numel() * 2)
 
+    def _init_tokens(self, layer, device, E, H, F, k, T):
+        routes = [synth.routing(E, k, 3, layer, 2, t, device=device) for t in range(T)]
+        self.ids = torch.stack([r[0] for r in routes]).contiguous()
+        self.gw = torch.stack([r[1] for r in routes]).contiguous()
+        self.x = synth.activations_bf16(T, H, 3, layer, 3, device=device)
+        self.xq = torch.empty((T, H), dtype=torch.int8, device=device)
+        self.xd = torch.empty((T, H // 32), dtype=torch.float32, device=device)
+        P = T * k
+        self.ws = torch.empty((P * (2 * F + H),), dtype=torch.float32, device=device)
+        self.ygu = self.ws[:P * 2 * F].view(T, k, 2 * F)
+        self.hq = torch.empty((T, k, F), dtype=torch.int8, device=device)
+        self.hd = torch.empty((T, k, F // 32), dtype=torch.float32, device=device)
+        self.ydn = self.ws[P * 2 * F:].view(T, k, H)
+        self.y = torch.empty((T, H), dtype=torch.float32, device=device)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=device)
+        # every distinct expert of the layer is read once per step
+        distinct = len(set(self.ids.flatten().tolist()))
+        self.pairs = P
+        self.distinct = distinct
+        self.weight_bytes = distinct * (self.gq[0].numel() + self.gd[0].numel() * 2 +
+                                        self.dq[0].numel() + self.dd[0].numel() * 2)
+
     def gemv(self, mem, *args, **kw):
         if self.fmt == "q4_0":
             return mem.memra_q4_0_moe_gemv(*args, **kw)
         return mem.memra_q8_0_moe_gemv(*args, **kw)
 
     def run(self, mem, fused=False):
+        if self.tokens > 1:
+            self.run_tokens(mem, fused)
+            return
         if fused:
             if self.fmt != "q8_0":
                 raise ValueError("the two-kernel routed FFN takes Q8_0 banks")
@@ -169,6 +212,28 @@ class MoeLayer:
         mem.memra_swiglu_quantize_q8_1(self.ygu, self.hq, self.hd)
         self.gemv(mem, self.dq, self.dd, self.ids, self.gw, self.hq, self.hd, True,
                   y=self.y, dev_status=self.status)
+
+    def run_tokens(self, mem, fused):
+        if fused:
+            mem.memra_q8_0_moe_ffn_tokens(self.gq, self.gd, self.dq, self.dd, self.ids, self.gw,
+                                          self.x, y=self.y, workspace=self.ws,
+                                          dev_status=self.status)
+            return
+        T, k = self.ids.shape
+        mem.memra_quantize_q8_1(self.x, self.xq, self.xd)
+        self.gemv_tokens(mem, False)
+        mem.memra_swiglu_quantize_q8_1(self.ygu.view(T * k, -1), self.hq.view(T * k, -1),
+                                       self.hd.view(T * k, -1))
+        self.gemv_tokens(mem, True)
+
+    def gemv_tokens(self, mem, down):
+        if down:
+            mem.memra_q8_0_moe_gemv_tokens(self.dq, self.dd, self.ids, self.gw, self.hq, self.hd,
+                                           True, y=self.y, workspace=self.ydn,
+                                           dev_status=self.status)
+        else:
+            mem.memra_q8_0_moe_gemv_tokens(self.gq, self.gd, self.ids, None, self.xq, self.xd,
+                                           False, y=self.ygu, dev_status=self.status)
 
 
 def run_gemv_op(mem, op, quantize=True, fused=False):
@@ -216,10 +281,12 @@ class Workload:
             self.ops = build_gemv_4096(mem, device)
         elif name == "stress_lm_head":
             self.ops = build_stress(mem, device, M=1) + build_stress(mem, device, M=8)
-        elif name in ("moe_top8", "moe_top8_q4_0"):
+        elif name in ("moe_top8", "moe_top8_q4_0", "moe_top8_tokens8"):
             n = synth.MOE["layers"] if layers is None else layers
             fmt = "q4_0" if name.endswith("q4_0") else "q8_0"
-            self.moe = [MoeLayer(mem, layer, device, fmt=fmt) for layer in range(n)]
+            tokens = 8 if name.endswith("tokens8") else 1
+            self.moe = [MoeLayer(mem, layer, device, fmt=fmt, tokens=tokens)
+                        for layer in range(n)]
         else:
             raise ValueError(name)
         self._pack_arenas()
@@ -279,6 +346,8 @@ class Workload:
         if self.chain is not None:
             return 1
         if self.moe is not None:
+            if self.moe[0].tokens > 1:  # + the gated sum per token
+                return (3 if self.fused else 5) * len(self.moe)
             return (2 if self.fused else 4) * len(self.moe)
         return (self.passes + (0 if self.fused else 1)) * len(self.ops)
 
@@ -309,6 +378,10 @@ class Workload:
             self.step()  # both launches of the fused layer stream weights
         elif self.moe is not None:
             for m in self.moe:
+                if m.tokens > 1:
+                    m.gemv_tokens(self.mem, False)
+                    m.gemv_tokens(self.mem, True)
+                    continue
                 m.gemv(self.mem, m.gq, m.gd, m.ids, None, m.xq[0], m.xd[0], False,
                        y=m.ygu, dev_status=m.status)
                 m.gemv(self.mem, m.dq, m.dd, m.ids, m.gw, m.hq, m.hd, True,
@@ -546,6 +619,12 @@ def workload_config(name, wl):
         cfg.update({"N": 4096, "K": 4096, "M": 1, "weight_copies": len(wl.ops)})
     elif name.startswith("moe_top8"):
         cfg.update(dict(synth.MOE))
+        if wl.moe[0].tokens > 1:
+            cfg["tokens"] = wl.moe[0].tokens
+            cfg["pairs_per_layer"] = wl.moe[0].pairs
+            cfg["distinct_experts_per_layer"] = round(
+                sum(m.distinct for m in wl.moe) / len(wl.moe), 2)
+            cfg["weight_bytes_counted"] = "each distinct routed expert of a layer once"
     elif name == "stress_lm_head":
         cfg.update({"shapes": [[n, N, K] for n, N, K in synth.STRESS["shapes"]], "M": [1, 8]})
     cfg["weights"] = ("N(0,0.02) fp32 quantised to Q4_0 (32 4-bit codes + fp16 scale per block)"
@@ -574,7 +653,8 @@ def run_memra(args):
 
     # Dense products quantise with a separate launch unless --fused; the routed FFN
     # uses its two-kernel entry point unless --unfused.
-    fused = (not args.unfused) if args.workload == "moe_top8" else args.fused
+    fused = ((not args.unfused) if args.workload in ("moe_top8", "moe_top8_tokens8")
+             else args.fused)
     wl = Workload(args.workload, mem, device, layers=args.layers, fused=fused,
                   chain=args.chain)
     stream = torch.cuda.Stream(device)
@@ -674,8 +754,13 @@ def run_memra(args):
                                           "(memra_q8_0_quant_gemm)" if wl.fused else
                                           "separate memra_quantize_q8_1 launch")
         else:
-            cfg["layer_calls"] = ("memra_q8_0_moe_ffn (2 kernels)" if wl.fused else
-                                  "quantize, moe_gemv, swiglu_quantize, moe_gemv")
+            if wl.moe[0].tokens > 1:
+                cfg["layer_calls"] = ("memra_q8_0_moe_ffn_tokens (3 kernels)" if wl.fused else
+                                      "quantize, moe_gemv_tokens, swiglu_quantize, "
+                                      "moe_gemv_tokens (gated: + per-token sum)")
+            else:
+                cfg["layer_calls"] = ("memra_q8_0_moe_ffn (2 kernels)" if wl.fused else
+                                      "quantize, moe_gemv, swiglu_quantize, moe_gemv")
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -684,8 +769,8 @@ def run_memra(args):
             "data": "synthetic (seeded N(0,0.02) weights, bf16 N(0,1) activations)",
             "config": cfg,
             "us_per_step": round(ms_per_step * 1e3, 2),
-            "tok_per_s": round(1e3 * (rows_of(args.workload) if args.workload.startswith(
-                "batch_m") else 1) / ms_per_step, 2) if args.workload.startswith(
+            "tok_per_s": round(1e3 * tokens_of(args.workload) / ms_per_step, 2)
+            if args.workload.startswith(
                 ("moe_top8", "dense27b_sweep", "verify_m", "batch_m")) else None,
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "hbm_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),

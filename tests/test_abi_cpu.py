@@ -117,6 +117,37 @@ def test_repack_argument_errors(L):
         assert f(None, 4, 0, None, None, None) == 0
 
 
+def test_moe_tokens_argument_errors(L):
+    g = L.memra_q8_0_moe_gemv_tokens
+
+    def call(E=4, N=16, K=64, gw=None, T=2, top_k=8, xpe=0, ws=None, y=A256):
+        return g(A256, A256, E, N, K, A256, gw, T, top_k, A256, A256, xpe, y, ws, None, None)
+
+    assert call(K=48) == 1                    # K % 32 != 0
+    assert call(T=-1) == 1
+    assert call(xpe=2) == 1
+    assert call(top_k=65) == 3                # beyond MEMRA_MAX_TOP_K
+    assert call(T=17, top_k=8) == 3           # 136 pairs > MEMRA_MAX_PAIRS
+    assert call(T=200, top_k=1) == 3
+    assert call(gw=A256, ws=None) == 1        # gated without a workspace
+    assert call(y=None) == 1
+    assert call(y=A256 + 2) == 2
+    assert call(T=0) == 0 and call(N=0) == 0  # empty: no work
+    f = L.memra_q8_0_moe_ffn_tokens
+
+    def ffn(H=64, F=32, gw=A256, T=2, top_k=8, dt=0, ws=A256, x=A256):
+        return f(A256, A256, A256, A256, 4, H, F, A256, gw, T, top_k, x, dt, A256, ws, None,
+                 None)
+
+    assert ffn(H=48) == 1 and ffn(F=48) == 1
+    assert ffn(dt=7) == 1
+    assert ffn(gw=None) == 1                  # the layer needs gate weights
+    assert ffn(T=17) == 3
+    assert ffn(ws=None) == 1 and ffn(x=None) == 1
+    assert ffn(ws=A256 + 4) == 2 and ffn(x=A256 + 8) == 2
+    assert ffn(T=0) == 0
+
+
 def test_moe_argument_errors(L):
     f = L.memra_q8_0_moe_gemv
     args = dict(wq=A256, wd=A256, E=4, N=16, K=64, ids=A256, gw=None, top_k=2, xq=A256,
