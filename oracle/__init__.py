@@ -38,6 +38,18 @@ def lib():
         L.oracle_quantize_q4_0.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         L.oracle_unpack_q4_0.argtypes = [_ptr, _i64, _i64, _ptr]
         L.oracle_repack_q8_0.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
+        L.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+        L.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_f32.restype = ctypes.c_float
+        L.oracle_f32_to_e2m1.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_e2m1.restype = ctypes.c_uint8
+        L.oracle_quantize_nvfp4.argtypes = [_ptr, _i64, _i64, _ptr, _ptr, _ptr]
+        L.oracle_unpack_nvfp4.argtypes = [_ptr, _i64, _i64, _ptr]
+        L.oracle_nvfp4_gemm.argtypes = [_ptr, _ptr, ctypes.c_float, _i64, _i64, _i64, _ptr, _ptr,
+                                        _ptr, ctypes.c_int]
+        L.oracle_nvfp4_dequant_gemm_f64.argtypes = [_ptr, _ptr, ctypes.c_float, _i64, _i64, _i64,
+                                                    _ptr, _ptr, _ptr]
         L.oracle_repack_q4_0.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         L.oracle_quantize_q8_1_f32.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
         L.oracle_quantize_q8_1_bf16.argtypes = [_ptr, _i64, _i64, _ptr, _ptr]
@@ -145,6 +157,72 @@ def repack_q4_0(blocks, N, K):
     d = np.empty((N, K // 32), np.uint16)
     lib().oracle_repack_q4_0(_p(blocks), N, K, _p(q4), _p(d))
     return q4, d
+
+
+def f32_to_e4m3(values):
+    v = np.asarray(values, np.float32)
+    return np.array([lib().oracle_f32_to_e4m3(float(x)) for x in v.ravel()],
+                    np.uint8).reshape(v.shape)
+
+
+def e4m3_to_f32(bits):
+    b = np.asarray(bits, np.uint8)
+    return np.array([lib().oracle_e4m3_to_f32(int(x)) for x in b.ravel()],
+                    np.float32).reshape(b.shape)
+
+
+def f32_to_e2m1(values):
+    v = np.asarray(values, np.float32)
+    return np.array([lib().oracle_f32_to_e2m1(float(x)) for x in v.ravel()],
+                    np.uint8).reshape(v.shape)
+
+
+def quantize_nvfp4(w):
+    """Weights fp32 [N, K] -> (codes uint8 [N, K/2], scales E4M3 bits uint8 [N, K/16], g)."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert K % 32 == 0
+    codes = np.empty((N, K // 2), np.uint8)
+    scales = np.empty((N, K // 16), np.uint8)
+    g = np.zeros(1, np.float32)
+    lib().oracle_quantize_nvfp4(_p(w), N, K, _p(codes), _p(scales), _p(g))
+    return codes, scales, np.float32(g[0])
+
+
+def unpack_nvfp4(codes):
+    """NVFP4 codes uint8 [N, K/2] -> twice their E2M1 values, int8 [N, K]."""
+    codes = _c(codes, np.uint8)
+    N, K2 = codes.shape
+    out = np.empty((N, 2 * K2), np.int8)
+    lib().oracle_unpack_nvfp4(_p(codes), N, 2 * K2, _p(out))
+    return out
+
+
+def gemm_nvfp4(codes, scales, g, xq, xd, threads=1):
+    """y[M, N] float32 = NVFP4 W (codes, E4M3 block scales, tensor scale g) times q8_1 x."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    xq = _c(xq, np.int8)
+    xd = _c(xd, np.float32)
+    N, K2 = codes.shape
+    M = xq.shape[0]
+    y = np.empty((M, N), np.float32)
+    lib().oracle_nvfp4_gemm(_p(codes), _p(scales), float(g), N, 2 * K2, M, _p(xq), _p(xd),
+                            _p(y), int(threads))
+    return y
+
+
+def nvfp4_dequant_gemm_f64(codes, scales, g, xq, xd):
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    xq = _c(xq, np.int8)
+    xd = _c(xd, np.float32)
+    N, K2 = codes.shape
+    M = xq.shape[0]
+    y = np.empty((M, N), np.float64)
+    lib().oracle_nvfp4_dequant_gemm_f64(_p(codes), _p(scales), float(g), N, 2 * K2, M, _p(xq),
+                                        _p(xd), _p(y))
+    return y
 
 
 def gemm_q4_0(q4, wd, xq, xd, threads=1):

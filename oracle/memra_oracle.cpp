@@ -26,6 +26,7 @@
 // through itself (closed forms, invariants, brute force in int64 / fp64, numpy's
 // IEEE conversions, libm).  No function here is "parity unpinned".
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -240,6 +241,164 @@ void oracle_repack_q4_0(const uint8_t* blocks, int64_t N, int64_t K, uint8_t* q4
       const uint8_t* blk = blocks + (n * nb + b) * 18;
       d[n * nb + b] = (uint16_t)(blk[0] | (blk[1] << 8));
       for (int j = 0; j < 16; ++j) q4[n * (K / 2) + b * 16 + j] = blk[2 + j];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 weights (the pages' third decode format: memra wiki, feature list; their
+// safetensors loader reads NVIDIA ModelOpt NVFP4 checkpoints byte for byte).  The
+// pages print none of it; the reading is ModelOpt's NVFP4, restated:
+//   a block is 16 consecutive weights of a row; each weight is an FP4 E2M1 code
+//   (sign, 2 exponent bits, 1 mantissa bit: magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6),
+//   each block has an FP8 E4M3 scale s, and the tensor one fp32 scale g, so that
+//   w ~= g * s * e2m1(code).  Byte j of a row's code plane holds element 2j in its
+//   low nibble and element 2j+1 in its high nibble.
+// Quantisation: g = amax|W| / (6 * 448); per block s = e4m3(amax_block / (6 g));
+// code = e2m1(w / (float(s) * g)), a block whose scale is 0 gets code 0.  Every
+// conversion rounds to nearest, ties to even, and saturates (448, 6).  Each fp32
+// operation is one IEEE operation in the order written.
+// ---------------------------------------------------------------------------
+
+// FP8 E4M3 ("fn": bias 7, no infinities, largest finite 448) from fp32, written
+// from the definition: the quantum of |f|'s binade (2^(e-3) for normals, 2^-9 for
+// subnormals), the nearest multiple of it (ties to even via nearbyint), saturation
+// at 448, then the encoding.
+uint8_t f32_to_e4m3(float f) {
+  const uint8_t sign = std::signbit(f) ? 0x80 : 0x00;
+  const double a = std::fabs((double)f);
+  if (a == 0.0) return sign;
+  int e2 = 0;
+  std::frexp(a, &e2);  // a = m * 2^e2 with m in [0.5, 1): binade exponent e2 - 1
+  const int be = std::max(e2 - 1, -6);
+  const double q = std::ldexp(1.0, be - 3);
+  double r = std::nearbyint(a / q) * q;
+  if (r > 448.0) r = 448.0;
+  if (r == 0.0) return sign;
+  int re = 0;
+  std::frexp(r, &re);
+  const int rbe = re - 1;
+  if (rbe < -6) return (uint8_t)(sign | (int)std::ldexp(r, 9));  // subnormal: r = m * 2^-9
+  const int m = (int)(std::ldexp(r, -rbe) * 8.0) - 8;             // r = 2^rbe * (1 + m/8)
+  return (uint8_t)(sign | ((rbe + 7) << 3) | m);
+}
+
+// FP8 E4M3 -> fp32, exact (0x7f / 0xff, the NaN codes, never occur here).
+float e4m3_to_f32(uint8_t b) {
+  const int e = (b >> 3) & 15;
+  const int m = b & 7;
+  const double mag = e == 0 ? std::ldexp((double)m, -9) : std::ldexp(1.0 + m / 8.0, e - 7);
+  return (float)((b & 0x80) ? -mag : mag);
+}
+
+// FP4 E2M1 from fp32: the quantum of |f|'s binade (0.5 below 2, 1 below 4, else 2),
+// the nearest multiple (ties to even), saturation at 6, then the code of that value.
+uint8_t f32_to_e2m1(float f) {
+  static const double kVal[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  const uint8_t sign = std::signbit(f) ? 8 : 0;
+  const double a = std::fabs((double)f);
+  const double q = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+  double r = std::nearbyint(a / q) * q;
+  if (r > 6.0) r = 6.0;
+  for (int i = 0; i < 8; ++i)
+    if (kVal[i] == r) return (uint8_t)(sign | i);
+  return sign;  // not reached for finite input
+}
+
+// Twice the E2M1 value of a code, an integer in [-12, 12].
+int e2m1_twice(uint8_t code) {
+  static const int kTwice[8] = {0, 1, 2, 3, 4, 6, 8, 12};
+  return (code & 8) ? -kTwice[code & 7] : kTwice[code & 7];
+}
+
+uint8_t oracle_f32_to_e4m3(float f) { return f32_to_e4m3(f); }
+float oracle_e4m3_to_f32(uint8_t b) { return e4m3_to_f32(b); }
+uint8_t oracle_f32_to_e2m1(float f) { return f32_to_e2m1(f); }
+
+// w: fp32 [N][K], K % 32 == 0.  codes: uint8 [N][K/2]; scales: E4M3 bits [N][K/16];
+// *g: the tensor scale.
+void oracle_quantize_nvfp4(const float* w, int64_t N, int64_t K, uint8_t* codes,
+                           uint8_t* scales, float* g_out) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < N * K; ++i) amax = std::max(amax, std::fabs(w[i]));
+  const float g = amax / 2688.0f;  // 6 * 448
+  *g_out = g;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t blk = 0; blk < K / 16; ++blk) {
+      const float* v = w + n * K + blk * 16;
+      float bmax = 0.0f;
+      for (int i = 0; i < 16; ++i) bmax = std::max(bmax, std::fabs(v[i]));
+      const uint8_t sc = g == 0.0f ? 0 : f32_to_e4m3(bmax / (6.0f * g));
+      scales[n * (K / 16) + blk] = sc;
+      const float denom = e4m3_to_f32(sc) * g;
+      for (int i = 0; i < 16; ++i) {
+        const uint8_t c = denom == 0.0f ? 0 : f32_to_e2m1(v[i] / denom);
+        const int64_t e = blk * 16 + i;  // element index within the row
+        uint8_t& byte = codes[n * (K / 2) + e / 2];
+        if (e % 2 == 0)
+          byte = c;
+        else
+          byte = (uint8_t)(byte | (c << 4));
+      }
+    }
+}
+
+// Codes -> twice their E2M1 values, int8 [N][K].
+void oracle_unpack_nvfp4(const uint8_t* codes, int64_t N, int64_t K, int8_t* twice) {
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t e = 0; e < K; ++e) {
+      const uint8_t byte = codes[n * (K / 2) + e / 2];
+      twice[n * K + e] = (int8_t)e2m1_twice(e % 2 == 0 ? (byte & 0x0F) : (byte >> 4));
+    }
+}
+
+// NVFP4 x q8_1: y[m][n] = (g / 2) * sum_b t_b, summed sequentially in b, with
+//   t_b = (s_lo * d_x) * S_lo + (s_hi * d_x) * S_hi,
+// S_lo, S_hi the exact int32 sums of (twice the E2M1 value) * xq over the first and
+// second 16 elements of activation block b, s_lo, s_hi their blocks' E4M3 scales.
+void oracle_nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float g, int64_t N,
+                       int64_t K, int64_t M, const int8_t* xq, const float* xd, float* y,
+                       int threads) {
+  const int64_t nb = K / 32;
+  (void)threads;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(threads_or_one(threads)) schedule(static)
+#endif
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t m = 0; m < M; ++m) {
+      float acc = 0.0f;
+      for (int64_t b = 0; b < nb; ++b) {
+        int32_t S[2] = {0, 0};
+        for (int i = 0; i < 32; ++i) {
+          const int64_t e = b * 32 + i;
+          const uint8_t byte = codes[n * (K / 2) + e / 2];
+          const int c2 = e2m1_twice(e % 2 == 0 ? (byte & 0x0F) : (byte >> 4));
+          S[i / 16] += c2 * (int32_t)xq[m * K + e];
+        }
+        const float dx = xd[m * nb + b];
+        const float lo = (e4m3_to_f32(scales[n * (K / 16) + 2 * b]) * dx) * (float)S[0];
+        const float hi = (e4m3_to_f32(scales[n * (K / 16) + 2 * b + 1]) * dx) * (float)S[1];
+        const float term = lo + hi;
+        acc = acc + term;
+      }
+      y[m * N + n] = (g * 0.5f) * acc;
+    }
+  }
+}
+
+// fp64 brute force of the same product: sum_k (g s e2m1) * (d_x q_x).
+void oracle_nvfp4_dequant_gemm_f64(const uint8_t* codes, const uint8_t* scales, float g,
+                                   int64_t N, int64_t K, int64_t M, const int8_t* xq,
+                                   const float* xd, double* y) {
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t e = 0; e < K; ++e) {
+        const uint8_t byte = codes[n * (K / 2) + e / 2];
+        const double v = 0.5 * e2m1_twice(e % 2 == 0 ? (byte & 0x0F) : (byte >> 4));
+        const double w = (double)g * (double)e4m3_to_f32(scales[n * (K / 16) + e / 16]) * v;
+        acc += w * ((double)xd[m * (K / 32) + e / 32] * (double)xq[m * K + e]);
+      }
+      y[m * N + n] = acc;
     }
 }
 

@@ -81,3 +81,19 @@ def test_gguf_q4_0_blocks_repack(orc):
     vals = orc.unpack_q4_0(q4)
     assert (vals[0].astype(int) + 8).tolist() == g["codes_row0"]
     assert not vals[1].any()
+
+
+def test_nvfp4_hand_row(orc):
+    g = load("nvfp4_hand_row.json")
+    w = np.array(g["w"], np.float32)[None]
+    codes, scales, gs = orc.quantize_nvfp4(w)
+    assert float(gs) == g["g"]
+    assert scales.ravel().tolist() == g["scales_e4m3_bits"]
+    assert orc.e4m3_to_f32(scales).ravel().tolist() == g["scales_values"]
+    c = np.array(g["codes"], np.uint8)
+    # ModelOpt packing, by hand: element 2j in the low nibble of byte j, 2j+1 in the high.
+    assert codes.ravel().tolist() == (c[0::2] | (c[1::2] << 4)).tolist()
+    xq, xd = orc.quantize_q8_1(np.array(g["x"], np.float32)[None])
+    assert xd.ravel().tolist() == [1.0, 1.0]
+    assert float(orc.gemm_nvfp4(codes, scales, gs, xq, xd)[0, 0]) == g["y"]
+    assert float(orc.nvfp4_dequant_gemm_f64(codes, scales, gs, xq, xd)[0, 0]) == g["y"]

@@ -674,3 +674,133 @@ def test_moe_gemv_tokens_per_pair_rows(orc):
     assert bad == 1 and not y[1, 2].any()
     assert np.array_equal(y[0, 2], orc.gemm(wq[3], wd[3], xq[0, 2:3], xd[0, 2:3])[0])
     assert np.array_equal(y[1, 0], orc.gemm(wq[1], wd[1], xq[1, 0:1], xd[1, 0:1])[0])
+
+
+# ----------------------------------------------------------------------------
+# NVFP4: the FP8 E4M3 and FP4 E2M1 conversions, the quantiser and the product.
+# ----------------------------------------------------------------------------
+
+def _torch_e4m3(values):
+    import torch
+    return torch.tensor(np.asarray(values, np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_exhaustive_against_torch(orc):
+    import torch
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    ref = torch.tensor(codes).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(orc.e4m3_to_f32(codes), ref)
+
+
+def test_e4m3_encode_against_torch(orc):
+    """Every E4M3 value, every midpoint between neighbours (ties to even), one fp32 ulp
+    either side of each midpoint, and random values, below the saturation point."""
+    import torch
+    pos = np.array(sorted(set(torch.tensor(np.arange(0, 127, dtype=np.uint8))
+                               .view(torch.float8_e4m3fn).float().numpy().tolist())), np.float32)
+    mids = ((pos[:-1].astype(np.float64) + pos[1:]) / 2).astype(np.float32)
+    vals = np.concatenate([pos, mids, np.nextafter(mids, np.float32(0)),
+                           np.nextafter(mids, np.float32(1000)),
+                           np.exp(rng(80).uniform(np.log(1e-4), np.log(448), 20000))
+                           .astype(np.float32)])
+    vals = vals[vals <= 448]
+    for v in (vals, -vals):
+        assert np.array_equal(orc.f32_to_e4m3(v), _torch_e4m3(v))
+
+
+def test_e4m3_saturates_at_448(orc):
+    assert orc.f32_to_e4m3([464.0, 500.0, 1e30]).tolist() == [0x7E] * 3
+    assert orc.f32_to_e4m3([-1e30]).tolist() == [0xFE]
+    assert orc.f32_to_e4m3([0.0, -0.0]).tolist() == [0x00, 0x80]
+
+
+def test_e2m1_table_ties_and_saturation(orc):
+    # grid values map to their codes; midpoints go to the even mantissa; beyond 6 saturates
+    table = {0.0: 0, 0.5: 1, 1.0: 2, 1.5: 3, 2.0: 4, 3.0: 5, 4.0: 6, 6.0: 7,
+             0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6,
+             0.2499: 0, 0.2501: 1, 5.0001: 7, 6.9: 7, 100.0: 7}
+    v = np.array(list(table), np.float32)
+    assert orc.f32_to_e2m1(v).tolist() == list(table.values())
+    assert orc.f32_to_e2m1(-v[1:]).tolist() == [c | 8 for c in list(table.values())[1:]]
+    assert orc.f32_to_e2m1([-0.0, -0.1]).tolist() == [8, 8]
+
+
+def _np_unpack_nvfp4(codes):
+    """Independent numpy unpack: byte j -> elements 2j (low nibble) and 2j + 1 (high)."""
+    twice = np.array([0, 1, 2, 3, 4, 6, 8, 12, 0, -1, -2, -3, -4, -6, -8, -12], np.int8)
+    N, K2 = codes.shape
+    out = np.empty((N, 2 * K2), np.int8)
+    out[:, 0::2] = twice[codes & 15]
+    out[:, 1::2] = twice[codes >> 4]
+    return out
+
+
+def test_nvfp4_unpack_matches_hand_packing(orc):
+    codes = rng(81).integers(0, 256, size=(7, 48)).astype(np.uint8)
+    assert np.array_equal(orc.unpack_nvfp4(codes), _np_unpack_nvfp4(codes))
+
+
+@pytest.mark.parametrize("std", [0.02, 1.0, 300.0])
+def test_nvfp4_quant_invariants(orc, std):
+    r = rng(82 + int(std))
+    N, K = 24, 256
+    w = (r.standard_normal((N, K)) * std).astype(np.float32)
+    w[3, 16:32] = 0.0                                       # one all-zero block
+    codes, scales, g = orc.quantize_nvfp4(w)
+    assert g == np.float32(np.abs(w).max()) / np.float32(2688)
+    bmax = np.abs(w).reshape(N, K // 16, 16).max(axis=2)
+    assert np.array_equal(scales, _torch_e4m3(bmax / (np.float32(6) * g)))
+    s = orc.e4m3_to_f32(scales).astype(np.float64)
+    assert scales[3, 1] == 0 and not _np_unpack_nvfp4(codes)[3, 16:32].any()
+    v = _np_unpack_nvfp4(codes).astype(np.float64).reshape(N, K // 16, 16) / 2
+    denom = (s * np.float64(g))[:, :, None]
+    ratio = w.reshape(N, K // 16, 16) / np.where(denom == 0, 1, denom)
+    # each code is the nearest E2M1 value of w / (s g) (half a grid step, within 6)
+    step = np.where(np.abs(v) < 2, 0.5, np.where(np.abs(v) < 4, 1.0, 2.0))
+    ok = (denom > 0) & (np.abs(ratio) <= 6)
+    assert np.all(np.abs(ratio - v)[ok] <= step[ok] / 2 + 1e-6)
+    # the block maximum maps to +-6 (the E4M3 scale is within 2^-4 of max / 6)
+    amax_pos = np.abs(w).reshape(N, K // 16, 16).argmax(axis=2)
+    top = np.take_along_axis(np.abs(v), amax_pos[:, :, None], axis=2)[:, :, 0]
+    assert np.all(top[scales > 0] == 6.0)
+
+
+def test_nvfp4_power_of_two_scaling_and_zero_tensor(orc):
+    w = (rng(85).standard_normal((8, 128)) * 0.7).astype(np.float32)
+    c1, s1, g1 = orc.quantize_nvfp4(w)
+    c2, s2, g2 = orc.quantize_nvfp4(w * np.float32(64))
+    assert np.array_equal(c1, c2) and np.array_equal(s1, s2) and g2 == g1 * 64
+    c0, s0, g0 = orc.quantize_nvfp4(np.zeros((2, 64), np.float32))
+    assert g0 == 0 and not c0.any() and not s0.any()
+
+
+@pytest.mark.parametrize("N,K,M", [(17, 256, 1), (9, 1024, 3), (5, 96, 2)])
+def test_nvfp4_gemm_within_bound_of_fp64_brute_force(orc, N, K, M):
+    r = rng(86 + K)
+    codes, scales, g = orc.quantize_nvfp4((r.standard_normal((N, K)) * 0.02).astype(np.float32))
+    xq, xd = orc.quantize_q8_1(r.standard_normal((M, K)).astype(np.float32))
+    y = orc.gemm_nvfp4(codes, scales, g, xq, xd)
+    y64 = orc.nvfp4_dequant_gemm_f64(codes, scales, g, xq, xd)
+    # sum of |term| over half-blocks, and the sequential fp32 bound (a few ulps per term)
+    c2 = _np_unpack_nvfp4(codes).astype(np.float64)
+    s = orc.e4m3_to_f32(scales).astype(np.float64)
+    S = np.einsum("nbi,mbi->mnb", c2.reshape(N, K // 16, 16),
+                  xq.astype(np.float64).reshape(M, K // 16, 16))
+    terms = np.abs(0.5 * float(g) * s[None] * np.repeat(xd, 2, axis=1)[:, None, :] * S).sum(2)
+    nb = K // 32
+    assert np.all(np.abs(y - y64) <= (nb + 4) * 2.0 ** -23 * terms + 1e-30)
+
+
+def test_nvfp4_gemm_one_hot_activation_exact(orc):
+    # x one-hot at element j with q = 127, d_x = 1: y_n = fl(fl(g/2) * fl(fl(s d_x) * c2 127))
+    N, K, j = 6, 64, 37
+    codes, scales, g = orc.quantize_nvfp4((rng(87).standard_normal((N, K))).astype(np.float32))
+    x = np.zeros((1, K), np.float32)
+    x[0, j] = 127.0
+    xq, xd = orc.quantize_q8_1(x)
+    y = orc.gemm_nvfp4(codes, scales, g, xq, xd)[0]
+    c2 = _np_unpack_nvfp4(codes)[:, j].astype(np.float32)
+    s = orc.e4m3_to_f32(scales[:, j // 16])
+    want = (np.float32(g) * np.float32(0.5)) * ((s * np.float32(1.0)) * (c2 * np.float32(127)))
+    assert np.array_equal(y, want.astype(np.float32))
