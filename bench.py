@@ -16,6 +16,7 @@ peak; ``cpu_baseline`` is the CPU oracle on the host cores over a bounded sample
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl memra|reference]
                   [--workload dense27b_sweep|gemv_4096|verify_m2|verify_m4|verify_m8|
                               batch_m16|moe_top8|stress_lm_head|dense27b_sweep_q4_0|
+                              dense27b_sweep_nvfp4|
                               moe_top8_q4_0|moe_top8_tokens8]
 """
 import argparse
@@ -41,7 +42,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8", "batch_m16",
              "moe_top8",
-             "stress_lm_head", "dense27b_sweep_q4_0", "moe_top8_q4_0", "moe_top8_tokens8")
+             "stress_lm_head", "dense27b_sweep_q4_0", "dense27b_sweep_nvfp4", "moe_top8_q4_0",
+             "moe_top8_tokens8")
 
 
 # ----------------------------------------------------------------------------
@@ -49,12 +51,13 @@ WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8
 # ----------------------------------------------------------------------------
 
 class Gemv:
-    """One product of a step: Q8_0 (wq int8 [N, K]) or Q4_0 (wq uint8 [N, K/2]) weights,
-    its bf16 activation(s), q8_1 buffers, y."""
+    """One product of a step: Q8_0 (wq int8 [N, K]), Q4_0 (wq uint8 [N, K/2]) or NVFP4
+    (wq uint8 codes [N, K/2], wd E4M3 scales [N, K/16], tensor scale g) weights, its
+    bf16 activation(s), q8_1 buffers, y."""
 
-    def __init__(self, wq, wd, x, name):
-        self.wq, self.wd, self.x, self.name = wq, wd, x, name
-        self.fmt = "q4_0" if wq.dtype == torch.uint8 else "q8_0"
+    def __init__(self, wq, wd, x, name, fmt=None, g=None):
+        self.wq, self.wd, self.x, self.name, self.g = wq, wd, x, name, g
+        self.fmt = fmt or ("q4_0" if wq.dtype == torch.uint8 else "q8_0")
         M, K = x.shape
         N = wq.shape[0]
         dev = wq.device
@@ -64,7 +67,7 @@ class Gemv:
 
     @property
     def weight_bytes(self):
-        return self.wq.numel() + self.wd.numel() * 2  # quant plane + fp16 scale plane
+        return self.wq.numel() + self.wd.numel() * self.wd.element_size()  # quants + scales
 
 
 def quantized_weights(mem, N, K, *keys, device, perturb=None, fmt="q8_0"):
@@ -73,6 +76,10 @@ def quantized_weights(mem, N, K, *keys, device, perturb=None, fmt="q8_0"):
         synth.perturb_blocks(w, *keys, **perturb)
     if fmt == "q4_0":
         wq, wd = mem.memra_quantize_q4_0(w)
+    elif fmt == "nvfp4":
+        wq, wd, g = mem.memra_quantize_nvfp4(w)
+        del w
+        return wq, wd, float(g.item())
     else:
         wq, wd = mem.memra_quantize_q8_0(w)
     del w
@@ -104,11 +111,12 @@ def build_dense_sweep(mem, device, M=1, layers=None, workload_id=1, fmt="q8_0"):
     ops = []
     for layer in range(L):
         for t, (name, N, K) in enumerate(cfg["gemvs"]):
-            wq, wd = quantized_weights(mem, N, K, workload_id, layer, t, device=device, fmt=fmt)
+            qw = quantized_weights(mem, N, K, workload_id, layer, t, device=device, fmt=fmt)
             x = synth.activations_bf16(M, K, workload_id, layer, t, 1000 + M,
                                        outlier_frac=cfg["outlier_frac"],
                                        outlier_scale=cfg["outlier_scale"], device=device)
-            ops.append(Gemv(wq, wd, x, "L%d.%s" % (layer, name)))
+            ops.append(Gemv(qw[0], qw[1], x, "L%d.%s" % (layer, name), fmt=fmt,
+                            g=qw[2] if fmt == "nvfp4" else None))
     return ops
 
 
@@ -246,6 +254,12 @@ def run_gemv_op(mem, op, quantize=True, fused=False):
         return
     if quantize:
         mem.memra_quantize_q8_1(op.x, op.xq, op.xd)
+    if op.fmt == "nvfp4":
+        if op.xq.shape[0] == 1:
+            mem.memra_nvfp4_gemv(op.wq, op.wd, op.g, op.xq[0], op.xd[0], y=op.y[0])
+        else:
+            mem.memra_nvfp4_gemm_small_m(op.wq, op.wd, op.g, op.xq, op.xd, y=op.y)
+        return
     if op.fmt == "q4_0":
         if op.xq.shape[0] == 1:
             mem.memra_q4_0_gemv(op.wq, op.wd, op.xq[0], op.xd[0], y=op.y[0])
@@ -271,6 +285,8 @@ class Workload:
         self.ops = []
         if name == "dense27b_sweep":
             self.ops = build_dense_sweep(mem, device, M=1, layers=layers)
+        elif name == "dense27b_sweep_nvfp4":
+            self.ops = build_dense_sweep(mem, device, layers=layers, workload_id=6, fmt="nvfp4")
         elif name == "dense27b_sweep_q4_0":
             self.ops = build_dense_sweep(mem, device, M=1, layers=layers, workload_id=5,
                                          fmt="q4_0")
@@ -629,6 +645,8 @@ def workload_config(name, wl):
         cfg.update({"shapes": [[n, N, K] for n, N, K in synth.STRESS["shapes"]], "M": [1, 8]})
     cfg["weights"] = ("N(0,0.02) fp32 quantised to Q4_0 (32 4-bit codes + fp16 scale per block)"
                       if name.endswith("q4_0") else
+                      "N(0,0.02) fp32 quantised to NVFP4 (E2M1 codes, E4M3 scale per 16, fp32 "
+                      "tensor scale)" if name.endswith("nvfp4") else
                       "N(0,0.02) fp32 quantised to Q8_0 (32 int8 + fp16 scale per block)")
     cfg["weight_bytes_per_step"] = wl.weight_bytes
     cfg["l2"] = ("inputs larger than L2: %.2f GB of distinct weights per step vs 129 MB L2"
@@ -697,7 +715,8 @@ def run_memra(args):
                 "peak_kind": peak_kind + " copy bandwidth (MEASURED_PEAKS hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "kernel": "%s product kernel (%s, M=%s)" % (
-                    "Q4_0" if wl.ops and wl.ops[0].fmt == "q4_0" else "Q8_0",
+                    {"q4_0": "Q4_0", "nvfp4": "NVFP4"}.get(wl.ops[0].fmt, "Q8_0") if wl.ops
+                    else "Q8_0",
                     "chained, one launch per step" if wl.chain is not None else
                     "routed experts" if wl.moe is not None else
                     ("quantise fused" if wl.fused else "q8_1 input"),

@@ -52,6 +52,9 @@ _SIGS = {
     "memra_q8_0_gemv": [_p, _p, _i64, _i64, _p, _p, _p, _p],
     "memra_quantize_q4_0": [_p, _i64, _i64, _p, _p, _p],
     "memra_repack_q8_0": [_p, _i64, _i64, _p, _p, _p],
+    "memra_quantize_nvfp4": [_p, _i64, _i64, _p, _p, _p, _p],
+    "memra_nvfp4_gemm_small_m": [_p, _p, ctypes.c_float, _i64, _i64, _i64, _p, _p, _p, _p],
+    "memra_nvfp4_gemv": [_p, _p, ctypes.c_float, _i64, _i64, _p, _p, _p, _p],
     "memra_repack_q4_0": [_p, _i64, _i64, _p, _p, _p],
     "memra_q4_0_gemv": [_p, _p, _i64, _i64, _p, _p, _p, _p],
     "memra_q4_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
@@ -311,6 +314,68 @@ def memra_q4_0_gemm_small_m(wq4, wd, xq, xd, y=None):
         _check("memra_q4_0_gemm_small_m",
                lib().memra_q4_0_gemm_small_m(_ptr(wq4), _ptr(wd), N, K, M, _ptr(xq), _ptr(xd),
                                              _ptr(y), _stream(wq4)))
+    return y
+
+
+def memra_quantize_nvfp4(w, codes=None, scales=None, g=None):
+    """fp32 weights [N, K] -> (codes uint8 [N, K/2], scales uint8 E4M3 bits [N, K/16],
+    g float32 [1] on the device: the tensor scale)."""
+    _need(w, "w", torch.float32)
+    N, K = w.shape
+    if codes is None:
+        codes = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, K // 16), dtype=torch.uint8, device=w.device)
+    if g is None:
+        g = torch.empty((1,), dtype=torch.float32, device=w.device)
+    _need(codes, "codes", torch.uint8, w.device, (N, K // 2))
+    _need(scales, "scales", torch.uint8, w.device, (N, K // 16))
+    _need(g, "g", torch.float32, w.device, (1,))
+    with torch.cuda.device(w.device):
+        _check("memra_quantize_nvfp4",
+               lib().memra_quantize_nvfp4(_ptr(w), N, K, _ptr(codes), _ptr(scales), _ptr(g),
+                                          _stream(w)))
+    return codes, scales, g
+
+
+def memra_nvfp4_gemm_small_m(codes, scales, g, xq, xd, y=None):
+    """y [M, N] = W (NVFP4: codes uint8 [N, K/2], scales uint8 E4M3 [N, K/16], tensor
+    scale g, a Python float) x (q8_1), M <= 16."""
+    _need(codes, "codes", torch.uint8)
+    N, K2 = codes.shape
+    K = 2 * K2
+    dev = codes.device
+    _need(scales, "scales", torch.uint8, dev, (N, K // 16))
+    _need(xq, "xq", torch.int8, dev)
+    M = xq.shape[0]
+    _need(xq, "xq", torch.int8, dev, (M, K))
+    _need(xd, "xd", torch.float32, dev, (M, K // 32))
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, (M, N))
+    with torch.cuda.device(dev):
+        _check("memra_nvfp4_gemm_small_m",
+               lib().memra_nvfp4_gemm_small_m(_ptr(codes), _ptr(scales), float(g), N, K, M,
+                                              _ptr(xq), _ptr(xd), _ptr(y), _stream(codes)))
+    return y
+
+
+def memra_nvfp4_gemv(codes, scales, g, xq, xd, y=None):
+    """y [N] = W (NVFP4) x (q8_1) for one activation row (xq [K], xd [K/32])."""
+    _need(codes, "codes", torch.uint8)
+    N, K2 = codes.shape
+    K = 2 * K2
+    dev = codes.device
+    _need(scales, "scales", torch.uint8, dev, (N, K // 16))
+    _need(xq, "xq", torch.int8, dev, (K,))
+    _need(xd, "xd", torch.float32, dev, (K // 32,))
+    if y is None:
+        y = torch.empty((N,), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, (N,))
+    with torch.cuda.device(dev):
+        _check("memra_nvfp4_gemv",
+               lib().memra_nvfp4_gemv(_ptr(codes), _ptr(scales), float(g), N, K, _ptr(xq),
+                                      _ptr(xd), _ptr(y), _stream(codes)))
     return y
 
 

@@ -82,9 +82,11 @@ static_assert(MEMRA_MAX_TOP_K <= MEMRA_MAX_PAIRS, "a single token's slots fit");
 
 enum Mode { kDense = 0, kMoeUngated = 1, kMoeGated = 2 };
 
-// Weight formats: Q8_0 (32 int8 quants a block, K bytes a row) and Q4_0 (32 4-bit
-// codes a block, K/2 bytes a row; byte j of a block holds elements j and j+16).
-enum Fmt { kQ8 = 0, kQ4 = 1 };
+// Weight formats: Q8_0 (32 int8 quants a block, K bytes a row), Q4_0 (32 4-bit
+// codes a block, K/2 bytes a row; byte j of a block holds elements j and j+16), and
+// NVFP4 (E2M1 codes, K/2 bytes a row, byte j holding elements 2j and 2j+1; an E4M3
+// scale per 16 elements, so a 32-block's two scales fill the 2-byte scale slot).
+enum Fmt { kQ8 = 0, kQ4 = 1, kNv4 = 2 };
 
 // dp4a with unsigned bytes in a and signed bytes in b (the Q4_0 codes against q8_1
 // activations): exact int32.
@@ -92,6 +94,43 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
   int d;
   asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
+}
+
+// NVFP4: the exact sum over 16 elements of (twice the E2M1 value of the code) times
+// the int8 activation.  Codes c0 (elements 0..7) and c1 (8..15), one nibble each in
+// element order; x: the 16 activation bytes.  prmt looks up each nibble of its
+// 16-bit selector in the 8 bytes {kLo, kHi} (twice the magnitudes 0, .5, 1, 1.5, 2,
+// 3, 4, 6); a nibble with bit 3 set (a negative code) takes the sign-replicated
+// byte instead, 0 for these bytes.  So the lookup of the codes gives the magnitudes
+// of the positive codes, that of the codes with every sign flipped the magnitudes of
+// the negative ones, and the sum is the difference of their two dp4a sums.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ int nv4_dot16(uint32_t c0, uint32_t c1, const uint4& x) {
+  constexpr uint32_t kLo = 0x03020100u, kHi = 0x0C080604u;
+  const uint32_t n0 = c0 ^ 0x88888888u;
+  const uint32_t n1 = c1 ^ 0x88888888u;
+  int p = __dp4a((int)prmt(kLo, kHi, c0), (int)x.x, 0);
+  int q = __dp4a((int)prmt(kLo, kHi, n0), (int)x.x, 0);
+  p = __dp4a((int)prmt(kLo, kHi, c0 >> 16), (int)x.y, p);
+  q = __dp4a((int)prmt(kLo, kHi, n0 >> 16), (int)x.y, q);
+  p = __dp4a((int)prmt(kLo, kHi, c1), (int)x.z, p);
+  q = __dp4a((int)prmt(kLo, kHi, n1), (int)x.z, q);
+  p = __dp4a((int)prmt(kLo, kHi, c1 >> 16), (int)x.w, p);
+  q = __dp4a((int)prmt(kLo, kHi, n1 >> 16), (int)x.w, q);
+  return p - q;
+}
+
+// The two E4M3 scales of a 32-element block (low byte: elements 0..15), exactly.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t bits) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(bits));
+  return make_float2(__half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu))),
+                     __half2float(__ushort_as_half((uint16_t)(h2 >> 16))));
 }
 
 // ----------------------------------------------------------------------------
@@ -120,6 +159,8 @@ struct Params {
   // Routed slots that share one activation row (xpe): slot k reads row k / xdiv.  A
   // batch of tokens routes top_k slots each and shares each token's row among them.
   int xdiv;
+  // NVFP4: half the tensor scale (the block sums use twice the E2M1 values).
+  float gscale;
   // Slots of a batched routed product (> 0): the grid gives every slot the same
   // number of CTAs at the same row offsets, so that slots routed to the same expert
   // stream its rows at the same time and the repeats are served from L2.
@@ -382,6 +423,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
           const int n = mt.r0 + r;
           yacc[n] = __fadd_rn(yacc[n], __fmul_rn(s_gate[g.k], tot));
         } else {
+          if (FMT == kNv4) tot = __fmul_rn(p.gscale, tot);
           p.y[(int64_t)m * p.units + g.out0 + mt.r0 + r] = tot;
         }
       }
@@ -545,7 +587,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     }
     // Bytes of one block and of one 32-block part in the ring's quant rows.
-    constexpr int kBlockBytes = FMT == kQ4 ? 16 : 32;
+    constexpr int kBlockBytes = FMT == kQ8 ? 32 : 16;
     constexpr int kPartBytes = 32 * kBlockBytes;
     const int Qrow = (int)p.qrow;
     // Q4_0 nibble masks and shifts of this lane (see the block dot below).
@@ -590,7 +632,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         for (int r = 0; r < R; ++r) {
           // Rows past the stage's end reuse a valid row; their sums are dropped.
           const int row = rbase + r < nr ? rbase + r : rbase;
-          wl[r] = ws + row * Qrow + (plo * 32 + lane) * kBlockBytes + (FMT == kQ4 ? 0 : h1 * 16);
+          wl[r] = ws + row * Qrow + (plo * 32 + lane) * kBlockBytes + (FMT == kQ8 ? h1 * 16 : 0);
           dl[r] = ds + row * nb + plo * 32 + lane;
         }
         const int8_t* xl = xs + (size_t)xrow * Ki + (plo * 32 + lane) * 32 + h1 * 16;
@@ -640,6 +682,19 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
                   b = dp4a_us(c.w & q4m1, (int)x1.w, b);
                   const int dot = (a >> q4s0) + (b >> (4 - q4s0));
                   acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, dot - 8 * sx);
+                }
+              } else if (FMT == kNv4) {
+                // Code bytes 0..7 are the block's elements 0..15 (first E4M3 scale),
+                // bytes 8..15 elements 16..31; x0 holds elements 16*h1 .., x1 the rest.
+                // Each half's exact sum, then the two terms in element order.
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                  const uint4 c = w0[r];
+                  const int sa = nv4_dot16(h1 ? c.z : c.x, h1 ? c.w : c.y, x0);
+                  const int sb = nv4_dot16(h1 ? c.x : c.z, h1 ? c.y : c.w, x1);
+                  const float2 sc = e4m3x2_to_float2(dw[r]);
+                  acc[r][m] = __fmaf_rn(__fmul_rn(sc.x, dx), (float)(h1 ? sb : sa), acc[r][m]);
+                  acc[r][m] = __fmaf_rn(__fmul_rn(sc.y, dx), (float)(h1 ? sa : sb), acc[r][m]);
                 }
               } else {
 #pragma unroll
@@ -1147,7 +1202,7 @@ template <int M, int R, int MODE, int XIN, int FMT = kQ8>
 memra_status run_product(Params p, cudaStream_t stream) {
   DeviceInfo info;
   if (!device_info(&info)) return MEMRA_ERR_CUDA;
-  p.qrow = FMT == kQ4 ? p.K / 2 : p.K;
+  p.qrow = FMT == kQ8 ? p.K : p.K / 2;
   p.nb = (int)(p.K / 32);
   p.cpr = (p.nb + 31) / 32;
   p.S = slices_for(p.cpr);
@@ -1168,7 +1223,7 @@ memra_status run_product(Params p, cudaStream_t stream) {
     return launch(q8_tma_kernel<M, R, MODE, XIN, FMT>, grid, tma_threads(M), smem, stream, info,
                   p);
   }
-  if (FMT == kQ4) return MEMRA_ERR_UNSUPPORTED;  // Q4_0 runs on the bulk-copy kernel only
+  if (FMT != kQ8) return MEMRA_ERR_UNSUPPORTED;  // 4-bit formats run on the bulk-copy kernel only
   grid = std::min<int64_t>(p.units, (int64_t)info.sms * reg_grid_ctas_per_sm(M));
   if (plan_reg<M, R, MODE, XIN>(p, info, grid, &smem))
     return launch(q8_reg_kernel<M, R, MODE, XIN>, grid, kRegThreads, smem, stream, info, p);
@@ -1181,16 +1236,17 @@ memra_status run_product(Params p, cudaStream_t stream) {
 // on the 64-layer sweep: 3.44 ms per token with 1-row tasks, 3.16 with 2, 3.32 with
 // 4).  M = 8 takes 2-row tasks too: with K = 17408 the activation planes and their
 // block sums leave room for 2-row stages only.
-memra_status dispatch_m_q4(const Params& p, int M, cudaStream_t s) {
+template <int FMT>
+memra_status dispatch_m_4bit(const Params& p, int M, cudaStream_t s) {
   switch (M) {
-    case 1: return run_product<1, 2, kDense, kXq8, kQ4>(p, s);
-    case 2: return run_product<2, 1, kDense, kXq8, kQ4>(p, s);
-    case 3: return run_product<3, 1, kDense, kXq8, kQ4>(p, s);
-    case 4: return run_product<4, 2, kDense, kXq8, kQ4>(p, s);
-    case 5: return run_product<5, 2, kDense, kXq8, kQ4>(p, s);
-    case 6: return run_product<6, 2, kDense, kXq8, kQ4>(p, s);
-    case 7: return run_product<7, 2, kDense, kXq8, kQ4>(p, s);
-    case 8: return run_product<8, 2, kDense, kXq8, kQ4>(p, s);
+    case 1: return run_product<1, 2, kDense, kXq8, FMT>(p, s);
+    case 2: return run_product<2, 1, kDense, kXq8, FMT>(p, s);
+    case 3: return run_product<3, 1, kDense, kXq8, FMT>(p, s);
+    case 4: return run_product<4, 2, kDense, kXq8, FMT>(p, s);
+    case 5: return run_product<5, 2, kDense, kXq8, FMT>(p, s);
+    case 6: return run_product<6, 2, kDense, kXq8, FMT>(p, s);
+    case 7: return run_product<7, 2, kDense, kXq8, FMT>(p, s);
+    case 8: return run_product<8, 2, kDense, kXq8, FMT>(p, s);
   }
   return MEMRA_ERR_UNSUPPORTED;
 }
@@ -1307,8 +1363,46 @@ extern "C" memra_status memra_q4_0_gemm_small_m(const uint8_t* wq4, const uint16
     p.xrows = (int)rows;
     p.y = y + m0 * N;
     p.units = N;
-    return dispatch_m_q4(p, (int)rows, stream);
+    return dispatch_m_4bit<kQ4>(p, (int)rows, stream);
   });
+}
+
+extern "C" memra_status memra_nvfp4_gemm_small_m(const uint8_t* codes, const uint8_t* scales,
+                                                 float g, int64_t N, int64_t K, int64_t M,
+                                                 const int8_t* xq, const float* xd, float* y,
+                                                 cudaStream_t stream) {
+  if (N < 0 || K < 0 || M < 0 || K % 32 != 0) return MEMRA_ERR_INVALID_ARG;
+  if (M > MEMRA_MAX_M) return MEMRA_ERR_UNSUPPORTED;
+  if (N > INT32_MAX || K > INT32_MAX) return MEMRA_ERR_UNSUPPORTED;
+  if (N == 0 || M == 0) return MEMRA_OK;
+  if (!y) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(y, 4)) return MEMRA_ERR_ALIGNMENT;
+  if (K == 0) return zero_fill(y, M * N, stream);
+  if (!codes || !scales || !xq || !xd) return MEMRA_ERR_INVALID_ARG;
+  if (K % 256 != 0) return MEMRA_ERR_UNSUPPORTED;
+  if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(xq, 16) || !aligned(xd, 16))
+    return MEMRA_ERR_ALIGNMENT;
+  if (!x_fits(pass_rows(M), K)) return MEMRA_ERR_UNSUPPORTED;
+  return in_passes(M, [&](int64_t m0, int64_t rows) {
+    Params p{};
+    p.wq = reinterpret_cast<const int8_t*>(codes);
+    p.wd = reinterpret_cast<const uint16_t*>(scales);
+    p.gscale = g * 0.5f;
+    p.N = N;
+    p.K = K;
+    p.xq = xq + m0 * K;
+    p.xd = xd + m0 * (K / 32);
+    p.xrows = (int)rows;
+    p.y = y + m0 * N;
+    p.units = N;
+    return dispatch_m_4bit<kNv4>(p, (int)rows, stream);
+  });
+}
+
+extern "C" memra_status memra_nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, float g,
+                                         int64_t N, int64_t K, const int8_t* xq, const float* xd,
+                                         float* y, cudaStream_t stream) {
+  return memra_nvfp4_gemm_small_m(codes, scales, g, N, K, 1, xq, xd, y, stream);
 }
 
 extern "C" memra_status memra_q4_0_gemv(const uint8_t* wq4, const uint16_t* wd, int64_t N, int64_t K,

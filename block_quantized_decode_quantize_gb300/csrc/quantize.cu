@@ -237,6 +237,89 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
+// ---------------------------------------------------------------------------
+// NVFP4 weight ingest: per-tensor fp32 scale g = amax / (6 * 448), per 16-block
+// FP8 E4M3 scale s = e4m3(amax_block / (6 g)), FP4 E2M1 codes of w / (s g), all
+// rounded to nearest even with saturation; element 2j in the low nibble of byte j.
+// Three launches: the tensor's amax (as fp32 bits, atomicMax: non-negative floats
+// order as their bit patterns), the blocks, then g.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3_rn_satfinite(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return r & 0xFFu;  // the second source lands in the low byte
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)b));
+  return __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu)));
+}
+
+// E2M1 code of v: the sign bit of v, and the magnitude code of the nearest grid value
+// (0, .5, 1, 1.5, 2, 3, 4, 6) with ties to the even mantissa, saturating at 6.  The
+// thresholds are the midpoints; a midpoint goes to the neighbour with mantissa 0.
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  const float a = fabsf(v);
+  const uint32_t m = a <= 0.25f ? 0u : a < 0.75f ? 1u : a <= 1.25f ? 2u : a < 1.75f ? 3u
+                   : a <= 2.5f  ? 4u : a < 3.5f  ? 5u : a <= 5.0f  ? 6u : 7u;
+  return (__float_as_uint(v) >> 31) << 3 | m;
+}
+
+__global__ void __launch_bounds__(kQuantThreads)
+    amax_kernel(const float4* __restrict__ w, int64_t n4, unsigned int* __restrict__ amax_bits) {
+  pdl_wait();
+  float m = 0.0f;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = w[i];
+    m = fmaxf(fmaxf(m, fabsf(v.x)), fmaxf(fabsf(v.y), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_nvfp4_kernel(const float4* __restrict__ w, int64_t nblk,
+                          const unsigned int* __restrict__ amax_bits, uint2* __restrict__ codes,
+                          uint8_t* __restrict__ scales) {
+  pdl_wait();
+  const float g = __fdiv_rn(__uint_as_float(__ldcg(amax_bits)), 2688.0f);
+  const float g6 = __fmul_rn(6.0f, g);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblk;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 t = w[i * 4 + q];
+      v[4 * q] = t.x;
+      v[4 * q + 1] = t.y;
+      v[4 * q + 2] = t.z;
+      v[4 * q + 3] = t.w;
+    }
+    float bmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(v[j]));
+    const uint32_t sc = g == 0.0f ? 0u : e4m3_rn_satfinite(__fdiv_rn(bmax, g6));
+    const float denom = __fmul_rn(e4m3_value(sc), g);
+    uint32_t lo = 0, hi = 0;
+    if (denom != 0.0f) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) lo |= e2m1_code(__fdiv_rn(v[j], denom)) << (4 * j);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) hi |= e2m1_code(__fdiv_rn(v[8 + j], denom)) << (4 * j);
+    }
+    codes[i] = make_uint2(lo, hi);
+    scales[i] = (uint8_t)sc;
+  }
+}
+
+__global__ void nvfp4_scale_kernel(float* __restrict__ g) {
+  pdl_wait();
+  *g = __fdiv_rn(__uint_as_float(*reinterpret_cast<const unsigned int*>(g)), 2688.0f);
+}
+
 int quant_grid(int64_t groups, const DeviceInfo& info) {
   const int64_t warps = (groups + 31) / 32;
   const int64_t blocks = (warps * 32 + kQuantThreads - 1) / kQuantThreads;
@@ -275,6 +358,34 @@ extern "C" memra_status memra_quantize_q4_0(const float* w, int64_t N, int64_t K
   const int64_t groups = N * K / 8;
   cudaError_t e = launch_kernel(quantize_q4_0_kernel, dim3(quant_grid(groups, info)),
                                 dim3(kQuantThreads), 0, stream, w, groups, wq4, wd);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MEMRA_OK;
+}
+
+extern "C" memra_status memra_quantize_nvfp4(const float* w, int64_t N, int64_t K,
+                                             uint8_t* codes, uint8_t* scales, float* g,
+                                             cudaStream_t stream) {
+  if (N < 0 || K < 0 || K % 32 != 0) return MEMRA_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return MEMRA_OK;
+  if (!w || !codes || !scales || !g) return MEMRA_ERR_INVALID_ARG;
+  if (N > INT64_MAX / K) return MEMRA_ERR_UNSUPPORTED;
+  if (!aligned(w, 16) || !aligned(codes, 8) || !aligned(g, 4)) return MEMRA_ERR_ALIGNMENT;
+  DeviceInfo info;
+  if (!device_info(&info)) return MEMRA_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned int* amax_bits = reinterpret_cast<unsigned int*>(g);
+  const int64_t n4 = N * K / 4;
+  e = launch_kernel(amax_kernel, dim3(quant_grid(n4, info)), dim3(kQuantThreads), 0, stream,
+                    reinterpret_cast<const float4*>(w), n4, amax_bits);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int64_t nblk = N * K / 16;
+  e = launch_kernel(quantize_nvfp4_kernel, dim3(quant_grid(nblk, info)), dim3(kQuantThreads), 0,
+                    stream, reinterpret_cast<const float4*>(w), nblk,
+                    static_cast<const unsigned int*>(amax_bits), reinterpret_cast<uint2*>(codes),
+                    scales);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch_kernel(nvfp4_scale_kernel, dim3(1), dim3(1), 0, stream, g);
   if (e != cudaSuccess) return cuda_fail(e);
   return MEMRA_OK;
 }

@@ -132,6 +132,43 @@ memra_status memra_quantize_q4_0(const float* w, int64_t N, int64_t K, uint8_t* 
                                  cudaStream_t stream);
 
 /*
+ * NVFP4 weights, the pages' third split-plane decode format (memra wiki, feature
+ * list; their safetensors loader reads NVIDIA ModelOpt NVFP4 checkpoints byte for
+ * byte).  The pages print nothing of it; this library's reading is ModelOpt's NVFP4:
+ * 16 consecutive weights of a row share one FP8 E4M3 scale s, each weight is an FP4
+ * E2M1 code e (magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 and a sign), and the tensor has
+ * one fp32 scale g: w ~= g * s * e.
+ *   Planes: codes uint8 [N][K/2], byte j holding element 2j in its low nibble and
+ *   element 2j+1 in its high nibble; scales E4M3 bits uint8 [N][K/16].
+ *   Quantisation: g = amax|W| / (6 * 448); s = e4m3(amax_block / (6 g)); e =
+ *   e2m1(w / (float(s) g)), a block with s == 0 gets code 0; every conversion rounds
+ *   to nearest, ties to even, saturating at 448 and 6; the code's sign is w's sign bit.
+ * memra_quantize_nvfp4 writes g to device memory (*g, fp32); w 16-byte aligned,
+ * codes 8-byte aligned.  It makes three launches and uses *g as its amax scratch.
+ */
+memra_status memra_quantize_nvfp4(const float* w, int64_t N, int64_t K, uint8_t* codes,
+                                  uint8_t* scales, float* g, cudaStream_t stream);
+
+/*
+ * NVFP4 x q8_1 products (W4A8: every block sum exact in int32):
+ *   y[m][n] = (g / 2) * sum_b [ (s_lo d_x[m][b]) S_lo + (s_hi d_x[m][b]) S_hi ],
+ * S_lo, S_hi the sums of (twice the E2M1 value) * xq over elements 0..15 and 16..31
+ * of activation block b, s_lo, s_hi their two E4M3 scales; the fp32 terms accumulate
+ * in this library's one summation order, so a row does not depend on M.  g is the
+ * tensor scale (host value).  M in [0, 16] (passes as memra_q8_0_gemm_small_m).  K a
+ * multiple of 256 (MEMRA_ERR_UNSUPPORTED otherwise); codes, scales, xq, xd 16-byte
+ * aligned.
+ */
+memra_status memra_nvfp4_gemm_small_m(const uint8_t* codes, const uint8_t* scales, float g,
+                                      int64_t N, int64_t K, int64_t M, const int8_t* xq,
+                                      const float* xd, float* y, cudaStream_t stream);
+
+/* The decode GEMV on NVFP4 weights: memra_nvfp4_gemm_small_m with M = 1, y fp32 [N]. */
+memra_status memra_nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, float g, int64_t N,
+                              int64_t K, const int8_t* xq, const float* xd, float* y,
+                              cudaStream_t stream);
+
+/*
  * Repack from GGUF's interleaved block arrays into the split planes (memra wiki,
  * feature list: decode runs on split-plane repacked weights).  The pages print no
  * block layout; the reading is GGUF's:

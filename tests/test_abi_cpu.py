@@ -117,6 +117,24 @@ def test_repack_argument_errors(L):
         assert f(None, 4, 0, None, None, None) == 0
 
 
+def test_nvfp4_argument_errors(L):
+    f = L.memra_nvfp4_gemm_small_m
+    assert f(A256, A256, 1.0, 64, 48, 1, A256, A256, A256, None) == 1     # K % 32 != 0
+    assert f(A256, A256, 1.0, 64, 256, 17, A256, A256, A256, None) == 3   # M > 16
+    assert f(A256, A256, 1.0, 64, 96, 1, A256, A256, A256, None) == 3     # K % 256 != 0
+    assert f(A256 + 8, A256, 1.0, 64, 256, 1, A256, A256, A256, None) == 2  # codes
+    assert f(A256, A256 + 8, 1.0, 64, 256, 1, A256, A256, A256, None) == 2  # scales
+    assert f(None, A256, 1.0, 64, 256, 1, A256, A256, A256, None) == 1
+    assert f(None, None, 1.0, 0, 256, 1, None, None, None, None) == 0      # empty
+    assert L.memra_nvfp4_gemv(A256, A256, 1.0, 64, 33, A256, A256, A256, None) == 1
+    q = L.memra_quantize_nvfp4
+    assert q(A256, 4, 48, A256, A256, A256, None) == 1                     # K % 32
+    assert q(A256, 4, 64, A256, A256, None, None) == 1                     # no g
+    assert q(A256 + 4, 4, 64, A256, A256, A256, None) == 2                 # w alignment
+    assert q(A256, 4, 64, A256 + 4, A256, A256, None) == 2                 # codes alignment
+    assert q(None, 0, 64, None, None, None, None) == 0
+
+
 def test_moe_tokens_argument_errors(L):
     g = L.memra_q8_0_moe_gemv_tokens
 
