@@ -17,7 +17,7 @@ peak; ``cpu_baseline`` is the CPU oracle on the host cores over a bounded sample
                   [--workload dense27b_sweep|gemv_4096|verify_m2|verify_m4|verify_m8|
                               batch_m16|moe_top8|stress_lm_head|dense27b_sweep_q4_0|
                               dense27b_sweep_nvfp4|
-                              moe_top8_q4_0|moe_top8_tokens8]
+                              moe_top8_q4_0|moe_top8_nvfp4|moe_top8_tokens8]
 """
 import argparse
 import hashlib
@@ -43,7 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8", "batch_m16",
              "moe_top8",
              "stress_lm_head", "dense27b_sweep_q4_0", "dense27b_sweep_nvfp4", "moe_top8_q4_0",
-             "moe_top8_tokens8")
+             "moe_top8_nvfp4", "moe_top8_tokens8")
 
 
 # ----------------------------------------------------------------------------
@@ -153,11 +153,16 @@ class MoeLayer:
         E, H, F, k = c["experts"], c["hidden"], c["ffn"], c["top_k"]
         self.fmt = fmt
         self.tokens = tokens
-        kdiv = 2 if fmt == "q4_0" else 1  # quant bytes per weight: 1/2 for Q4_0
-        gq, gd = quantized_weights(mem, E * 2 * F, H, 3, layer, 0, device=device, fmt=fmt)
-        dq, dd = quantized_weights(mem, E * H, F, 3, layer, 1, device=device, fmt=fmt)
-        self.gq, self.gd = gq.view(E, 2 * F, H // kdiv), gd.view(E, 2 * F, H // 32)
-        self.dq, self.dd = dq.view(E, H, F // kdiv), dd.view(E, H, F // 32)
+        kdiv = 1 if fmt == "q8_0" else 2  # quant bytes per weight: 1/2 for the 4-bit formats
+        qg = quantized_weights(mem, E * 2 * F, H, 3, layer, 0, device=device, fmt=fmt)
+        qd = quantized_weights(mem, E * H, F, 3, layer, 1, device=device, fmt=fmt)
+        sdiv = 16 if fmt == "nvfp4" else 32  # scale entries per row: one per 16 or per 32
+        self.gq, self.gd = qg[0].view(E, 2 * F, H // kdiv), qg[1].view(E, 2 * F, H // sdiv)
+        self.dq, self.dd = qd[0].view(E, H, F // kdiv), qd[1].view(E, H, F // sdiv)
+        if fmt == "nvfp4":
+            # each bank quantised as one tensor: every expert carries the bank's scale
+            self.ggu = torch.full((E,), qg[2], dtype=torch.float32, device=device)
+            self.gdn = torch.full((E,), qd[2], dtype=torch.float32, device=device)
         if tokens > 1:
             if fmt != "q8_0":
                 raise ValueError("the batched routed FFN takes Q8_0 banks")
@@ -173,8 +178,9 @@ class MoeLayer:
         self.y = torch.empty((H,), dtype=torch.float32, device=device)
         self.status = torch.zeros((1,), dtype=torch.int32, device=device)
         # the selected experts' quant and scale planes, read once per token
-        self.weight_bytes = k * (self.gq[0].numel() + self.gd[0].numel() * 2 +
-                                 self.dq[0].numel() + self.dd[0].numel() * 2)
+        es = self.gd.element_size()
+        self.weight_bytes = k * (self.gq[0].numel() + self.gd[0].numel() * es +
+                                 self.dq[0].numel() + self.dd[0].numel() * es)
 
     def _init_tokens(self, layer, device, E, H, F, k, T):
         routes = [synth.routing(E, k, 3, layer, 2, t, device=device) for t in range(T)]
@@ -198,7 +204,12 @@ class MoeLayer:
         self.weight_bytes = distinct * (self.gq[0].numel() + self.gd[0].numel() * 2 +
                                         self.dq[0].numel() + self.dd[0].numel() * 2)
 
-    def gemv(self, mem, *args, **kw):
+    def gemv(self, mem, bank, *args, **kw):
+        if self.fmt == "nvfp4":
+            scales = args[0]
+            gexp = self.ggu if bank is self.gq else self.gdn
+            return mem.memra_nvfp4_moe_gemv(bank, scales, gexp, *args[1:], **kw)
+        args = (bank,) + args
         if self.fmt == "q4_0":
             return mem.memra_q4_0_moe_gemv(*args, **kw)
         return mem.memra_q8_0_moe_gemv(*args, **kw)
@@ -297,9 +308,10 @@ class Workload:
             self.ops = build_gemv_4096(mem, device)
         elif name == "stress_lm_head":
             self.ops = build_stress(mem, device, M=1) + build_stress(mem, device, M=8)
-        elif name in ("moe_top8", "moe_top8_q4_0", "moe_top8_tokens8"):
+        elif name in ("moe_top8", "moe_top8_q4_0", "moe_top8_nvfp4", "moe_top8_tokens8"):
             n = synth.MOE["layers"] if layers is None else layers
-            fmt = "q4_0" if name.endswith("q4_0") else "q8_0"
+            fmt = ("q4_0" if name.endswith("q4_0") else
+                   "nvfp4" if name.endswith("nvfp4") else "q8_0")
             tokens = 8 if name.endswith("tokens8") else 1
             self.moe = [MoeLayer(mem, layer, device, fmt=fmt, tokens=tokens)
                         for layer in range(n)]
@@ -715,8 +727,8 @@ def run_memra(args):
                 "peak_kind": peak_kind + " copy bandwidth (MEASURED_PEAKS hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "kernel": "%s product kernel (%s, M=%s)" % (
-                    {"q4_0": "Q4_0", "nvfp4": "NVFP4"}.get(wl.ops[0].fmt, "Q8_0") if wl.ops
-                    else "Q8_0",
+                    {"q4_0": "Q4_0", "nvfp4": "NVFP4"}.get(
+                        wl.ops[0].fmt if wl.ops else wl.moe[0].fmt, "Q8_0"),
                     "chained, one launch per step" if wl.chain is not None else
                     "routed experts" if wl.moe is not None else
                     ("quantise fused" if wl.fused else "q8_1 input"),

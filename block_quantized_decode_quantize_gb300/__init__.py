@@ -55,6 +55,10 @@ _SIGS = {
     "memra_quantize_nvfp4": [_p, _i64, _i64, _p, _p, _p, _p],
     "memra_nvfp4_gemm_small_m": [_p, _p, ctypes.c_float, _i64, _i64, _i64, _p, _p, _p, _p],
     "memra_nvfp4_gemv": [_p, _p, ctypes.c_float, _i64, _i64, _p, _p, _p, _p],
+    "memra_nvfp4_moe_gemv": [_p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p,
+                             _p],
+    "memra_nvfp4_moe_gemv_tokens": [_p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _i64, _p, _p,
+                                    _i32, _p, _p, _p, _p],
     "memra_repack_q4_0": [_p, _i64, _i64, _p, _p, _p],
     "memra_q4_0_gemv": [_p, _p, _i64, _i64, _p, _p, _p, _p],
     "memra_q4_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
@@ -533,6 +537,76 @@ def memra_q8_0_moe_ffn_tokens(gu_q, gu_d, dn_q, dn_d, ids, gate_w, x, y=None, wo
                                                H, F, _ptr(ids), _ptr(gate_w), T, top_k, _ptr(x),
                                                dt, _ptr(y), _ptr(workspace), _ptr(dev_status),
                                                _stream(gu_q)))
+    return y
+
+
+def memra_nvfp4_moe_gemv(codes_bank, scales_bank, gexp, ids, gate_w, xq, xd, x_per_expert,
+                         y=None, dev_status=None):
+    """Routed experts on an NVFP4 bank: codes_bank uint8 [E, N, K/2], scales_bank uint8
+    E4M3 [E, N, K/16], gexp float32 [E] (each expert's tensor scale, on the device);
+    the rest as memra_q8_0_moe_gemv."""
+    _need(codes_bank, "codes_bank", torch.uint8)
+    E, N, K2 = codes_bank.shape
+    K = 2 * K2
+    dev = codes_bank.device
+    _need(scales_bank, "scales_bank", torch.uint8, dev, (E, N, K // 16))
+    _need(gexp, "gexp", torch.float32, dev, (E,))
+    _need(ids, "ids", torch.int32, dev)
+    top_k = ids.shape[0]
+    if gate_w is not None:
+        _need(gate_w, "gate_w", torch.float32, dev, (top_k,))
+    xpe = 1 if x_per_expert else 0
+    rows = (top_k,) if xpe else ()
+    _need(xq, "xq", torch.int8, dev, rows + (K,))
+    _need(xd, "xd", torch.float32, dev, rows + (K // 32,))
+    yshape = (N,) if gate_w is not None else (top_k, N)
+    if y is None:
+        y = torch.empty(yshape, dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, yshape)
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    with torch.cuda.device(dev):
+        _check("memra_nvfp4_moe_gemv",
+               lib().memra_nvfp4_moe_gemv(_ptr(codes_bank), _ptr(scales_bank), _ptr(gexp), E, N,
+                                          K, _ptr(ids), _ptr(gate_w), top_k, _ptr(xq), _ptr(xd),
+                                          xpe, _ptr(y), _ptr(dev_status), _stream(codes_bank)))
+    return y
+
+
+def memra_nvfp4_moe_gemv_tokens(codes_bank, scales_bank, gexp, ids, gate_w, xq, xd,
+                                x_per_expert, y=None, workspace=None, dev_status=None):
+    """memra_q8_0_moe_gemv_tokens on an NVFP4 bank (layout as memra_nvfp4_moe_gemv)."""
+    _need(codes_bank, "codes_bank", torch.uint8)
+    E, N, K2 = codes_bank.shape
+    K = 2 * K2
+    dev = codes_bank.device
+    _need(scales_bank, "scales_bank", torch.uint8, dev, (E, N, K // 16))
+    _need(gexp, "gexp", torch.float32, dev, (E,))
+    _need(ids, "ids", torch.int32, dev)
+    T, top_k = ids.shape
+    if gate_w is not None:
+        _need(gate_w, "gate_w", torch.float32, dev, (T, top_k))
+    xpe = 1 if x_per_expert else 0
+    rows = (T, top_k) if xpe else (T,)
+    _need(xq, "xq", torch.int8, dev, rows + (K,))
+    _need(xd, "xd", torch.float32, dev, rows + (K // 32,))
+    yshape = (T, N) if gate_w is not None else (T, top_k, N)
+    if y is None:
+        y = torch.empty(yshape, dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, yshape)
+    if gate_w is not None:
+        if workspace is None:
+            workspace = torch.empty((T, top_k, N), dtype=torch.float32, device=dev)
+        _need(workspace, "workspace", torch.float32, dev, (T, top_k, N))
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    with torch.cuda.device(dev):
+        _check("memra_nvfp4_moe_gemv_tokens",
+               lib().memra_nvfp4_moe_gemv_tokens(_ptr(codes_bank), _ptr(scales_bank), _ptr(gexp),
+                                                 E, N, K, _ptr(ids), _ptr(gate_w), T, top_k,
+                                                 _ptr(xq), _ptr(xd), xpe, _ptr(y),
+                                                 _ptr(workspace), _ptr(dev_status),
+                                                 _stream(codes_bank)))
     return y
 
 

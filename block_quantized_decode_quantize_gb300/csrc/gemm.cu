@@ -159,8 +159,10 @@ struct Params {
   // Routed slots that share one activation row (xpe): slot k reads row k / xdiv.  A
   // batch of tokens routes top_k slots each and shares each token's row among them.
   int xdiv;
-  // NVFP4: half the tensor scale (the block sums use twice the E2M1 values).
+  // NVFP4: half the tensor scale (the block sums use twice the E2M1 values); routed
+  // products take each expert's tensor scale from gexp[id] (fp32 [E], device).
   float gscale;
+  const float* gexp;
   // Slots of a batched routed product (> 0): the grid gives every slot the same
   // number of CTAs at the same row offsets, so that slots routed to the same expert
   // stream its rows at the same time and the repeats are served from L2.
@@ -278,7 +280,8 @@ constexpr int kOffAbort = 8 * 2 * kMaxStages;
 constexpr int kOffMeta = kOffAbort + 16;
 constexpr int kOffIds = kOffMeta + 16 * kMaxStages;
 constexpr int kOffGate = kOffIds + 4 * kMaxTopK;
-constexpr int kHeaderBytes = (kOffGate + 4 * kMaxTopK + 127) / 128 * 128;
+constexpr int kOffGsc = kOffGate + 4 * kMaxTopK;  // NVFP4 routed: half each slot's g
+constexpr int kHeaderBytes = (kOffGsc + 4 * kMaxTopK + 127) / 128 * 128;
 
 // What the producer put in a ring slot: rows [r0, r0 + nr) of segment `seg`, with
 // activation row `xrow`.  nr == 0 marks the end of the CTA's stages.  A packed stage
@@ -302,6 +305,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + kOffMeta);
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem + kOffIds);
   float* s_gate = reinterpret_cast<float*>(smem + kOffGate);
+  float* s_gsc = reinterpret_cast<float*>(smem + kOffGsc);
   int8_t* xs = reinterpret_cast<int8_t*>(smem + p.off_x);
   float* xds = reinterpret_cast<float*>(smem + p.off_xd);
   unsigned char* ring = smem + p.off_ring;
@@ -346,6 +350,9 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       // stale L1 line).
       if (!p.routing_ready) pdl_wait();
       load_routing<MODE>(p, s_ids, s_gate, lane, 32);
+      if (FMT == kNv4)  // the same lane wrote s_ids[k] just above
+        for (int k = lane; k < p.top_k; k += 32)
+          s_gsc[k] = s_ids[k] >= 0 ? __fmul_rn(0.5f, __ldcg(p.gexp + s_ids[k])) : 0.0f;
     }
     if (MODE == kMoeGated) {
       for (int64_t i = lane; i < u1 - u0; i += 32) yacc[i] = 0.0f;
@@ -406,6 +413,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
             const float* q = pp + (size_t)(k * n + i) * S;
             float tot = q[0];
             for (int s = 1; s < S; ++s) tot = __fadd_rn(tot, q[s]);
+            if (FMT == kNv4) tot = __fmul_rn(s_gsc[k], tot);
             acc = __fadd_rn(acc, __fmul_rn(s_gate[k], tot));
           }
           yacc[i] = acc;
@@ -419,11 +427,11 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         const int m = i - r * M;
         float tot = pp[((size_t)r * S) * M + m];
         for (int s = 1; s < S; ++s) tot = __fadd_rn(tot, pp[((size_t)r * S + s) * M + m]);
+        if (FMT == kNv4) tot = __fmul_rn(MODE == kDense ? p.gscale : s_gsc[g.k], tot);
         if (MODE == kMoeGated) {
           const int n = mt.r0 + r;
           yacc[n] = __fadd_rn(yacc[n], __fmul_rn(s_gate[g.k], tot));
         } else {
-          if (FMT == kNv4) tot = __fmul_rn(p.gscale, tot);
           p.y[(int64_t)m * p.units + g.out0 + mt.r0 + r] = tot;
         }
       }
@@ -1449,7 +1457,7 @@ template <int FMT>
 memra_status moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank, int64_t E, int64_t N,
                       int64_t K, const int32_t* ids, const float* gate_w, int64_t top_k,
                       const int8_t* xq, const float* xd, int32_t x_per_expert, float* y,
-                      int32_t* dev_status, cudaStream_t stream) {
+                      int32_t* dev_status, cudaStream_t stream, const float* gexp = nullptr) {
   if (E < 1 || N < 0 || K < 0 || K % 32 != 0 || top_k < 1) return MEMRA_ERR_INVALID_ARG;
   if (x_per_expert != 0 && x_per_expert != 1) return MEMRA_ERR_INVALID_ARG;
   if (top_k > MEMRA_MAX_TOP_K) return MEMRA_ERR_UNSUPPORTED;
@@ -1461,9 +1469,11 @@ memra_status moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank, int64_t E,
     return MEMRA_ERR_ALIGNMENT;
   if (K == 0) return zero_fill(y, gate_w ? N : top_k * N, stream);
   if (!wq_bank || !wd_bank || !xq || !xd) return MEMRA_ERR_INVALID_ARG;
-  if (FMT == kQ4) {
+  if (FMT != kQ8) {
+    if (FMT == kNv4 && !gexp) return MEMRA_ERR_INVALID_ARG;
     if (K % 256 != 0) return MEMRA_ERR_UNSUPPORTED;
-    if (!aligned(wq_bank, 16) || !aligned(wd_bank, 16) || !aligned(xq, 16) || !aligned(xd, 16))
+    if (!aligned(wq_bank, 16) || !aligned(wd_bank, 16) || !aligned(xq, 16) || !aligned(xd, 16) ||
+        (gexp && !aligned(gexp, 4)))
       return MEMRA_ERR_ALIGNMENT;
   } else if (!aligned(wq_bank, 32) || !aligned(wd_bank, 2) || !aligned(xq, 16) ||
              !aligned(xd, 4)) {
@@ -1486,6 +1496,7 @@ memra_status moe_gemv(const int8_t* wq_bank, const uint16_t* wd_bank, int64_t E,
   p.E = E;
   p.xpe = x_per_expert;
   p.status = dev_status;
+  p.gexp = gexp;
   if (gate_w) {
     p.units = N;
     return run_product<1, 1, kMoeGated, kXq8, FMT>(p, stream);
@@ -1513,7 +1524,8 @@ memra_status moe_gemv_tokens(const int8_t* wq_bank, const uint16_t* wd_bank, int
                              int64_t N, int64_t K, const int32_t* ids, const float* gate_w,
                              int64_t T, int64_t top_k, const int8_t* xq, const float* xd,
                              int32_t x_per_expert, float* y, float* workspace,
-                             int32_t* dev_status, cudaStream_t stream) {
+                             int32_t* dev_status, cudaStream_t stream,
+                             const float* gexp = nullptr) {
   if (E < 1 || N < 0 || K < 0 || K % 32 != 0 || top_k < 1 || T < 0) return MEMRA_ERR_INVALID_ARG;
   if (x_per_expert != 0 && x_per_expert != 1) return MEMRA_ERR_INVALID_ARG;
   if (top_k > MEMRA_MAX_TOP_K || T > MEMRA_MAX_PAIRS || T * top_k > MEMRA_MAX_PAIRS)
@@ -1527,9 +1539,11 @@ memra_status moe_gemv_tokens(const int8_t* wq_bank, const uint16_t* wd_bank, int
   const int64_t P = T * top_k;
   if (K == 0) return zero_fill(y, gate_w ? T * N : P * N, stream);
   if (!wq_bank || !wd_bank || !xq || !xd) return MEMRA_ERR_INVALID_ARG;
-  if (FMT == kQ4) {
+  if (FMT != kQ8) {
+    if (FMT == kNv4 && !gexp) return MEMRA_ERR_INVALID_ARG;
     if (K % 256 != 0) return MEMRA_ERR_UNSUPPORTED;
-    if (!aligned(wq_bank, 16) || !aligned(wd_bank, 16) || !aligned(xq, 16) || !aligned(xd, 16))
+    if (!aligned(wq_bank, 16) || !aligned(wd_bank, 16) || !aligned(xq, 16) || !aligned(xd, 16) ||
+        (gexp && !aligned(gexp, 4)))
       return MEMRA_ERR_ALIGNMENT;
   } else if (!aligned(wq_bank, 32) || !aligned(wd_bank, 2) || !aligned(xq, 16) ||
              !aligned(xd, 4)) {
@@ -1553,6 +1567,7 @@ memra_status moe_gemv_tokens(const int8_t* wq_bank, const uint16_t* wd_bank, int
   p.xdiv = x_per_expert ? 1 : (int)top_k;
   p.lockstep = (int)P;
   p.status = dev_status;
+  p.gexp = gexp;
   p.units = P * N;
   const memra_status st = run_product<1, 1, kMoeUngated, kXq8, FMT>(p, stream);
   if (st != MEMRA_OK || !gate_w) return st;
@@ -1577,6 +1592,33 @@ extern "C" memra_status memra_q4_0_moe_gemv(const uint8_t* wq4_bank, const uint1
                                             int32_t* dev_status, cudaStream_t stream) {
   return moe_gemv<kQ4>(reinterpret_cast<const int8_t*>(wq4_bank), wd_bank, E, N, K, ids, gate_w,
                        top_k, xq, xd, x_per_expert, y, dev_status, stream);
+}
+
+extern "C" memra_status memra_nvfp4_moe_gemv(const uint8_t* codes_bank,
+                                             const uint8_t* scales_bank, const float* gexp,
+                                             int64_t E, int64_t N, int64_t K, const int32_t* ids,
+                                             const float* gate_w, int64_t top_k,
+                                             const int8_t* xq, const float* xd,
+                                             int32_t x_per_expert, float* y, int32_t* dev_status,
+                                             cudaStream_t stream) {
+  return moe_gemv<kNv4>(reinterpret_cast<const int8_t*>(codes_bank),
+                        reinterpret_cast<const uint16_t*>(scales_bank), E, N, K, ids, gate_w,
+                        top_k, xq, xd, x_per_expert, y, dev_status, stream, gexp);
+}
+
+extern "C" memra_status memra_nvfp4_moe_gemv_tokens(const uint8_t* codes_bank,
+                                                    const uint8_t* scales_bank,
+                                                    const float* gexp, int64_t E, int64_t N,
+                                                    int64_t K, const int32_t* ids,
+                                                    const float* gate_w, int64_t T,
+                                                    int64_t top_k, const int8_t* xq,
+                                                    const float* xd, int32_t x_per_expert,
+                                                    float* y, float* workspace,
+                                                    int32_t* dev_status, cudaStream_t stream) {
+  return moe_gemv_tokens<kNv4>(reinterpret_cast<const int8_t*>(codes_bank),
+                               reinterpret_cast<const uint16_t*>(scales_bank), E, N, K, ids,
+                               gate_w, T, top_k, xq, xd, x_per_expert, y, workspace, dev_status,
+                               stream, gexp);
 }
 
 extern "C" memra_status memra_q8_0_moe_gemv_tokens(const int8_t* wq_bank, const uint16_t* wd_bank,

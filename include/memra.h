@@ -371,6 +371,28 @@ memra_status memra_q4_0_moe_gemv_tokens(const uint8_t* wq4_bank, const uint16_t*
                                         cudaStream_t stream);
 
 /*
+ * Routed experts on an NVFP4 bank: codes_bank uint8 [E][N][K/2] and scales_bank E4M3
+ * bits [E][N][K/16] as memra_quantize_nvfp4 lays out one matrix, and gexp: fp32 [E]
+ * (device), each expert's tensor scale (ModelOpt stores one per expert).  Slot k's
+ * output is expert ids[k]'s memra_nvfp4_gemv result, bit for bit; the rest (gated
+ * sum, ids, outputs, dev_status) as memra_q8_0_moe_gemv.  K a multiple of 256;
+ * banks, xq, xd 16-byte aligned, gexp 4-byte aligned.
+ */
+memra_status memra_nvfp4_moe_gemv(const uint8_t* codes_bank, const uint8_t* scales_bank,
+                                  const float* gexp, int64_t E, int64_t N, int64_t K,
+                                  const int32_t* ids, const float* gate_w, int64_t top_k,
+                                  const int8_t* xq, const float* xd, int32_t x_per_expert,
+                                  float* y, int32_t* dev_status, cudaStream_t stream);
+
+/* memra_q8_0_moe_gemv_tokens on an NVFP4 bank (layout as memra_nvfp4_moe_gemv). */
+memra_status memra_nvfp4_moe_gemv_tokens(const uint8_t* codes_bank, const uint8_t* scales_bank,
+                                         const float* gexp, int64_t E, int64_t N, int64_t K,
+                                         const int32_t* ids, const float* gate_w, int64_t T,
+                                         int64_t top_k, const int8_t* xq, const float* xd,
+                                         int32_t x_per_expert, float* y, float* workspace,
+                                         int32_t* dev_status, cudaStream_t stream);
+
+/*
  * memra_q8_0_moe_ffn for a batch of T tokens, in three kernels: gate|up of every
  * (token, slot) pair with each token's row quantised in the prologue, down of every
  * pair with its SwiGLU + q8_1 in the prologue, and the gated sum per token.

@@ -342,6 +342,33 @@ def moe_ffn(x, gu_q, gu_d, dn_q, dn_d, ids, gate_w):
     return y, bad
 
 
+def moe_gemv_nvfp4(codes_bank, scales_bank, gexp, ids, gate_w, xq, xd, x_per_expert):
+    """Routed experts on an NVFP4 bank, composed from gemm_nvfp4: slot k is expert ids[k]'s
+    product with its own tensor scale gexp[ids[k]]; gated: y = sum over valid k, in
+    ascending k, of gate_w[k] * y_k, from 0 with one fp32 rounding per multiply and add.
+    Returns (y, n_bad)."""
+    ids = np.asarray(ids)
+    E, N = codes_bank.shape[0], codes_bank.shape[1]
+    xq = np.asarray(xq)
+    xd = np.asarray(xd)
+    ys, bad = [], 0
+    for k, e in enumerate(ids):
+        if e < 0 or e >= E:
+            bad += 1
+            ys.append(np.zeros(N, np.float32))
+            continue
+        xk = (xq[k], xd[k]) if x_per_expert else (xq.reshape(-1), xd.reshape(-1))
+        ys.append(gemm_nvfp4(codes_bank[e], scales_bank[e], gexp[e], xk[0][None],
+                             xk[1][None])[0])
+    if gate_w is None:
+        return np.stack(ys), bad
+    acc = np.zeros(N, np.float32)
+    for k, e in enumerate(ids):
+        if 0 <= e < E:
+            acc = (acc + np.float32(gate_w[k]) * ys[k]).astype(np.float32)
+    return acc, bad
+
+
 def moe_gemv_tokens(wq_bank, wd_bank, ids, gate_w, xq, xd, x_per_expert):
     """Routed experts for a batch of tokens: each token's routed product on its own (the
     pages' batching changes which weights are read together, not what a token gets).

@@ -127,3 +127,71 @@ def test_nvfp4_rejects_k_not_multiple_of_256(mem):
     with pytest.raises(mem.MemraError) as e:
         mem.memra_nvfp4_gemm_small_m(codes, scales, 1.0, xq, xd)
     assert e.value.status == 3
+
+
+def nvfp4_bank(mem, E, N, K, seed):
+    """Each expert quantised on its own (its own tensor scale), stacked into a bank."""
+    parts = [mem.memra_quantize_nvfp4(synth.weights_fp32(N, K, seed, e, std=0.01 * (1 + e % 3))
+                                      .cuda()) for e in range(E)]
+    codes = torch.stack([c for c, _, _ in parts])
+    scales = torch.stack([s for _, s, _ in parts])
+    gexp = torch.cat([g for _, _, g in parts])
+    return codes, scales, gexp
+
+
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("per_expert", [False, True])
+def test_nvfp4_moe_gemv_parity(mem, orc, gated, per_expert):
+    E, N, K, top_k = 10, 200, 1024, 8
+    codes, scales, gexp = nvfp4_bank(mem, E, N, K, 610)
+    ids = torch.tensor([3, 9, 0, 7, 3, 5, 12, 1], dtype=torch.int32)   # 12 is out of range
+    gw = torch.tensor([0.2, 0.15, 0.1, 0.1, 0.15, 0.1, 0.1, 0.1], dtype=torch.float32)
+    x = synth.activations_bf16(top_k if per_expert else 1, K, 611)
+    xq, xd = mem.memra_quantize_q8_1(x.cuda())
+    xq_in, xd_in = (xq, xd) if per_expert else (xq[0], xd[0])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = mem.memra_nvfp4_moe_gemv(codes, scales, gexp, ids.cuda(), gw.cuda() if gated else None,
+                                 xq_in, xd_in, per_expert, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 1
+    g_np = np_(gexp)
+    if not gated:
+        for k, e in enumerate(ids.tolist()):
+            if e >= E:
+                assert not y[k].any()
+                continue
+            one = mem.memra_nvfp4_gemv(codes[e], scales[e], float(g_np[e]),
+                                       xq[k if per_expert else 0], xd[k if per_expert else 0])
+            torch.cuda.synchronize()
+            assert torch.equal(one.view(torch.int32), y[k].view(torch.int32)), k
+    oxq, oxd = np_(xq), np_(xd)
+    y_ref, bad = orc.moe_gemv_nvfp4(np_(codes), np_(scales), g_np, np_(ids),
+                                    np_(gw) if gated else None, oxq if per_expert else oxq[0],
+                                    oxd if per_expert else oxd[0], int(per_expert))
+    assert bad == 1
+    terms = np.stack([nvfp4_terms(orc, np_(codes)[e], np_(scales)[e], g_np[e],
+                                  oxq[k:k + 1] if per_expert else oxq[:1],
+                                  oxd[k:k + 1] if per_expert else oxd[:1])[0]
+                      if e < E else np.zeros(N) for k, e in enumerate(ids.tolist())])
+    if gated:
+        assert_within(np_(y), y_ref, (np_(gw)[:, None] * terms).sum(axis=0), "nvfp4 moe gated")
+    else:
+        assert_within(np_(y), y_ref, terms, "nvfp4 moe")
+
+
+def test_nvfp4_moe_gemv_tokens_matches_single_token(mem):
+    E, N, K, top_k, T = 12, 160, 2048, 8, 5
+    codes, scales, gexp = nvfp4_bank(mem, E, N, K, 620)
+    ids = torch.stack([synth.routing(E, top_k, 621, t)[0] for t in range(T)])
+    gw = torch.stack([synth.routing(E, top_k, 621, t)[1] for t in range(T)])
+    x = synth.activations_bf16(T, K, 622)
+    xq, xd = mem.memra_quantize_q8_1(x.cuda())
+    for gated in (False, True):
+        g = gw.cuda() if gated else None
+        y = mem.memra_nvfp4_moe_gemv_tokens(codes, scales, gexp, ids.cuda(), g, xq, xd, False)
+        torch.cuda.synchronize()
+        for t in range(T):
+            one = mem.memra_nvfp4_moe_gemv(codes, scales, gexp, ids[t].cuda(),
+                                           g[t] if gated else None, xq[t], xd[t], False)
+            torch.cuda.synchronize()
+            assert torch.equal(one.view(torch.int32), y[t].view(torch.int32)), (gated, t)

@@ -804,3 +804,27 @@ def test_nvfp4_gemm_one_hot_activation_exact(orc):
     s = orc.e4m3_to_f32(scales[:, j // 16])
     want = (np.float32(g) * np.float32(0.5)) * ((s * np.float32(1.0)) * (c2 * np.float32(127)))
     assert np.array_equal(y, want.astype(np.float32))
+
+
+def test_moe_gemv_nvfp4_reduces_to_the_dense_product(orc):
+    E, N, K = 4, 12, 256
+    r = rng(88)
+    banks = [orc.quantize_nvfp4((r.standard_normal((N, K)) * (0.01 * (e + 1))).astype(np.float32))
+             for e in range(E)]
+    codes = np.stack([b[0] for b in banks])
+    scales = np.stack([b[1] for b in banks])
+    gexp = np.array([b[2] for b in banks], np.float32)
+    assert len(set(gexp.tolist())) == E                 # each expert its own tensor scale
+    xq, xd = orc.quantize_q8_1(r.standard_normal((1, K)).astype(np.float32))
+    ids = np.array([2, 0, 9, 3], np.int32)
+    y, bad = orc.moe_gemv_nvfp4(codes, scales, gexp, ids, None, xq, xd, 0)
+    assert bad == 1 and not y[2].any()
+    for k, e in ((0, 2), (1, 0), (3, 3)):
+        assert np.array_equal(y[k], orc.gemm_nvfp4(codes[e], scales[e], gexp[e], xq, xd)[0])
+    y1, _ = orc.moe_gemv_nvfp4(codes, scales, gexp, ids[:1], np.ones(1, np.float32), xq, xd, 0)
+    assert np.array_equal(y1, y[0])
+    gw = np.array([0.5, 0.25, 0.75, 0.25], np.float32)
+    yg, _ = orc.moe_gemv_nvfp4(codes, scales, gexp, ids, gw, xq, xd, 0)
+    ref = sum(float(gw[k]) * orc.nvfp4_dequant_gemm_f64(codes[e], scales[e], gexp[e], xq, xd)[0]
+              for k, e in ((0, 2), (1, 0), (3, 3)))
+    assert np.allclose(yg, ref, rtol=1e-5, atol=1e-7 * np.abs(ref).max())
