@@ -195,7 +195,9 @@ memra_status memra_repack_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t
  * bit for bit).  M in [0, 16], in passes as for memra_q8_0_gemm_small_m; xq [M][K],
  * xd [M][K/32], y fp32 [M][N].
  * K must be a multiple of 256 (MEMRA_ERR_UNSUPPORTED otherwise); wq4, wd, xq and xd
- * 16-byte aligned.
+ * 16-byte aligned.  The 4-bit formats stream through shared memory only: a pass whose
+ * activation rows and two weight rows do not fit a CTA's shared memory (at M = 1, K
+ * above about 96,000) returns MEMRA_ERR_UNSUPPORTED.
  */
 memra_status memra_q4_0_gemm_small_m(const uint8_t* wq4, const uint16_t* wd, int64_t N, int64_t K,
                                      int64_t M, const int8_t* xq, const float* xd, float* y,

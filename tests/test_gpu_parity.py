@@ -487,3 +487,41 @@ def test_moe_ffn_bad_ids(mem):
     torch.cuda.synchronize()
     assert int(st.item()) == 1
     assert torch.equal(y.view(torch.int32), y1.view(torch.int32))
+
+
+def test_activation_at_the_size_limit(mem, orc):
+    """M = 1 with K = 174752, the largest multiple of 32 whose q8_1 activation fits
+    MEMRA_MAX_X_BYTES (K + K/8 <= 196608): parity; one block more is refused."""
+    K = 174752
+    assert K + K // 8 <= 196608 < (K + 32) + (K + 32) // 8
+    (wq, wd, xq, xd), (oq, od, oxq, oxd) = run_pair(mem, orc, 40, K, 1, seed=97)
+    y = Guarded((1, 40), torch.float32)
+    mem.memra_q8_0_gemv(wq, wd, xq[0], xd[0], y=y.view[0])
+    torch.cuda.synchronize()
+    assert y.intact()
+    assert_within(np_(y.view), orc.gemm(oq, od, oxq, oxd),
+                  abs_terms(orc.block_dots(oq, oxq), od, oxd), "K at the limit")
+    K2 = K + 32
+    with pytest.raises(mem.MemraError) as e:
+        mem.memra_q8_0_gemv(torch.zeros((4, K2), dtype=torch.int8, device="cuda"),
+                            torch.zeros((4, K2 // 32), dtype=torch.float16, device="cuda"),
+                            torch.zeros((K2,), dtype=torch.int8, device="cuda"),
+                            torch.zeros((K2 // 32,), dtype=torch.float32, device="cuda"))
+    assert e.value.status == 3
+
+
+def test_four_bit_rows_beyond_shared_memory_are_refused(mem):
+    """The 4-bit formats stream through shared memory only: a row of K = 131072 with its
+    activation cannot fit a CTA, and the call returns MEMRA_ERR_UNSUPPORTED."""
+    K = 131072
+    wq4 = torch.zeros((8, K // 2), dtype=torch.uint8, device="cuda")
+    xq = torch.zeros((1, K), dtype=torch.int8, device="cuda")
+    xd = torch.zeros((1, K // 32), dtype=torch.float32, device="cuda")
+    with pytest.raises(mem.MemraError) as e:
+        mem.memra_q4_0_gemm_small_m(wq4, torch.zeros((8, K // 32), dtype=torch.float16,
+                                                     device="cuda"), xq, xd)
+    assert e.value.status == 3
+    with pytest.raises(mem.MemraError) as e:
+        mem.memra_nvfp4_gemm_small_m(wq4, torch.zeros((8, K // 16), dtype=torch.uint8,
+                                                      device="cuda"), 1.0, xq, xd)
+    assert e.value.status == 3
