@@ -650,9 +650,13 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         for (int r = 0; r < R; ++r)
 #pragma unroll
           for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
-        for (int pt = plo; pt < phi; ++pt) {
-          const int q = pt - plo;
-          if (pt < p.cpr - 1 || last_ok) {
+        // A slice has at most kSlicePartsMax parts.  Unrolled over that bound, every
+        // part's offsets are constants; the parts are still taken in order, so each
+        // lane's sum is unchanged.
+#pragma unroll
+        for (int q = 0; q < kSlicePartsMax; ++q) {
+          const int pt = plo + q;
+          if (pt < phi && (pt < p.cpr - 1 || last_ok)) {
             uint4 w0[R], w1[R];
             uint16_t dw[R];
 #pragma unroll
