@@ -603,11 +603,16 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
     const uint32_t q4m1 = ~q4m0;
     const int q4s0 = h1 ? 4 : 0;
     uint32_t tbase = 0;  // tasks in all earlier stages: deals tasks round-robin over warps
-    for (uint32_t it = 0;; ++it) {
-      const int slot = it % ns;
+    // A warp's tasks are kConsumerWarps apart: in (group, slice) form a step of
+    // (dgi, dsl) with a carry, so no task needs a division.
+    const int dgi = kConsumerWarps / S;
+    const int dsl = kConsumerWarps - dgi * S;
+    int slot = 0;
+    uint32_t phase = 0;
+    for (;;) {
       // Every warp waits for every stage, tasks or not: an arrival on the stage's
       // empty barrier must never run ahead of the stage itself.
-      if (!mbar_wait(full_bar(slot), (it / ns) & 1, abort_flag)) return;
+      if (!mbar_wait(full_bar(slot), phase, abort_flag)) return;
       const StageMeta mt = meta[slot];
       if (mt.nr <= 0) break;
       const int nr = mt.nr;
@@ -621,9 +626,17 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       const uint16_t* ds =
           reinterpret_cast<const uint16_t*>(ring + (size_t)slot * p.stage_bytes + p.wd_off);
       float* pp = part + (size_t)slot * p.rps * S * M;
+      int ngi = t0 / S;
+      int nsl = t0 - ngi * S;
       for (int t = t0; t < ntasks; t += kConsumerWarps) {
-        const int gi = t / S;
-        const int s = t - gi * S;
+        const int gi = ngi;
+        const int s = nsl;
+        ngi += dgi;
+        nsl += dsl;
+        if (nsl >= S) {
+          nsl -= S;
+          ++ngi;
+        }
         const int rbase = gi * R;
         int xrow = mt.xrow;
         if (packed_stage) {
@@ -722,6 +735,10 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(slot));
+      if (++slot == ns) {
+        slot = 0;
+        phase ^= 1;
+      }
     }
   }
 }
