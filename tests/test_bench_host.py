@@ -65,3 +65,17 @@ def test_dist_info_defaults(monkeypatch):
     for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
         monkeypatch.delenv(k, raising=False)
     assert bench.dist_info() == (1, 0, 0)
+
+
+def test_workload_rows_and_tokens():
+    assert bench.rows_of("dense27b_sweep") == 1
+    assert bench.rows_of("verify_m8") == 8 and bench.rows_of("batch_m16") == 16
+    assert bench.tokens_of("batch_m16") == 16 and bench.tokens_of("moe_top8_tokens8") == 8
+    assert bench.tokens_of("dense27b_sweep_nvfp4") == 1 and bench.tokens_of("verify_m4") == 1
+    for name in ("batch_m16", "moe_top8_tokens8", "dense27b_sweep_nvfp4", "moe_top8_nvfp4"):
+        assert name in bench.WORKLOADS
+
+
+def test_unknown_workload_is_rejected():
+    with pytest.raises(SystemExit):
+        bench.main(["--workload", "no_such_workload"])
