@@ -72,6 +72,14 @@ _SIGS = {
                                    _p, _p, _p, _p],
     "memra_q8_0_moe_ffn_tokens": [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _i64, _p, _i32,
                                   _p, _p, _p, _p],
+    "memra_q4_0_moe_ffn": [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _i32, _p, _p, _p,
+                           _p],
+    "memra_nvfp4_moe_ffn": [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _i32, _p,
+                            _p, _p, _p],
+    "memra_q4_0_moe_ffn_tokens": [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _i64, _p, _i32,
+                                  _p, _p, _p, _p],
+    "memra_nvfp4_moe_ffn_tokens": [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _i64,
+                                   _p, _i32, _p, _p, _p, _p],
     "memra_swiglu_quantize_q8_1": [_p, _i64, _i64, _p, _p, _p],
     "memra_q8_0_moe_ffn": [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _i32, _p, _p, _p,
                            _p],
@@ -647,6 +655,73 @@ def memra_q8_0_moe_ffn(gu_q, gu_d, dn_q, dn_d, ids, gate_w, x, y=None, workspace
                                         _ptr(ids), _ptr(gate_w), top_k, _ptr(x), dt, _ptr(y),
                                         _ptr(workspace), _ptr(dev_status), _stream(gu_q)))
     return y
+
+
+def _moe_ffn_4bit(fmt, gu, gu_s, gu_g, dn, dn_s, dn_g, ids, gate_w, x, y, workspace,
+                  dev_status):
+    """Shared marshalling of the Q4_0 and NVFP4 routed FFN entry points (one token when
+    ids is 1-D, a batch of tokens when it is [T, top_k])."""
+    _need(gu, "gate|up bank", torch.uint8)
+    E, F2, H2 = gu.shape
+    H, F = 2 * H2, F2 // 2
+    dev = gu.device
+    sdt, sdiv = (torch.float16, 32) if fmt == "q4_0" else (torch.uint8, 16)
+    _need(gu_s, "gate|up scales", sdt, dev, (E, F2, H // sdiv))
+    _need(dn, "down bank", torch.uint8, dev, (E, H, F // 2))
+    _need(dn_s, "down scales", sdt, dev, (E, H, F // sdiv))
+    if fmt == "nvfp4":
+        _need(gu_g, "gu_g", torch.float32, dev, (E,))
+        _need(dn_g, "dn_g", torch.float32, dev, (E,))
+    _need(ids, "ids", torch.int32, dev)
+    tokens = ids.dim() == 2
+    T, top_k = (ids.shape if tokens else (1, ids.shape[0]))
+    _need(gate_w, "gate_w", torch.float32, dev, tuple(ids.shape))
+    if x.dtype == torch.bfloat16:
+        dt = MEMRA_BF16
+    elif x.dtype == torch.float32:
+        dt = MEMRA_F32
+    else:
+        raise TypeError("x must be bfloat16 or float32")
+    yshape = (T, H) if tokens else (H,)
+    _need(x, "x", x.dtype, dev, yshape)
+    if y is None:
+        y = torch.empty(yshape, dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, yshape)
+    ws = T * top_k * (F2 + H) if tokens else top_k * F2
+    if workspace is None:
+        workspace = torch.empty((ws,), dtype=torch.float32, device=dev)
+    _need(workspace, "workspace", torch.float32, dev)
+    if workspace.numel() != ws:
+        raise ValueError("workspace must hold %d floats" % ws)
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    L = lib()
+    name = "memra_%s_moe_ffn%s" % (fmt, "_tokens" if tokens else "")
+    banks = ([_ptr(gu), _ptr(gu_s), _ptr(dn), _ptr(dn_s)] if fmt == "q4_0" else
+             [_ptr(gu), _ptr(gu_s), _ptr(gu_g), _ptr(dn), _ptr(dn_s), _ptr(dn_g)])
+    sizes = [E, H, F, _ptr(ids), _ptr(gate_w)] + ([T, top_k] if tokens else [top_k])
+    with torch.cuda.device(dev):
+        _check(name, getattr(L, name)(*banks, *sizes, _ptr(x), dt, _ptr(y), _ptr(workspace),
+                                      _ptr(dev_status), _stream(gu)))
+    return y
+
+
+def memra_q4_0_moe_ffn(gu_q4, gu_d, dn_q4, dn_d, ids, gate_w, x, y=None, workspace=None,
+                       dev_status=None):
+    """The routed FFN layer on Q4_0 banks (gu_q4 uint8 [E, 2F, H/2], gu_d float16
+    [E, 2F, H/32], dn_q4 uint8 [E, H, F/2], dn_d float16 [E, H, F/32]).  ids [top_k] for
+    one token (x [H]) or [T, top_k] for a batch (x [T, H], the batched entry point)."""
+    return _moe_ffn_4bit("q4_0", gu_q4, gu_d, None, dn_q4, dn_d, None, ids, gate_w, x, y,
+                         workspace, dev_status)
+
+
+def memra_nvfp4_moe_ffn(gu_codes, gu_scales, gu_g, dn_codes, dn_scales, dn_g, ids, gate_w, x,
+                        y=None, workspace=None, dev_status=None):
+    """The routed FFN layer on NVFP4 banks (codes uint8 [E, rows, K/2], E4M3 scales uint8
+    [E, rows, K/16], per-expert tensor scales float32 [E] for each bank).  ids [top_k]
+    for one token or [T, top_k] for a batch."""
+    return _moe_ffn_4bit("nvfp4", gu_codes, gu_scales, gu_g, dn_codes, dn_scales, dn_g, ids,
+                         gate_w, x, y, workspace, dev_status)
 
 
 def memra_q8_0_moe_ffn_noalloc(gu_q, gu_d, dn_q, dn_d, ids, gate_w, x, y, dev_status=None):

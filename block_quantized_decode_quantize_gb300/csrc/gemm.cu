@@ -1682,13 +1682,98 @@ extern "C" memra_status memra_q4_0_moe_gemv_tokens(const uint8_t* wq4_bank,
                               stream);
 }
 
-extern "C" memra_status memra_q8_0_moe_ffn_tokens(const int8_t* gu_q, const uint16_t* gu_d,
-                                                  const int8_t* dn_q, const uint16_t* dn_d,
-                                                  int64_t E, int64_t H, int64_t F,
-                                                  const int32_t* ids, const float* gate_w,
-                                                  int64_t T, int64_t top_k, const void* x,
-                                                  int32_t dtype, float* y, float* workspace,
-                                                  int32_t* dev_status, cudaStream_t stream) {
+namespace memra {
+namespace {
+// The routed FFN's two banks: present for their format (NVFP4 also needs each bank's
+// per-expert tensor scales), and aligned for the bulk copies.
+template <int FMT>
+bool banks_ok(const int8_t* gu_q, const uint16_t* gu_d, const int8_t* dn_q,
+              const uint16_t* dn_d, int64_t, int64_t, const float* ggu, const float* gdn) {
+  if (!gu_q || !gu_d || !dn_q || !dn_d) return false;
+  return FMT != kNv4 || (ggu && gdn);
+}
+
+template <int FMT>
+bool banks_aligned(const int8_t* gu_q, const uint16_t* gu_d, const int8_t* dn_q,
+                   const uint16_t* dn_d, const float* ggu, const float* gdn) {
+  if (FMT == kQ8)
+    return aligned(gu_q, 32) && aligned(gu_d, 2) && aligned(dn_q, 32) && aligned(dn_d, 2);
+  return aligned(gu_q, 16) && aligned(gu_d, 16) && aligned(dn_q, 16) && aligned(dn_d, 16) &&
+         (!ggu || aligned(ggu, 4)) && (!gdn || aligned(gdn, 4));
+}
+
+template <int FMT>
+memra_status moe_ffn(const int8_t* gu_q, const uint16_t* gu_d, const int8_t* dn_q,
+                     const uint16_t* dn_d, int64_t E, int64_t H, int64_t F, const int32_t* ids,
+                     const float* gate_w, int64_t top_k, const void* x, int32_t dtype, float* y,
+                     float* workspace, int32_t* dev_status, cudaStream_t stream,
+                     const float* ggu = nullptr, const float* gdn = nullptr) {
+  if (E < 1 || H < 0 || F < 0 || H % 32 != 0 || F % 32 != 0 || top_k < 1)
+    return MEMRA_ERR_INVALID_ARG;
+  if (dtype != MEMRA_BF16 && dtype != MEMRA_F32) return MEMRA_ERR_INVALID_ARG;
+  if (top_k > MEMRA_MAX_TOP_K) return MEMRA_ERR_UNSUPPORTED;
+  if (H > INT32_MAX / 2 || F > INT32_MAX / 2 || E > INT32_MAX) return MEMRA_ERR_UNSUPPORTED;
+  if (H == 0) return MEMRA_OK;
+  if (!y || !ids || !gate_w) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(y, 4) || !aligned(ids, 4) || !aligned(gate_w, 4) ||
+      (dev_status && !aligned(dev_status, 4)))
+    return MEMRA_ERR_ALIGNMENT;
+  if (F == 0) return zero_fill(y, H, stream);
+  if (!gu_q || !gu_d || !dn_q || !dn_d || !x || !workspace) return MEMRA_ERR_INVALID_ARG;
+  if (!banks_ok<FMT>(gu_q, gu_d, dn_q, dn_d, H, F, ggu, gdn)) return MEMRA_ERR_INVALID_ARG;
+  if (FMT != kQ8 && (H % 256 != 0 || F % 256 != 0)) return MEMRA_ERR_UNSUPPORTED;
+  if (!banks_aligned<FMT>(gu_q, gu_d, dn_q, dn_d, ggu, gdn) || !aligned(x, 16) ||
+      !aligned(workspace, 16))
+    return MEMRA_ERR_ALIGNMENT;
+  if (!x_fits(1, H) || !x_fits(top_k, F)) return MEMRA_ERR_UNSUPPORTED;
+  // gate|up rows of every selected expert: workspace[k][0, 2F) = W_gu[ids[k]] x.
+  Params a{};
+  a.wq = gu_q;
+  a.wd = gu_d;
+  a.N = 2 * F;
+  a.K = H;
+  a.xin = x;
+  a.xrows = 1;
+  a.y = workspace;
+  a.ids = ids;
+  a.top_k = (int)top_k;
+  a.E = E;
+  a.xpe = 0;
+  a.status = dev_status;
+  a.gexp = ggu;
+  a.units = top_k * 2 * F;
+  memra_status st = dtype == MEMRA_BF16
+                        ? run_product<1, 1, kMoeUngated, kXbf16, FMT>(a, stream)
+                        : run_product<1, 1, kMoeUngated, kXf32, FMT>(a, stream);
+  if (st != MEMRA_OK) return st;
+  // down rows with SwiGLU + q8_1 of each expert's gate|up row in the prologue.
+  Params b{};
+  b.wq = dn_q;
+  b.wd = dn_d;
+  b.N = H;
+  b.K = F;
+  b.xin = workspace;
+  b.xrows = (int)top_k;
+  b.y = y;
+  b.ids = ids;
+  b.gate_w = gate_w;
+  b.top_k = (int)top_k;
+  b.E = E;
+  b.xpe = 1;
+  b.status = dev_status;
+  b.routing_ready = 1;  // the gate|up kernel above waited for the routing
+  b.gexp = gdn;
+  b.units = H;
+  return run_product<1, 1, kMoeGated, kXswiglu, FMT>(b, stream);
+}
+
+template <int FMT>
+memra_status moe_ffn_tokens(const int8_t* gu_q, const uint16_t* gu_d, const int8_t* dn_q,
+                            const uint16_t* dn_d, int64_t E, int64_t H, int64_t F,
+                            const int32_t* ids, const float* gate_w, int64_t T, int64_t top_k,
+                            const void* x, int32_t dtype, float* y, float* workspace,
+                            int32_t* dev_status, cudaStream_t stream,
+                            const float* ggu = nullptr, const float* gdn = nullptr) {
   if (E < 1 || H < 0 || F < 0 || H % 32 != 0 || F % 32 != 0 || top_k < 1 || T < 0)
     return MEMRA_ERR_INVALID_ARG;
   if (dtype != MEMRA_BF16 && dtype != MEMRA_F32) return MEMRA_ERR_INVALID_ARG;
@@ -1702,8 +1787,10 @@ extern "C" memra_status memra_q8_0_moe_ffn_tokens(const int8_t* gu_q, const uint
     return MEMRA_ERR_ALIGNMENT;
   if (F == 0) return zero_fill(y, T * H, stream);
   if (!gu_q || !gu_d || !dn_q || !dn_d || !x || !workspace) return MEMRA_ERR_INVALID_ARG;
-  if (!aligned(gu_q, 32) || !aligned(gu_d, 2) || !aligned(dn_q, 32) || !aligned(dn_d, 2) ||
-      !aligned(x, 16) || !aligned(workspace, 16))
+  if (!banks_ok<FMT>(gu_q, gu_d, dn_q, dn_d, H, F, ggu, gdn)) return MEMRA_ERR_INVALID_ARG;
+  if (FMT != kQ8 && (H % 256 != 0 || F % 256 != 0)) return MEMRA_ERR_UNSUPPORTED;
+  if (!banks_aligned<FMT>(gu_q, gu_d, dn_q, dn_d, ggu, gdn) || !aligned(x, 16) ||
+      !aligned(workspace, 16))
     return MEMRA_ERR_ALIGNMENT;
   const int64_t P = T * top_k;
   if (!x_fits(T, H) || !x_fits(P, F)) return MEMRA_ERR_UNSUPPORTED;
@@ -1725,9 +1812,11 @@ extern "C" memra_status memra_q8_0_moe_ffn_tokens(const int8_t* gu_q, const uint
   a.xdiv = (int)top_k;
   a.lockstep = (int)P;
   a.status = dev_status;
+  a.gexp = ggu;
   a.units = P * 2 * F;
-  memra_status st = dtype == MEMRA_BF16 ? run_product<1, 1, kMoeUngated, kXbf16>(a, stream)
-                                        : run_product<1, 1, kMoeUngated, kXf32>(a, stream);
+  memra_status st = dtype == MEMRA_BF16
+                        ? run_product<1, 1, kMoeUngated, kXbf16, FMT>(a, stream)
+                        : run_product<1, 1, kMoeUngated, kXf32, FMT>(a, stream);
   if (st != MEMRA_OK) return st;
   // down, with SwiGLU + q8_1 of each pair's gate|up row in the prologue.
   Params b{};
@@ -1746,11 +1835,15 @@ extern "C" memra_status memra_q8_0_moe_ffn_tokens(const int8_t* gu_q, const uint
   b.lockstep = (int)P;
   b.status = dev_status;
   b.routing_ready = 1;  // the gate|up kernel above waited for the routing
+  b.gexp = gdn;
   b.units = P * H;
-  st = run_product<1, 1, kMoeUngated, kXswiglu>(b, stream);
+  st = run_product<1, 1, kMoeUngated, kXswiglu, FMT>(b, stream);
   if (st != MEMRA_OK) return st;
   return launch_combine(yp, ids, gate_w, T, top_k, H, E, y, stream);
 }
+
+}  // namespace
+}  // namespace memra
 
 extern "C" memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* gu_d,
                                            const int8_t* dn_q, const uint16_t* dn_d, int64_t E,
@@ -1758,59 +1851,73 @@ extern "C" memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* g
                                            const float* gate_w, int64_t top_k, const void* x,
                                            int32_t dtype, float* y, float* workspace,
                                            int32_t* dev_status, cudaStream_t stream) {
-  if (E < 1 || H < 0 || F < 0 || H % 32 != 0 || F % 32 != 0 || top_k < 1)
-    return MEMRA_ERR_INVALID_ARG;
-  if (dtype != MEMRA_BF16 && dtype != MEMRA_F32) return MEMRA_ERR_INVALID_ARG;
-  if (top_k > MEMRA_MAX_TOP_K) return MEMRA_ERR_UNSUPPORTED;
-  if (H > INT32_MAX / 2 || F > INT32_MAX / 2 || E > INT32_MAX) return MEMRA_ERR_UNSUPPORTED;
-  if (H == 0) return MEMRA_OK;
-  if (!y || !ids || !gate_w) return MEMRA_ERR_INVALID_ARG;
-  if (!aligned(y, 4) || !aligned(ids, 4) || !aligned(gate_w, 4) ||
-      (dev_status && !aligned(dev_status, 4)))
-    return MEMRA_ERR_ALIGNMENT;
-  if (F == 0) return zero_fill(y, H, stream);
-  if (!gu_q || !gu_d || !dn_q || !dn_d || !x || !workspace) return MEMRA_ERR_INVALID_ARG;
-  if (!aligned(gu_q, 32) || !aligned(gu_d, 2) || !aligned(dn_q, 32) || !aligned(dn_d, 2) ||
-      !aligned(x, 16) || !aligned(workspace, 16))
-    return MEMRA_ERR_ALIGNMENT;
-  if (!x_fits(1, H) || !x_fits(top_k, F)) return MEMRA_ERR_UNSUPPORTED;
-  // gate|up rows of every selected expert: workspace[k][0, 2F) = W_gu[ids[k]] x.
-  Params a{};
-  a.wq = gu_q;
-  a.wd = gu_d;
-  a.N = 2 * F;
-  a.K = H;
-  a.xin = x;
-  a.xrows = 1;
-  a.y = workspace;
-  a.ids = ids;
-  a.top_k = (int)top_k;
-  a.E = E;
-  a.xpe = 0;
-  a.status = dev_status;
-  a.units = top_k * 2 * F;
-  memra_status st = dtype == MEMRA_BF16 ? run_product<1, 1, kMoeUngated, kXbf16>(a, stream)
-                                        : run_product<1, 1, kMoeUngated, kXf32>(a, stream);
-  if (st != MEMRA_OK) return st;
-  // down rows with SwiGLU + q8_1 of each expert's gate|up row in the prologue.
-  Params b{};
-  b.wq = dn_q;
-  b.wd = dn_d;
-  b.N = H;
-  b.K = F;
-  b.xin = workspace;
-  b.xrows = (int)top_k;
-  b.y = y;
-  b.ids = ids;
-  b.gate_w = gate_w;
-  b.top_k = (int)top_k;
-  b.E = E;
-  b.xpe = 1;
-  b.status = dev_status;
-  b.routing_ready = 1;  // the gate|up kernel above waited for the routing
-  b.units = H;
-  return run_product<1, 1, kMoeGated, kXswiglu>(b, stream);
+  return moe_ffn<kQ8>(gu_q, gu_d, dn_q, dn_d, E, H, F, ids, gate_w, top_k, x, dtype, y,
+                      workspace, dev_status, stream);
 }
+
+extern "C" memra_status memra_q4_0_moe_ffn(const uint8_t* gu_q4, const uint16_t* gu_d,
+                                           const uint8_t* dn_q4, const uint16_t* dn_d, int64_t E,
+                                           int64_t H, int64_t F, const int32_t* ids,
+                                           const float* gate_w, int64_t top_k, const void* x,
+                                           int32_t dtype, float* y, float* workspace,
+                                           int32_t* dev_status, cudaStream_t stream) {
+  return moe_ffn<kQ4>(reinterpret_cast<const int8_t*>(gu_q4), gu_d,
+                      reinterpret_cast<const int8_t*>(dn_q4), dn_d, E, H, F, ids, gate_w, top_k,
+                      x, dtype, y, workspace, dev_status, stream);
+}
+
+extern "C" memra_status memra_nvfp4_moe_ffn(const uint8_t* gu_codes, const uint8_t* gu_scales,
+                                            const float* gu_g, const uint8_t* dn_codes,
+                                            const uint8_t* dn_scales, const float* dn_g,
+                                            int64_t E, int64_t H, int64_t F, const int32_t* ids,
+                                            const float* gate_w, int64_t top_k, const void* x,
+                                            int32_t dtype, float* y, float* workspace,
+                                            int32_t* dev_status, cudaStream_t stream) {
+  return moe_ffn<kNv4>(reinterpret_cast<const int8_t*>(gu_codes),
+                       reinterpret_cast<const uint16_t*>(gu_scales),
+                       reinterpret_cast<const int8_t*>(dn_codes),
+                       reinterpret_cast<const uint16_t*>(dn_scales), E, H, F, ids, gate_w, top_k,
+                       x, dtype, y, workspace, dev_status, stream, gu_g, dn_g);
+}
+
+extern "C" memra_status memra_q8_0_moe_ffn_tokens(const int8_t* gu_q, const uint16_t* gu_d,
+                                                  const int8_t* dn_q, const uint16_t* dn_d,
+                                                  int64_t E, int64_t H, int64_t F,
+                                                  const int32_t* ids, const float* gate_w,
+                                                  int64_t T, int64_t top_k, const void* x,
+                                                  int32_t dtype, float* y, float* workspace,
+                                                  int32_t* dev_status, cudaStream_t stream) {
+  return moe_ffn_tokens<kQ8>(gu_q, gu_d, dn_q, dn_d, E, H, F, ids, gate_w, T, top_k, x, dtype,
+                             y, workspace, dev_status, stream);
+}
+
+extern "C" memra_status memra_q4_0_moe_ffn_tokens(const uint8_t* gu_q4, const uint16_t* gu_d,
+                                                  const uint8_t* dn_q4, const uint16_t* dn_d,
+                                                  int64_t E, int64_t H, int64_t F,
+                                                  const int32_t* ids, const float* gate_w,
+                                                  int64_t T, int64_t top_k, const void* x,
+                                                  int32_t dtype, float* y, float* workspace,
+                                                  int32_t* dev_status, cudaStream_t stream) {
+  return moe_ffn_tokens<kQ4>(reinterpret_cast<const int8_t*>(gu_q4), gu_d,
+                             reinterpret_cast<const int8_t*>(dn_q4), dn_d, E, H, F, ids, gate_w,
+                             T, top_k, x, dtype, y, workspace, dev_status, stream);
+}
+
+extern "C" memra_status memra_nvfp4_moe_ffn_tokens(
+    const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_g,
+    const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_g, int64_t E, int64_t H,
+    int64_t F, const int32_t* ids, const float* gate_w, int64_t T, int64_t top_k, const void* x,
+    int32_t dtype, float* y, float* workspace, int32_t* dev_status, cudaStream_t stream) {
+  return moe_ffn_tokens<kNv4>(reinterpret_cast<const int8_t*>(gu_codes),
+                              reinterpret_cast<const uint16_t*>(gu_scales),
+                              reinterpret_cast<const int8_t*>(dn_codes),
+                              reinterpret_cast<const uint16_t*>(dn_scales), E, H, F, ids, gate_w,
+                              T, top_k, x, dtype, y, workspace, dev_status, stream, gu_g, dn_g);
+}
+
+
+
+
 
 // ----------------------------------------------------------------------------
 // memra_q8_0_moe_ffn_noalloc: the routed FFN with its gate|up workspace in a

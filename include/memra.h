@@ -412,6 +412,42 @@ memra_status memra_q8_0_moe_ffn_tokens(const int8_t* gu_q, const uint16_t* gu_d,
                                        int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * memra_q8_0_moe_ffn and memra_q8_0_moe_ffn_tokens on Q4_0 banks (gu_q4 uint8
+ * [E][2F][H/2], gu_d fp16 [E][2F][H/32], dn_q4 uint8 [E][H][F/2], dn_d fp16
+ * [E][H][F/32], packed as memra_quantize_q4_0 packs a matrix) and on NVFP4 banks
+ * (codes uint8 [E][rows][K/2], E4M3 scales uint8 [E][rows][K/16], and each bank's
+ * per-expert tensor scales gu_g, dn_g: fp32 [E], device).  Same arithmetic, outputs,
+ * workspace and id handling as the Q8_0 entry points, with the block sums of the
+ * format's products; each token's output is bit-identical to the format's routed
+ * GEMVs (gate|up ungated, SwiGLU + q8_1, down gated) run in sequence.  H and F must be
+ * multiples of 256 (MEMRA_ERR_UNSUPPORTED otherwise); banks 16-byte aligned.
+ */
+memra_status memra_q4_0_moe_ffn(const uint8_t* gu_q4, const uint16_t* gu_d, const uint8_t* dn_q4,
+                                const uint16_t* dn_d, int64_t E, int64_t H, int64_t F,
+                                const int32_t* ids, const float* gate_w, int64_t top_k,
+                                const void* x, int32_t dtype, float* y, float* workspace,
+                                int32_t* dev_status, cudaStream_t stream);
+memra_status memra_nvfp4_moe_ffn(const uint8_t* gu_codes, const uint8_t* gu_scales,
+                                 const float* gu_g, const uint8_t* dn_codes,
+                                 const uint8_t* dn_scales, const float* dn_g, int64_t E,
+                                 int64_t H, int64_t F, const int32_t* ids, const float* gate_w,
+                                 int64_t top_k, const void* x, int32_t dtype, float* y,
+                                 float* workspace, int32_t* dev_status, cudaStream_t stream);
+memra_status memra_q4_0_moe_ffn_tokens(const uint8_t* gu_q4, const uint16_t* gu_d,
+                                       const uint8_t* dn_q4, const uint16_t* dn_d, int64_t E,
+                                       int64_t H, int64_t F, const int32_t* ids,
+                                       const float* gate_w, int64_t T, int64_t top_k,
+                                       const void* x, int32_t dtype, float* y, float* workspace,
+                                       int32_t* dev_status, cudaStream_t stream);
+memra_status memra_nvfp4_moe_ffn_tokens(const uint8_t* gu_codes, const uint8_t* gu_scales,
+                                        const float* gu_g, const uint8_t* dn_codes,
+                                        const uint8_t* dn_scales, const float* dn_g, int64_t E,
+                                        int64_t H, int64_t F, const int32_t* ids,
+                                        const float* gate_w, int64_t T, int64_t top_k,
+                                        const void* x, int32_t dtype, float* y, float* workspace,
+                                        int32_t* dev_status, cudaStream_t stream);
+
+/*
  * memra_q8_0_moe_ffn without caller memory.  The pages have no counterpart: this
  * entry point exists for callers that cannot allocate device memory when they call
  * -- code running under a fixed memory arena or budget, plug-ins and embedded
