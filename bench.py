@@ -17,7 +17,7 @@ peak; ``cpu_baseline`` is the CPU oracle on the host cores over a bounded sample
                   [--workload dense27b_sweep|gemv_4096|verify_m2|verify_m4|verify_m8|
                               batch_m16|moe_top8|stress_lm_head|dense27b_sweep_q4_0|
                               dense27b_sweep_nvfp4|
-                              moe_top8_q4_0|moe_top8_nvfp4|moe_top8_tokens8]
+                              moe_top8_q4_0|moe_top8_nvfp4|moe_top8_tokens8|moe_top8_tokens16]
 """
 import argparse
 import hashlib
@@ -43,7 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("dense27b_sweep", "gemv_4096", "verify_m2", "verify_m4", "verify_m8", "batch_m16",
              "moe_top8",
              "stress_lm_head", "dense27b_sweep_q4_0", "dense27b_sweep_nvfp4", "moe_top8_q4_0",
-             "moe_top8_nvfp4", "moe_top8_tokens8")
+             "moe_top8_nvfp4", "moe_top8_tokens8", "moe_top8_tokens16")
 
 
 # ----------------------------------------------------------------------------
@@ -90,8 +90,8 @@ def tokens_of(name):
     """Tokens one step decodes: a batch of sequences or of routed tokens, else 1."""
     if name.startswith("batch_m"):
         return rows_of(name)
-    if name.endswith("tokens8"):
-        return 8
+    if "_tokens" in name:
+        return int(name.rsplit("_tokens", 1)[1])
     return 1
 
 
@@ -308,11 +308,12 @@ class Workload:
             self.ops = build_gemv_4096(mem, device)
         elif name == "stress_lm_head":
             self.ops = build_stress(mem, device, M=1) + build_stress(mem, device, M=8)
-        elif name in ("moe_top8", "moe_top8_q4_0", "moe_top8_nvfp4", "moe_top8_tokens8"):
+        elif name in ("moe_top8", "moe_top8_q4_0", "moe_top8_nvfp4", "moe_top8_tokens8",
+                      "moe_top8_tokens16"):
             n = synth.MOE["layers"] if layers is None else layers
             fmt = ("q4_0" if name.endswith("q4_0") else
                    "nvfp4" if name.endswith("nvfp4") else "q8_0")
-            tokens = 8 if name.endswith("tokens8") else 1
+            tokens = tokens_of(name)
             self.moe = [MoeLayer(mem, layer, device, fmt=fmt, tokens=tokens)
                         for layer in range(n)]
         else:
@@ -683,7 +684,8 @@ def run_memra(args):
 
     # Dense products quantise with a separate launch unless --fused; the routed FFN
     # uses its two-kernel entry point unless --unfused.
-    fused = ((not args.unfused) if args.workload in ("moe_top8", "moe_top8_tokens8")
+    fused = ((not args.unfused) if args.workload in ("moe_top8", "moe_top8_tokens8",
+                                                     "moe_top8_tokens16")
              else args.fused)
     wl = Workload(args.workload, mem, device, layers=args.layers, fused=fused,
                   chain=args.chain)

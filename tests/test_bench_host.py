@@ -71,6 +71,7 @@ def test_workload_rows_and_tokens():
     assert bench.rows_of("dense27b_sweep") == 1
     assert bench.rows_of("verify_m8") == 8 and bench.rows_of("batch_m16") == 16
     assert bench.tokens_of("batch_m16") == 16 and bench.tokens_of("moe_top8_tokens8") == 8
+    assert bench.tokens_of("moe_top8_tokens16") == 16
     assert bench.tokens_of("dense27b_sweep_nvfp4") == 1 and bench.tokens_of("verify_m4") == 1
     for name in ("batch_m16", "moe_top8_tokens8", "dense27b_sweep_nvfp4", "moe_top8_nvfp4"):
         assert name in bench.WORKLOADS
