@@ -59,7 +59,7 @@ def test_gemv_4096_full(mem, orc):
 
 
 @pytest.mark.parametrize("layer", [0, 63])
-@pytest.mark.parametrize("M", [1, 2, 4, 8])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
 def test_dense27b_layer_sampled(mem, orc, layer, M):
     cfg = synth.DENSE27B
     wid = 1 if M == 1 else 2
@@ -104,6 +104,41 @@ def test_dense27b_q4_0_layer_sampled(mem, orc, layer):
         terms = abs_terms(orc.block_dots(orc.unpack_q4_0(oq4), oxq), od, oxd)
         assert_within(np_(op.y)[:, rows], y_ref, terms, "q4_0 L%d %s" % (layer, name))
         del w, wq4, wd, op
+    torch.cuda.empty_cache()
+
+
+def test_dense27b_nvfp4_layer_sampled(mem, orc):
+    """The NVFP4 sweep's layer 0 as bench.py builds it.  The tensor scale depends on the
+    whole matrix, so the oracle quantises each full matrix (from the generator's fp32
+    weights on the host) and the products are compared on sampled rows."""
+    cfg = synth.DENSE27B
+    layer = 0
+    for t, (name, N, K) in enumerate(cfg["gemvs"]):
+        codes, scales, g = bench.quantized_weights(mem, N, K, 6, layer, t, device="cuda",
+                                                   fmt="nvfp4")
+        x = synth.activations_bf16(1, K, 6, layer, t, 1001, outlier_frac=cfg["outlier_frac"],
+                                   outlier_scale=cfg["outlier_scale"], device="cuda")
+        op = bench.Gemv(codes, scales, x, name, fmt="nvfp4", g=g)
+        assert op.weight_bytes == N * K // 2 + N * K // 16
+        bench.run_gemv_op(mem, op)
+        torch.cuda.synchronize()
+        # the generator's values as bench.py draws them (on the device), read back whole
+        w_host = synth.weights_fp32(N, K, 6, layer, t, device="cuda").cpu().numpy()
+        oc, osc, og = orc.quantize_nvfp4(w_host)
+        del w_host
+        assert np.float32(g).view(np.uint32) == np.float32(og).view(np.uint32), name + ": g"
+        rows = sample_rows(N, seed=600 + t)
+        idx = torch.as_tensor(rows, device="cuda")
+        assert np.array_equal(np_(codes[idx]), oc[rows]), name + ": codes"
+        assert np.array_equal(np_(scales[idx]), osc[rows]), name + ": scales"
+        oxq, oxd = orc.quantize_q8_1(bf16_bits_np(x.cpu()))
+        y_ref = orc.gemm_nvfp4(oc[rows], osc[rows], og, oxq, oxd)
+        c2 = orc.unpack_nvfp4(oc[rows]).astype(np.float64).reshape(len(rows), K // 16, 16)
+        S = np.einsum("nbi,bi->nb", c2, oxq[0].astype(np.float64).reshape(K // 16, 16))
+        terms = np.abs(0.5 * float(og) * orc.e4m3_to_f32(osc[rows]).astype(np.float64) *
+                       np.repeat(oxd[0].astype(np.float64), 2)[None] * S).sum(axis=1)
+        assert_within(np_(op.y)[:, rows], y_ref, terms[None], "nvfp4 L0 %s" % name)
+        del codes, scales, op, oc, osc
     torch.cuda.empty_cache()
 
 
