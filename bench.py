@@ -565,6 +565,31 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
+def read_ceiling(mem, device, stream, nbytes=4 << 30, reps=8):
+    """A plain read stream over `nbytes` of device memory (memra_read_stream), best over
+    1-4 CTAs per SM: the ceiling the weight-streaming kernels approach."""
+    buf = torch.ones((nbytes,), dtype=torch.uint8, device=device)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    best, per = 0.0, {}
+    for c in (1, 2, 3, 4):
+        sink = torch.zeros((sms * c,), dtype=torch.int32, device=device)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                mem.memra_read_stream(buf, sink, c)
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for _ in range(reps):
+                mem.memra_read_stream(buf, sink, c)
+            end.record(stream)
+        end.synchronize()
+        gbs = nbytes * reps / (start.elapsed_time(end) / 1e3) / 1e9
+        per[str(c)] = round(gbs, 1)
+        best = max(best, gbs)
+    del buf
+    return best, per
+
+
 def time_graph(graph, reps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -603,22 +628,22 @@ class CpuOracleSample:
             self.items.append((name, wq, wd, xb, synth.q8_0_bytes(N, K)))
         self.done = 0
 
-    def run_one(self):
+    def run_one(self, threads=None):
         """Run the next product; returns (seconds, weight bytes)."""
         name, wq, wd, xb, b = self.items[self.done % len(self.items)]
         t0 = time.perf_counter()
         xq, xd = self.oracle.quantize_q8_1(xb)
-        self.oracle.gemm(wq, wd, xq, xd, threads=self.threads)
+        self.oracle.gemm(wq, wd, xq, xd, threads=threads or self.threads)
         dt = time.perf_counter() - t0
         self.done += 1
         return dt, b
 
-    def run_for(self, budget_s):
+    def run_for(self, budget_s, threads=None):
         """Run products until `budget_s` seconds of oracle time; returns (GB/s, seconds,
         products)."""
         spent, nbytes, n = 0.0, 0, 0
         while spent < budget_s or n < len(self.items):
-            dt, b = self.run_one()
+            dt, b = self.run_one(threads)
             spent += dt
             nbytes += b
             n += 1
@@ -741,6 +766,11 @@ def run_memra(args):
                 "bytes_per_launch": int(bytes_per_launch),
                 "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
 
+    # The read-only stream ceiling on this GPU (4 GiB, larger than L2), for context.
+    ceiling, ceiling_per = read_ceiling(mem, device, stream)
+    roofline["read_ceiling_gbs"] = round(ceiling, 1)
+    roofline["frac_of_read_ceiling"] = round(achieved / ceiling, 4)
+
     # End to end through the public API: pinned host activations in, every output out.
     # The step's activations and outputs live in one arena each: one copy each way.
     ins = [wl.in_arena]
@@ -773,8 +803,11 @@ def run_memra(args):
     if rank == 0 and not args.no_cpu_baseline:
         cs = CpuOracleSample()
         v, spent, n = cs.run_for(args.cpu_budget)
+        v1, spent1, n1 = cs.run_for(min(4.0, args.cpu_budget), threads=1)
         cpu = {"value": round(v, 3), "unit": "GB/s", "cores": cs.threads, "kind": "oracle",
-               "sample": cs.describe(n), "seconds": round(spent, 2)}
+               "sample": cs.describe(n), "seconds": round(spent, 2),
+               "single_thread": {"value": round(v1, 3), "unit": "GB/s", "products": n1,
+                                 "seconds": round(spent1, 2)}}
 
     if rank == 0:
         cfg = workload_config(args.workload, wl)
@@ -815,6 +848,9 @@ def run_memra(args):
                             "the step's C-ABI calls, D2H of the output arena, host sync per step",
                     "steps": e2e_steps},
             "gpu_launches": wl.launches_per_step * args.steps,
+            "read_ceiling": {"value": round(ceiling, 1), "unit": "GB/s",
+                             "kernel": "memra_read_stream (diagnostic)", "bytes": 4 << 30,
+                             "by_ctas_per_sm": ceiling_per},
             "clocks": clock_info,
         }
         if status_bad:

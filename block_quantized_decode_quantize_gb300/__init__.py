@@ -53,6 +53,7 @@ _SIGS = {
     "memra_quantize_q4_0": [_p, _i64, _i64, _p, _p, _p],
     "memra_repack_q8_0": [_p, _i64, _i64, _p, _p, _p],
     "memra_quantize_nvfp4": [_p, _i64, _i64, _p, _p, _p, _p],
+    "memra_read_stream": [_p, _i64, _p, _i32, _p],
     "memra_nvfp4_gemm_small_m": [_p, _p, ctypes.c_float, _i64, _i64, _i64, _p, _p, _p, _p],
     "memra_nvfp4_gemv": [_p, _p, ctypes.c_float, _i64, _i64, _p, _p, _p, _p],
     "memra_nvfp4_moe_gemv": [_p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p,
@@ -220,6 +221,22 @@ def memra_repack_q4_0(blocks, N, K, wq4=None, wd=None):
         _check("memra_repack_q4_0",
                lib().memra_repack_q4_0(_ptr(blocks), N, K, _ptr(wq4), _ptr(wd), _stream(blocks)))
     return wq4, wd
+
+
+def memra_read_stream(buf, sink=None, ctas_per_sm=2):
+    """Read every byte of the CUDA tensor `buf` once (diagnostic read stream); returns the
+    per-CTA xor sink (uint32, zeroed here when not given)."""
+    if not isinstance(buf, torch.Tensor) or not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    nbytes = buf.numel() * buf.element_size()
+    if sink is None:
+        sms = torch.cuda.get_device_properties(buf.device).multi_processor_count
+        sink = torch.zeros((sms * ctas_per_sm,), dtype=torch.int32, device=buf.device)
+    with torch.cuda.device(buf.device):
+        _check("memra_read_stream",
+               lib().memra_read_stream(_ptr(buf), nbytes, _ptr(sink), ctas_per_sm,
+                                       _stream(buf)))
+    return sink
 
 
 def memra_quantize_q8_1(x, xq=None, xd=None):

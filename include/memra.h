@@ -486,6 +486,17 @@ memra_status memra_q8_0_block_dots(const int8_t* wq, int64_t N, int64_t K, const
                                    int64_t M, int32_t* s, cudaStream_t stream);
 
 /* Static text for a status code. */
+/*
+ * Diagnostic, not part of the decode path: read `bytes` of device memory once (every
+ * 16-byte word, streaming loads) with sms * ctas_per_sm CTAs of 512 threads, and fold
+ * them into sink[blockIdx] (uint32, one per CTA, xor-accumulated: the caller zeroes it
+ * to compare runs).  Timing it gives the read-only stream ceiling that the weight-
+ * streaming products approach.  bytes % 16 == 0; buf 16-byte aligned; ctas_per_sm in
+ * [1, 4].
+ */
+memra_status memra_read_stream(const void* buf, int64_t bytes, uint32_t* sink,
+                               int32_t ctas_per_sm, cudaStream_t stream);
+
 const char* memra_status_string(memra_status status);
 
 /* The cudaError_t (as int) of the calling thread's last MEMRA_ERR_CUDA, else 0. */
