@@ -189,3 +189,28 @@ def test_moe_tokens_at_the_routed_workload_shapes(mem):
         one = mem.memra_q8_0_moe_ffn(gq, gd, dq, dd, ids[t].cuda(), gw[t].cuda(), x[t])
         torch.cuda.synchronize()
         assert torch.equal(one.view(torch.int32), y[t].view(torch.int32)), t
+
+
+def test_tokens_degenerate_sizes(mem):
+    """K = 0: every sum is empty, so outputs are zero-filled; T = 0 or N = 0: nothing."""
+    E, N, T, top_k = 3, 16, 2, 2
+    ids = torch.zeros((T, top_k), dtype=torch.int32, device="cuda")
+    gw = torch.full((T, top_k), 0.5, device="cuda")
+    wq = torch.zeros((E, N, 0), dtype=torch.int8, device="cuda")
+    wd = torch.zeros((E, N, 0), dtype=torch.float16, device="cuda")
+    xq = torch.zeros((T, 0), dtype=torch.int8, device="cuda")
+    xd = torch.zeros((T, 0), dtype=torch.float32, device="cuda")
+    y = torch.full((T, top_k, N), 7.0, device="cuda")
+    mem.memra_q8_0_moe_gemv_tokens(wq, wd, ids, None, xq, xd, False, y=y)
+    yg = torch.full((T, N), 7.0, device="cuda")
+    mem.memra_q8_0_moe_gemv_tokens(wq, wd, ids, gw, xq, xd, False, y=yg)
+    torch.cuda.synchronize()
+    assert not y.any() and not yg.any()
+    lib = mem.lib()
+    sentinel = torch.full((4,), 3.0, device="cuda")
+    assert lib.memra_q8_0_moe_gemv_tokens(None, None, E, N, 64, None, None, 0, top_k, None, None,
+                                          0, sentinel.data_ptr(), None, None, None) == 0
+    assert lib.memra_q8_0_moe_gemv_tokens(None, None, E, 0, 64, None, None, T, top_k, None, None,
+                                          0, sentinel.data_ptr(), None, None, None) == 0
+    torch.cuda.synchronize()
+    assert torch.all(sentinel == 3.0)

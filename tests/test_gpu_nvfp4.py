@@ -195,3 +195,23 @@ def test_nvfp4_moe_gemv_tokens_matches_single_token(mem):
                                            g[t] if gated else None, xq[t], xd[t], False)
             torch.cuda.synchronize()
             assert torch.equal(one.view(torch.int32), y[t].view(torch.int32)), (gated, t)
+
+
+def test_nvfp4_degenerate_sizes(mem):
+    """K = 0 zero-fills y; N = 0 or M = 0 launches nothing; an empty ingest leaves g."""
+    y = torch.full((3, 5), 7.0, device="cuda")
+    mem.memra_nvfp4_gemm_small_m(torch.zeros((5, 0), dtype=torch.uint8, device="cuda"),
+                                 torch.zeros((5, 0), dtype=torch.uint8, device="cuda"), 1.0,
+                                 torch.zeros((3, 0), dtype=torch.int8, device="cuda"),
+                                 torch.zeros((3, 0), dtype=torch.float32, device="cuda"), y=y)
+    torch.cuda.synchronize()
+    assert not y.any()
+    y0 = mem.memra_nvfp4_gemm_small_m(torch.zeros((0, 128), dtype=torch.uint8, device="cuda"),
+                                      torch.zeros((0, 16), dtype=torch.uint8, device="cuda"), 1.0,
+                                      torch.zeros((2, 256), dtype=torch.int8, device="cuda"),
+                                      torch.zeros((2, 8), dtype=torch.float32, device="cuda"))
+    assert y0.shape == (2, 0)
+    g = torch.full((1,), 5.0, device="cuda")
+    mem.memra_quantize_nvfp4(torch.zeros((0, 64), device="cuda"), g=g)
+    torch.cuda.synchronize()
+    assert float(g.item()) == 5.0
