@@ -662,7 +662,10 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
           wl[r] = ws + row * Qrow + (plo * 32 + lane) * kBlockBytes + (FMT == kQ8 ? h1 * 16 : 0);
           dl[r] = ds + row * nb + plo * 32 + lane;
         }
-        const int8_t* xl = xs + (size_t)xrow * Ki + (plo * 32 + lane) * 32 + h1 * 16;
+        // NVFP4 reads the activation halves in element order (xh = 0): it is issue-bound,
+        // and the half order's selects cost more there than a 2-way bank conflict.
+        const int xh = FMT == kNv4 ? 0 : h1;
+        const int8_t* xl = xs + (size_t)xrow * Ki + (plo * 32 + lane) * 32 + xh * 16;
         const float* xdl = xds + (size_t)xrow * nb + plo * 32 + lane;
         float acc[R][M];
 #pragma unroll
@@ -691,7 +694,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
             for (int m = 0; m < M; ++m) {
               const int8_t* xm = xl + (size_t)m * Ki + q * 1024;
               const uint4 x0 = *reinterpret_cast<const uint4*>(xm);
-              const uint4 x1 = *reinterpret_cast<const uint4*>(xm + 16 - 32 * h1);
+              const uint4 x1 = *reinterpret_cast<const uint4*>(xm + 16 - 32 * xh);
               const float dx = xdl[(size_t)m * nb + q * 32];
               if (FMT == kQ4) {
                 // x0 holds half h1 of the block (elements 16*h1 ..), x1 the other half.
@@ -716,16 +719,16 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
                 }
               } else if (FMT == kNv4) {
                 // Code bytes 0..7 are the block's elements 0..15 (first E4M3 scale),
-                // bytes 8..15 elements 16..31; x0 holds elements 16*h1 .., x1 the rest.
+                // bytes 8..15 elements 16..31; x0 and x1 hold the same halves (xh = 0).
                 // Each half's exact sum, then the two terms in element order.
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                   const uint4 c = w0[r];
-                  const int sa = nv4_dot16(h1 ? c.z : c.x, h1 ? c.w : c.y, x0);
-                  const int sb = nv4_dot16(h1 ? c.x : c.z, h1 ? c.y : c.w, x1);
+                  const int sa = nv4_dot16(c.x, c.y, x0);  // elements 0..15
+                  const int sb = nv4_dot16(c.z, c.w, x1);  // elements 16..31
                   const float2 sc = e4m3x2_to_float2(dw[r]);
-                  acc[r][m] = __fmaf_rn(__fmul_rn(sc.x, dx), (float)(h1 ? sb : sa), acc[r][m]);
-                  acc[r][m] = __fmaf_rn(__fmul_rn(sc.y, dx), (float)(h1 ? sa : sb), acc[r][m]);
+                  acc[r][m] = __fmaf_rn(__fmul_rn(sc.x, dx), (float)sa, acc[r][m]);
+                  acc[r][m] = __fmaf_rn(__fmul_rn(sc.y, dx), (float)sb, acc[r][m]);
                 }
               } else {
 #pragma unroll
