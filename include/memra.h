@@ -489,8 +489,8 @@ memra_status memra_q8_0_block_dots(const int8_t* wq, int64_t N, int64_t K, const
 /*
  * Diagnostic, not part of the decode path: read `bytes` of device memory once (every
  * 16-byte word, streaming loads) with sms * ctas_per_sm CTAs of 512 threads, and fold
- * them into sink[blockIdx] (uint32, one per CTA, xor-accumulated: the caller zeroes it
- * to compare runs).  Timing it gives the read-only stream ceiling that the weight-
+ * them into sink[blockIdx]: sink is uint32 [sms * ctas_per_sm] (sms = the device's
+ * multiprocessor count), xor-accumulated, so the caller zeroes it to compare runs.  Timing it gives the read-only stream ceiling that the weight-
  * streaming products approach.  bytes % 16 == 0; buf 16-byte aligned; ctas_per_sm in
  * [1, 4].
  */
