@@ -828,3 +828,25 @@ def test_moe_gemv_nvfp4_reduces_to_the_dense_product(orc):
     ref = sum(float(gw[k]) * orc.nvfp4_dequant_gemm_f64(codes[e], scales[e], gexp[e], xq, xd)[0]
               for k, e in ((0, 2), (1, 0), (3, 3)))
     assert np.allclose(yg, ref, rtol=1e-5, atol=1e-7 * np.abs(ref).max())
+
+
+def test_e2m1_against_brute_force_nearest(orc):
+    """E2M1 rounding by brute force: the nearest of the 8 grid magnitudes, a tie going to
+    the neighbour with mantissa bit 0 (codes 0, 2, 4, 6), saturation at 6, sign bit kept."""
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    mids = (grid[:-1] + grid[1:]) / 2
+    r = rng(89)
+    v = np.concatenate([r.uniform(-8, 8, 50000), grid, mids,
+                        np.nextafter(mids.astype(np.float32), np.float32(0)),
+                        np.nextafter(mids.astype(np.float32), np.float32(9)),
+                        [6.5, 100.0, 1e30]]).astype(np.float32)
+
+    def brute(x):
+        a = min(abs(float(x)), 6.0)
+        d = np.abs(grid - a)
+        best = np.flatnonzero(d == d.min())
+        code = best[0] if len(best) == 1 else [c for c in best if c % 2 == 0][0]
+        return int(code) | (8 if np.signbit(x) else 0)
+
+    want = np.array([brute(x) for x in v], np.uint8)
+    assert np.array_equal(orc.f32_to_e2m1(v), want)
