@@ -1,10 +1,11 @@
 /*
- * memra.h -- C ABI of the GB300 (sm_103a) Q8_0 decode library.
+ * memra.h -- C ABI of the GB300 (sm_103a) block-quantised decode library.
  *
  * The single-user decode step of an LLM streams block-quantised weights through
  * a fused dequantise matrix-vector (M = 1) or skinny matrix (M <= 16: speculative
- * verify, batched decode) product, plus a routed-expert (MoE) variant.  The memra pages name this
- * path: Q8_0 decode through split-plane repacked matvecs with warp-level dp4a and
+ * verify, batched decode) product, plus a routed-expert (MoE) variant for one token
+ * or a batch of tokens.  Weights come as Q8_0 (below), Q4_0 or NVFP4 (declared with
+ * their entry points).  The memra pages name this path: Q8_0 decode through split-plane repacked matvecs with warp-level dp4a and
  * per-shape dispatch (memra wiki, github.com/avifenesh/memra/wiki, feature list);
  * one batched K+1 verify for MTP speculative decoding (same list); routed MoE
  * experts (same list); Q8_0 27B plain decode as a measured cell ("memra
@@ -44,7 +45,8 @@
  *     launch failure returns MEMRA_ERR_CUDA; memra_last_cuda_error() gives the
  *     cudaError_t of the calling thread's last failure.
  *   - Alignment: wq and wq_bank 32 bytes; xq, hq (outputs of the quantisers) and
- *     the quantiser inputs 16 bytes; wd 2 bytes; xd, y, ids, gate_w 4 bytes.
+ *     the quantiser inputs 16 bytes; wd 2 bytes; xd, y, ids, gate_w 4 bytes.  The
+ *     4-bit formats' planes and their q8_1 inputs: 16 bytes.
  *   - Inputs must be finite.
  */
 #ifndef MEMRA_H
