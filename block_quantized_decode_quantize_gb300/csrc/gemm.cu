@@ -1964,10 +1964,14 @@ extern "C" memra_status memra_q8_0_moe_ffn_noalloc(const int8_t* gu_q, const uin
                                                    int64_t top_k, const void* x, int32_t dtype,
                                                    float* y, int32_t* dev_status,
                                                    cudaStream_t stream) {
-  if (top_k >= 1 && F >= 0 && top_k * 2 * F > MEMRA_MOE_NOALLOC_SCRATCH_FLOATS)
+  // top_k * 2F > the array's size, tested without forming the product (top_k and F
+  // are not range-checked yet, so the product could overflow).  Other out-of-range
+  // sizes are refused by the workspace entry point below.
+  const bool top_k_ok = top_k >= 1 && top_k <= MEMRA_MAX_TOP_K;
+  if (top_k_ok && F > MEMRA_MOE_NOALLOC_SCRATCH_FLOATS / (2 * top_k))
     return MEMRA_ERR_UNSUPPORTED;
   float* ws = nullptr;
-  if (H > 0 && F > 0 && top_k >= 1) {
+  if (H > 0 && F > 0 && top_k_ok) {
     const memra_status st = memra::moe_scratch_address(&ws);
     if (st != MEMRA_OK) return st;
   }

@@ -465,6 +465,9 @@ memra_status memra_nvfp4_moe_ffn_tokens(const uint8_t* gu_codes, const uint8_t* 
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call before
  *     any stream capture on the device.
+ *   - That address is kept for the life of the process.  A cudaDeviceReset destroys
+ *     the context that holds the array, so after one this entry point must not be
+ *     called again in the same process (it would write to the old address).
  *   - Every call shares the one array.  Calls that may overlap on the GPU (on
  *     different streams, or before an earlier one has finished on another stream)
  *     race on it; keep such calls on one stream.  The array keeps the last call's
@@ -487,7 +490,6 @@ memra_status memra_q8_0_moe_ffn_noalloc(const int8_t* gu_q, const uint16_t* gu_d
 memra_status memra_q8_0_block_dots(const int8_t* wq, int64_t N, int64_t K, const int8_t* xq,
                                    int64_t M, int32_t* s, cudaStream_t stream);
 
-/* Static text for a status code. */
 /*
  * Diagnostic, not part of the decode path: read `bytes` of device memory once (every
  * 16-byte word, streaming loads) with sms * ctas_per_sm CTAs of 512 threads, and fold
@@ -499,6 +501,7 @@ memra_status memra_q8_0_block_dots(const int8_t* wq, int64_t N, int64_t K, const
 memra_status memra_read_stream(const void* buf, int64_t bytes, uint32_t* sink,
                                int32_t ctas_per_sm, cudaStream_t stream);
 
+/* Static text for a status code. */
 const char* memra_status_string(memra_status status);
 
 /* The cudaError_t (as int) of the calling thread's last MEMRA_ERR_CUDA, else 0. */

@@ -27,6 +27,18 @@ def abs_terms(s, wd_u16, xd):
     return np.abs(c * s.astype(np.float64)).sum(axis=2)
 
 
+def nvfp4_terms(orc, oc, os_, og, oxq, oxd):
+    """sum over 16-element half-blocks of |(g/2) s d_x S| as fp64 [M, N], S the exact sum of
+    twice the E2M1 values times the activation quants (the NVFP4 product's terms)."""
+    N, K = oc.shape[0], oc.shape[1] * 2
+    M = oxq.shape[0]
+    c2 = orc.unpack_nvfp4(oc).astype(np.float64).reshape(N, K // 16, 16)
+    S = np.einsum("nbi,mbi->mnb", c2, oxq.astype(np.float64).reshape(M, K // 16, 16))
+    s = orc.e4m3_to_f32(os_).astype(np.float64)
+    dx = np.repeat(oxd.astype(np.float64), 2, axis=1)
+    return np.abs(0.5 * float(og) * s[None] * dx[:, None, :] * S).sum(axis=2)
+
+
 def assert_within(y, y_ref, terms, what=""):
     y = np.asarray(y, np.float64)
     y_ref = np.asarray(y_ref, np.float64)

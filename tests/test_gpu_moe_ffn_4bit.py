@@ -1,15 +1,19 @@
 """GPU checks of the routed FFN layer on Q4_0 and NVFP4 banks, through the C ABI.
 
-The layer entry points must give, bit for bit, the format's own routed GEMVs run in
-sequence (gate|up ungated on q8_1(x), SwiGLU + q8_1, down gated); the batched-token
-entry points must give, bit for bit, the single-token layer on each token.  The routed
-GEMVs themselves are checked against the oracle in test_gpu_q4_0.py and
-test_gpu_nvfp4.py.
+The layer entry points must match the oracle's layer, built from its own quantisation
+of the generator's fp32 weights and activations, stage by stage: the gate|up rows
+within the product tolerance, then the output against the oracle's down projection of
+its own SwiGLU rows within the bound that a one-step difference in the requantised
+rows allows.  They must also give, bit for bit, the format's own routed GEMVs run in
+sequence (gate|up ungated on q8_1(x), SwiGLU + q8_1, down gated), and the
+batched-token entry points the single-token layer on each token.
 """
+import numpy as np
 import pytest
 import torch
 
 import synth
+from _util import abs_terms, assert_within, bf16_bits_np, np_, nvfp4_terms, wd_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -102,3 +106,94 @@ def test_nvfp4_layer_needs_the_expert_scales(mem):
                                  gw.data_ptr(), TOP_K, x.data_ptr(), 0, y.data_ptr(),
                                  ws.data_ptr(), None, None)
     assert st == 1                                   # no gate|up tensor scales
+
+
+def oracle_banks(orc, fmt, seed):
+    """The banks of `banks` quantised by the oracle from the generator's fp32, expert by
+    expert: (planes [E, rows, ...], scales [E, rows, ...], tensor scales [E] or None)."""
+    def bank(rows, K, key):
+        parts = []
+        for e in range(E):
+            w = np_(synth.weights_fp32(rows, K, seed, key, e))
+            parts.append(orc.quantize_q4_0(w) + (None,) if fmt == "q4_0" else
+                         orc.quantize_nvfp4(w))
+        g = None if fmt == "q4_0" else np.array([p[2] for p in parts], np.float32)
+        return np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]), g
+    return bank(2 * F, H, 0), bank(H, F, 1)
+
+
+def assert_bank_equal(fmt, gpu, ob):
+    assert np.array_equal(np_(gpu[0]), ob[0])
+    if fmt == "q4_0":
+        assert np.array_equal(wd_bits(gpu[1]), ob[1])
+    else:
+        assert np.array_equal(np_(gpu[1]), ob[1])
+        assert np.array_equal(np_(gpu[2]).view(np.uint32), ob[2].view(np.uint32))
+
+
+def oracle_product(orc, fmt, ob, e, xq, xd):
+    """Expert e's product with q8_1 rows (y [M, N]) and its tolerance terms [M, N]."""
+    if fmt == "q4_0":
+        y = orc.gemm_q4_0(ob[0][e], ob[1][e], xq, xd)
+        return y, abs_terms(orc.block_dots(orc.unpack_q4_0(ob[0][e]), xq), ob[1][e], xd)
+    y = orc.gemm_nvfp4(ob[0][e], ob[1][e], ob[2][e], xq, xd)
+    return y, nvfp4_terms(orc, ob[0][e], ob[1][e], ob[2][e], xq, xd)
+
+
+def abs_weights(orc, fmt, ob, e):
+    """|W| of expert e dequantised in fp64 [N, K]."""
+    if fmt == "q4_0":
+        v = orc.unpack_q4_0(ob[0][e]).astype(np.float64)
+        d = np.repeat(ob[1][e].view(np.float16).astype(np.float64), 32, axis=1)
+        return np.abs(v * d)
+    v = orc.unpack_nvfp4(ob[0][e]).astype(np.float64)
+    s = np.repeat(orc.e4m3_to_f32(ob[1][e]).astype(np.float64), 16, axis=1)
+    return np.abs(0.5 * float(ob[2][e]) * s * v)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "nvfp4"])
+@pytest.mark.parametrize("T", [1, 5])
+def test_layer_matches_oracle(mem, orc, fmt, T):
+    seed = 830 if fmt == "q4_0" else 831
+    gu, dn = banks(mem, fmt, seed)
+    gu_o, dn_o = oracle_banks(orc, fmt, seed)
+    assert_bank_equal(fmt, gu, gu_o)
+    assert_bank_equal(fmt, dn, dn_o)
+    routes = [synth.routing(E, TOP_K, seed + 2, t) for t in range(T)]
+    ids = torch.stack([r[0] for r in routes])
+    gw = torch.stack([r[1] for r in routes])
+    x = synth.activations_bf16(T, H, seed + 3, outlier_frac=0.001)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if T == 1:
+        ws = torch.empty((TOP_K * 2 * F,), device="cuda")
+        y = layer(mem, fmt, gu, dn, ids[0].cuda(), gw[0].cuda(), x[0].cuda(), workspace=ws,
+                  dev_status=st)[None]
+    else:
+        ws = torch.empty((T * TOP_K * (2 * F + H),), device="cuda")
+        y = layer(mem, fmt, gu, dn, ids.cuda(), gw.cuda(), x.cuda(), workspace=ws,
+                  dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ygu = np_(ws[:T * TOP_K * 2 * F]).reshape(T, TOP_K, 2 * F)
+    y = np_(y)
+    for t in range(T):
+        xq, xd = orc.quantize_q8_1(bf16_bits_np(x[t:t + 1]))
+        sel = np_(ids[t])
+        g = np_(gw[t])
+        # gate|up: every selected expert's rows within the product tolerance
+        pr = [oracle_product(orc, fmt, gu_o, e, xq, xd) for e in sel]
+        ygu_ref = np.stack([p[0][0] for p in pr])
+        assert_within(ygu[t], ygu_ref, np.stack([p[1][0] for p in pr]),
+                      "%s gate|up t=%d" % (fmt, t))
+        # down from the oracle's own SwiGLU rows; gated sum in ascending k from 0
+        hq, hd = orc.swiglu_quantize_q8_1(ygu_ref)
+        y_ref = np.zeros(H, np.float32)
+        bound = np.zeros(H)
+        for k, e in enumerate(sel):
+            yk = oracle_product(orc, fmt, dn_o, e, hq[k:k + 1], hd[k:k + 1])[0][0]
+            y_ref = (y_ref + np.float32(g[k]) * yk).astype(np.float32)
+            # the GPU requantises its own gate|up rows: each h may sit one step away
+            bound += float(g[k]) * (abs_weights(orc, fmt, dn_o, e) @
+                                    np.repeat(2.0 * hd[k].astype(np.float64), 32))
+        err = np.abs(y[t].astype(np.float64) - y_ref)
+        assert np.all(err <= bound + 1e-4 * np.abs(y_ref).max() + 1e-6), (fmt, t)

@@ -33,6 +33,30 @@ def make_bank(mem, E, N, K, seed):
     return wq.view(E, N, K), wd.view(E, N, K // 32)
 
 
+def oracle_bank(orc, E, N, K, seed, wq=None, wd=None):
+    """The same bank quantised by the oracle from the generator's fp32 (never from the
+    GPU's planes); when the GPU's planes are given they must equal it bit for bit."""
+    w = torch.stack([synth.weights_fp32(N, K, seed, 700, e) for e in range(E)])
+    oq, od = orc.quantize_q8_0(np_(w).reshape(E * N, K))
+    oq, od = oq.reshape(E, N, K), od.reshape(E, N, K // 32)
+    if wq is not None:
+        assert np.array_equal(np_(wq), oq) and np.array_equal(wd_bits(wd), od)
+    return oq, od
+
+
+def oracle_x(orc, x, xq=None, xd=None):
+    """q8_1 of the generator's activation rows by the oracle; the GPU's quantisation, when
+    given, must equal it bit for bit."""
+    if x.dtype == torch.bfloat16:
+        oxq, oxd = orc.quantize_q8_1(bf16_bits_np(x.cpu()))
+    else:
+        oxq, oxd = orc.quantize_q8_1(np_(x))
+    if xq is not None:
+        assert np.array_equal(np_(xq).reshape(oxq.shape), oxq)
+        assert np.array_equal(np_(xd).reshape(oxd.shape).view(np.uint32), oxd.view(np.uint32))
+    return oxq, oxd
+
+
 def batch_routing(E, T, top_k, seed):
     """Each token's top-k of its own seeded router; with E small the tokens share experts."""
     ids, gw = zip(*[synth.routing(E, top_k, seed, t) for t in range(T)])
@@ -73,9 +97,12 @@ def test_moe_gemv_tokens_parity(mem, orc, T, gated, per_expert):
                                       xq[t], xd[t], per_expert)
         torch.cuda.synchronize()
         assert torch.equal(one.view(torch.int32), y.view[t].view(torch.int32)), t
-    # and the oracle, each token on its own
-    oq, od = np_(wq), wd_bits(wd)
-    oxq, oxd = np_(xq), np_(xd)
+    # and the oracle, each token on its own, on its own quantisation of the generator's
+    # values (asserted equal to the GPU's first)
+    oq, od = oracle_bank(orc, E, N, K, 40 + T, wq, wd)
+    oxq, oxd = oracle_x(orc, x, xq, xd)
+    if per_expert:
+        oxq, oxd = oxq.reshape(T, top_k, K), oxd.reshape(T, top_k, K // 32)
     y_ref, bad = orc.moe_gemv_tokens(oq, od, np_(ids), np_(gw) if gated else None, oxq, oxd,
                                      int(per_expert))
     assert bad == 0
@@ -168,8 +195,9 @@ def test_moe_ffn_tokens_matches_single_token_layer(mem, orc, dtype, T):
     # bound the single-token FFN test uses
     xo = bf16_bits_np(x.cpu()) if dtype == torch.bfloat16 else np_(x)
     xf = orc.bf16_bits_to_f32(xo) if dtype == torch.bfloat16 else xo
-    y_ref, bad = orc.moe_ffn_tokens(xf, np_(gq), wd_bits(gd), np_(dq), wd_bits(dd), np_(ids),
-                                    np_(gw))
+    ogq, ogd = oracle_bank(orc, E, 2 * F, H, 60, gq, gd)
+    odq, odd = oracle_bank(orc, E, H, F, 61, dq, dd)
+    y_ref, bad = orc.moe_ffn_tokens(xf, ogq, ogd, odq, odd, np_(ids), np_(gw))
     assert bad == 0
     err = np.abs(np_(y).astype(np.float64) - y_ref)
     assert np.all(err <= 0.02 * np.abs(y_ref).max(axis=1, keepdims=True) + 1e-5)

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import synth
-from _util import Guarded, assert_within, bf16_bits_np, np_
+from _util import Guarded, assert_within, bf16_bits_np, np_, nvfp4_terms
 
 pytestmark = pytest.mark.gpu
 
@@ -40,16 +40,6 @@ def check_nvfp4_weights(orc, mem, w_cpu):
     assert np.array_equal(np_(scales), os_)
     assert np.array_equal(np_(codes), oc)
     return codes, scales, float(np_(g)[0]), oc, os_, og
-
-
-def nvfp4_terms(orc, oc, os_, og, oxq, oxd):
-    N, K = oc.shape[0], oc.shape[1] * 2
-    M = oxq.shape[0]
-    c2 = orc.unpack_nvfp4(oc).astype(np.float64).reshape(N, K // 16, 16)
-    S = np.einsum("nbi,mbi->mnb", c2, oxq.astype(np.float64).reshape(M, K // 16, 16))
-    s = orc.e4m3_to_f32(os_).astype(np.float64)
-    dx = np.repeat(oxd.astype(np.float64), 2, axis=1)
-    return np.abs(0.5 * float(og) * s[None] * dx[:, None, :] * S).sum(axis=2)
 
 
 @pytest.mark.parametrize("N,K,seed,std", [(37, 96, 1, 0.02), (4096, 4096, 0, 0.02),
@@ -129,13 +119,24 @@ def test_nvfp4_rejects_k_not_multiple_of_256(mem):
     assert e.value.status == 3
 
 
-def nvfp4_bank(mem, E, N, K, seed):
-    """Each expert quantised on its own (its own tensor scale), stacked into a bank."""
-    parts = [mem.memra_quantize_nvfp4(synth.weights_fp32(N, K, seed, e, std=0.01 * (1 + e % 3))
-                                      .cuda()) for e in range(E)]
+def nvfp4_bank(mem, E, N, K, seed, orc=None):
+    """Each expert quantised on its own (its own tensor scale), stacked into a bank.  With
+    the oracle given, each expert's GPU ingest is checked bit for bit against the oracle's
+    quantisation of the same fp32 weights, and the oracle's bank is returned as well."""
+    ws = [synth.weights_fp32(N, K, seed, e, std=0.01 * (1 + e % 3)) for e in range(E)]
+    if orc is not None:
+        parts = [check_nvfp4_weights(orc, mem, w) for w in ws]
+        obank = (np.stack([p[3] for p in parts]), np.stack([p[4] for p in parts]),
+                 np.array([p[5] for p in parts], np.float32))
+        parts = [(p[0], p[1], torch.tensor([p[2]], dtype=torch.float32, device="cuda"))
+                 for p in parts]
+    else:
+        parts = [mem.memra_quantize_nvfp4(w.cuda()) for w in ws]
     codes = torch.stack([c for c, _, _ in parts])
     scales = torch.stack([s for _, s, _ in parts])
     gexp = torch.cat([g for _, _, g in parts])
+    if orc is not None:
+        return codes, scales, gexp, obank
     return codes, scales, gexp
 
 
@@ -143,7 +144,7 @@ def nvfp4_bank(mem, E, N, K, seed):
 @pytest.mark.parametrize("per_expert", [False, True])
 def test_nvfp4_moe_gemv_parity(mem, orc, gated, per_expert):
     E, N, K, top_k = 10, 200, 1024, 8
-    codes, scales, gexp = nvfp4_bank(mem, E, N, K, 610)
+    codes, scales, gexp, (oc, os_, og) = nvfp4_bank(mem, E, N, K, 610, orc)
     ids = torch.tensor([3, 9, 0, 7, 3, 5, 12, 1], dtype=torch.int32)   # 12 is out of range
     gw = torch.tensor([0.2, 0.15, 0.1, 0.1, 0.15, 0.1, 0.1, 0.1], dtype=torch.float32)
     x = synth.activations_bf16(top_k if per_expert else 1, K, 611)
@@ -164,12 +165,15 @@ def test_nvfp4_moe_gemv_parity(mem, orc, gated, per_expert):
                                        xq[k if per_expert else 0], xd[k if per_expert else 0])
             torch.cuda.synchronize()
             assert torch.equal(one.view(torch.int32), y[k].view(torch.int32)), k
-    oxq, oxd = np_(xq), np_(xd)
-    y_ref, bad = orc.moe_gemv_nvfp4(np_(codes), np_(scales), g_np, np_(ids),
+    # the oracle on its own quantisation of the generator's values (equal to the GPU's)
+    oxq, oxd = orc.quantize_q8_1(bf16_bits_np(x))
+    assert np.array_equal(np_(xq), oxq) and np.array_equal(np_(xd), oxd)
+    assert np.array_equal(g_np.view(np.uint32), og.view(np.uint32))
+    y_ref, bad = orc.moe_gemv_nvfp4(oc, os_, og, np_(ids),
                                     np_(gw) if gated else None, oxq if per_expert else oxq[0],
                                     oxd if per_expert else oxd[0], int(per_expert))
     assert bad == 1
-    terms = np.stack([nvfp4_terms(orc, np_(codes)[e], np_(scales)[e], g_np[e],
+    terms = np.stack([nvfp4_terms(orc, oc[e], os_[e], og[e],
                                   oxq[k:k + 1] if per_expert else oxq[:1],
                                   oxd[k:k + 1] if per_expert else oxd[:1])[0]
                       if e < E else np.zeros(N) for k, e in enumerate(ids.tolist())])

@@ -62,6 +62,23 @@ def test_noalloc_matches_workspace_entry_on_two_calls(mem):
         assert torch.equal(y.view(torch.int32), ref.view(torch.int32))   # in fact bit-identical
 
 
+def test_noalloc_at_the_size_limit(mem):
+    """top_k * 2F exactly fills the array (the kernels write its last float): the result
+    equals the workspace entry point's, bit for bit, on two calls in a row."""
+    E, H, F, top_k = 8, 256, 4096, 8
+    assert top_k * 2 * F == mem.MOE_NOALLOC_SCRATCH_FLOATS
+    for key in (3, 4):
+        gq, gd, dq, dd, ids, gw, x = layer(mem, E, H, F, top_k, key)
+        y = torch.full((H,), float("nan"), device="cuda")
+        mem.memra_q8_0_moe_ffn_noalloc(gq, gd, dq, dd, ids, gw, x, y)
+        ws = torch.full((top_k, 2 * F), float("nan"), device="cuda")
+        ref = mem.memra_q8_0_moe_ffn(gq, gd, dq, dd, ids, gw, x, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.isfinite(ws).all()          # every gate|up row was written
+        assert torch.isfinite(y).all()
+        assert torch.equal(y.view(torch.int32), ref.view(torch.int32)), key
+
+
 def test_noalloc_rejects_oversized_workspace(mem):
     E, H, F, top_k = 2, 64, 4128, 8     # top_k * 2F = 66048 > 65536 floats
     assert top_k * 2 * F > mem.MOE_NOALLOC_SCRATCH_FLOATS
