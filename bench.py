@@ -120,6 +120,22 @@ def build_dense_sweep(mem, device, M=1, layers=None, workload_id=1, fmt="q8_0"):
     return ops
 
 
+def sweep_rows_like(ops, M, workload_id=2):
+    """The products of a built dense sweep (same weight tensors, no new weights) with M
+    independent activation rows each, seeded like the verify workloads' activations."""
+    cfg = synth.DENSE27B
+    per_layer = len(cfg["gemvs"])
+    out = []
+    for i, op in enumerate(ops):
+        layer, t = divmod(i, per_layer)
+        K = op.x.shape[1]
+        x = synth.activations_bf16(M, K, workload_id, layer, t, 1000 + M,
+                                   outlier_frac=cfg["outlier_frac"],
+                                   outlier_scale=cfg["outlier_scale"], device=op.wq.device)
+        out.append(Gemv(op.wq, op.wd, x, op.name))
+    return out
+
+
 def build_gemv_4096(mem, device, copies=32):
     """One 4096x4096 GEMV (seed 0); `copies` distinct weight copies rotate so that the
     weights of consecutive calls are not L2 resident (32 x 17.8 MB >> 129 MB L2)."""
@@ -255,9 +271,16 @@ class MoeLayer:
                                            False, y=self.ygu, dev_status=self.status)
 
 
-def run_gemv_op(mem, op, quantize=True, fused=False):
+def mma_suits(op):
+    """Shapes the tensor-core entry point takes (K a multiple of 1024 up to 5120)."""
+    N, K = op.wq.shape
+    return op.fmt == "q8_0" and K % 1024 == 0 and K <= 5120 and N >= 16
+
+
+def run_gemv_op(mem, op, quantize=True, fused=False, mma=False):
     """One product of a step: the fused entry point (quantisation in the kernel's
-    prologue), or a q8_1 quantise launch followed by the GEMV / verify GEMM."""
+    prologue), or a q8_1 quantise launch followed by the GEMV / verify GEMM (with
+    `mma`, the tensor-core entry point where the shape suits it)."""
     if fused:
         if op.fmt != "q8_0":
             raise ValueError("the fused quantise entry point takes Q8_0 weights")
@@ -277,7 +300,9 @@ def run_gemv_op(mem, op, quantize=True, fused=False):
         else:
             mem.memra_q4_0_gemm_small_m(op.wq, op.wd, op.xq, op.xd, y=op.y)
         return
-    if op.xq.shape[0] == 1:
+    if mma and mma_suits(op):
+        mem.memra_q8_0_gemm_small_m_mma(op.wq, op.wd, op.xq, op.xd, y=op.y)
+    elif op.xq.shape[0] == 1:
         mem.memra_q8_0_gemv(op.wq, op.wd, op.xq[0], op.xd[0], y=op.y[0])
     else:
         mem.memra_q8_0_gemm_small_m(op.wq, op.wd, op.xq, op.xd, y=op.y)
@@ -286,15 +311,19 @@ def run_gemv_op(mem, op, quantize=True, fused=False):
 class Workload:
     """A step = a fixed list of library calls; captured once into a CUDA graph."""
 
-    def __init__(self, name, mem, device, layers=None, fused=False, chain=False):
+    def __init__(self, name, mem, device, layers=None, fused=False, chain=False, ops=None,
+                 mma=False):
         self.name = name
         self.fused = fused
+        self.mma = mma
         self.chain = None
         self.mem = mem
         self.device = device
         self.moe = None
         self.ops = []
-        if name == "dense27b_sweep":
+        if ops is not None:
+            self.ops = ops
+        elif name == "dense27b_sweep":
             self.ops = build_dense_sweep(mem, device, M=1, layers=layers)
         elif name == "dense27b_sweep_nvfp4":
             self.ops = build_dense_sweep(mem, device, layers=layers, workload_id=6, fmt="nvfp4")
@@ -397,7 +426,7 @@ class Workload:
                 m.run(self.mem, fused=self.fused)
         else:
             for op in self.ops:
-                run_gemv_op(self.mem, op, fused=self.fused)
+                run_gemv_op(self.mem, op, fused=self.fused, mma=self.mma)
 
     def gemv_only(self):
         """The step's weight-streaming kernels alone (activations already quantised)."""
@@ -417,7 +446,7 @@ class Workload:
                        y=m.y, dev_status=m.status)
         else:
             for op in self.ops:
-                run_gemv_op(self.mem, op, quantize=False, fused=self.fused)
+                run_gemv_op(self.mem, op, quantize=False, fused=self.fused, mma=self.mma)
 
     def inputs(self):
         if self.moe is not None:
@@ -692,6 +721,68 @@ def workload_config(name, wl):
     return cfg
 
 
+def time_step_and_products(wl, steps, warmup, stream):
+    """Seconds for `steps` CUDA-graph replays of the whole step and of its product
+    launches alone, after `warmup` replays of the step."""
+    step_graph = wl.capture(wl.step)
+    gemv_graph = wl.capture(wl.gemv_only)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step_graph.replay()
+    torch.cuda.synchronize(wl.device)
+    el = time_graph(step_graph, steps, stream)
+    gel = time_graph(gemv_graph, steps, stream)
+    return el, gel
+
+
+def measure_configs(mem, device, main_wl, stream, peak, warmup):
+    """Every other configuration of the benchmark on this GPU, each timed over a short
+    region (CUDA-graph replays, CUDA events on the launching stream): the 4096 x 4096
+    GEMV, the verify GEMMs at M = 2, 4, 8 on the dense sweep's own weights, the top-8
+    MoE layer sweep, and the LM head + down stress shapes at M = 1 and 8."""
+    legs = []
+    legs.append(("cfg0_gemv_4096", lambda: Workload("gemv_4096", mem, device), 200,
+                 "one call = q8_1 quantise + GEMV; 32 rotating weight copies (570 MB > L2)",
+                 32))
+    for M in (2, 4, 8):
+        legs.append(("cfg2_verify_m%d" % M,
+                     lambda M=M: Workload("verify_m%d" % M, mem, device,
+                                          ops=sweep_rows_like(main_wl.ops, M)), 10,
+                     "64-layer sweep, M = %d rows per product (the dense sweep's weights)" % M,
+                     None))
+    legs.append(("cfg3_moe_top8", lambda: Workload("moe_top8", mem, device, fused=True), 50,
+                 "48 routed layers (memra_q8_0_moe_ffn), top-8 of 128 experts, one token",
+                 None))
+    for M in (1, 8):
+        legs.append(("cfg4_lm_head_down_m%d" % M,
+                     lambda M=M: Workload("stress_lm_head", mem, device,
+                                          ops=build_stress(mem, device, M=M)), 50,
+                     "LM head 151936x5120 + down 5120x17408, M = %d, 1%% zero and 1%% x50 blocks"
+                     % M, None))
+    out = {}
+    for key, make, steps, what, calls in legs:
+        wl = make()
+        el, gel = time_step_and_products(wl, steps, warmup, stream)
+        b = wl.weight_bytes
+        us = el / steps * 1e6
+        gbs = b * steps / el / 1e9
+        d = {"what": what, "us_per_step": round(us, 2), "gb_s": round(gbs, 1),
+             "frac_of_measured": round(gbs / peak, 4),
+             "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+             "products_alone_gb_s": round(b * wl.passes * steps / gel / 1e9, 1),
+             "weight_bytes_per_step": b, "steps": steps,
+             "launches_per_step": wl.launches_per_step}
+        if calls:
+            d["us_per_call"] = round(us / calls, 3)
+        if wl.moe is not None:
+            d["tok_per_s"] = round(1e6 / us, 1)
+        out[key] = d
+        del wl
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_memra(args):
     world, rank, local = dist_info()
     if world > 1:
@@ -713,7 +804,7 @@ def run_memra(args):
                                                      "moe_top8_tokens16")
              else args.fused)
     wl = Workload(args.workload, mem, device, layers=args.layers, fused=fused,
-                  chain=args.chain)
+                  chain=args.chain, mma=args.mma)
     stream = torch.cuda.Stream(device)
     step_graph = wl.capture(wl.step)
     gemv_graph = wl.capture(wl.gemv_only)
@@ -797,6 +888,12 @@ def run_memra(args):
     e2e_s = max_over_ranks(e2e_s, world, backend_device=device)
     e2e_value = world * bytes_step * e2e_steps / e2e_s / 1e9
 
+    configs = None
+    if args.workload == "dense27b_sweep" and args.layers is None and not args.no_configs:
+        cs = ClockSampler(device)
+        configs = measure_configs(mem, device, wl, stream, peak, args.warmup)
+        configs["clocks"] = cs.stop()
+
     status_bad = 0
     if wl.moe is not None:
         status_bad = int(sum(int(m.status.item()) for m in wl.moe))
@@ -818,6 +915,9 @@ def run_memra(args):
             cfg["activation_quantise"] = ("in the chained kernel, after a grid barrier on the "
                                           "previous product (memra_q8_0_gemv_chain)")
         elif wl.moe is None:
+            if wl.mma:
+                cfg["products"] = ("memra_q8_0_gemm_small_m_mma (tensor cores) where K is a "
+                                   "multiple of 1024 up to 5120, else memra_q8_0_gemm_small_m")
             cfg["activation_quantise"] = ("fused into the product's prologue "
                                           "(memra_q8_0_quant_gemm)" if wl.fused else
                                           "separate memra_quantize_q8_1 launch")
@@ -855,6 +955,8 @@ def run_memra(args):
                              "by_ctas_per_sm": ceiling_per} if ceiling else None,
             "clocks": clock_info,
         }
+        if configs is not None:
+            line["configs"] = configs
         if status_bad:
             line["moe_status_flags"] = status_bad
         print(json.dumps(line), flush=True)
@@ -910,8 +1012,14 @@ def main(argv=None):
     ap.add_argument("--chain", action="store_true",
                     help="dense M = 1 workloads: the whole step as one memra_q8_0_gemv_chain "
                          "launch")
+    ap.add_argument("--mma", action="store_true",
+                    help="dense workloads: the tensor-core entry point "
+                         "(memra_q8_0_gemm_small_m_mma) for the products it takes")
     ap.add_argument("--unfused", action="store_true",
                     help="moe_top8: four calls per layer instead of memra_q8_0_moe_ffn")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="default workload: skip the short measurements of the other "
+                         "configurations")
     ap.add_argument("--no-read-ceiling", action="store_true",
                     help="skip the 4 GiB read-stream ceiling (profiling captures)")
     ap.add_argument("--layers", type=int, default=None,

@@ -65,6 +65,7 @@ _SIGS = {
     "memra_q4_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
     "memra_q4_0_moe_gemv": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p, _p],
     "memra_q8_0_gemm_small_m": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
+    "memra_q8_0_gemm_small_m_mma": [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p],
     "memra_q8_0_quant_gemm": [_p, _p, _i64, _i64, _i64, _p, _i32, _p, _p],
     "memra_q8_0_moe_gemv": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _p, _i32, _p, _p, _p],
     "memra_q8_0_moe_gemv_tokens": [_p, _p, _i64, _i64, _i64, _p, _p, _i64, _i64, _p, _p, _i32,
@@ -278,6 +279,27 @@ def memra_q8_0_gemm_small_m(wq, wd, xq, xd, y=None):
         _check("memra_q8_0_gemm_small_m",
                lib().memra_q8_0_gemm_small_m(_ptr(wq), _ptr(wd), N, K, M, _ptr(xq), _ptr(xd),
                                              _ptr(y), _stream(wq)))
+    return y
+
+
+def memra_q8_0_gemm_small_m_mma(wq, wd, xq, xd, y=None):
+    """memra_q8_0_gemm_small_m with the block sums on the tensor cores (bit-identical
+    results; K a multiple of 1024 up to 5120, N >= 16)."""
+    _need(wq, "wq", torch.int8)
+    N, K = wq.shape
+    dev = wq.device
+    _need(wd, "wd", torch.float16, dev, (N, K // 32))
+    _need(xq, "xq", torch.int8, dev)
+    M = xq.shape[0]
+    _need(xq, "xq", torch.int8, dev, (M, K))
+    _need(xd, "xd", torch.float32, dev, (M, K // 32))
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, dev, (M, N))
+    with torch.cuda.device(dev):
+        _check("memra_q8_0_gemm_small_m_mma",
+               lib().memra_q8_0_gemm_small_m_mma(_ptr(wq), _ptr(wd), N, K, M, _ptr(xq),
+                                                 _ptr(xd), _ptr(y), _stream(wq)))
     return y
 
 

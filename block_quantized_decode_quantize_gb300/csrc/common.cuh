@@ -319,6 +319,12 @@ cudaError_t allow_dynamic_smem(Kern kernel, size_t smem, const DeviceInfo& info)
                               info.max_smem_optin);
 }
 
+// The tensor-core product of M = 1..8 activation rows (mma.cu).  Returns
+// MEMRA_ERR_UNSUPPORTED, having launched nothing, when the shape or the alignment does
+// not suit it (K a multiple of 1024, N >= 16, 16-byte aligned planes and activations).
+memra_status run_mma_product(const int8_t* wq, const uint16_t* wd, int64_t N, int64_t K, int M,
+                             const int8_t* xq, const float* xd, float* y, cudaStream_t stream);
+
 // Programmatic dependent launch is on unless the environment sets MEMRA_PDL=0
 // (read once per process).
 bool pdl_enabled();

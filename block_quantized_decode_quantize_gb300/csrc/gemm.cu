@@ -1107,10 +1107,15 @@ int gemv_path_override() {
     const char* e = std::getenv("MEMRA_GEMV_PATH");
     if (e && std::strcmp(e, "reg") == 0) return 1;
     if (e && std::strcmp(e, "tma") == 0) return 2;
+    if (e && std::strcmp(e, "mma") == 0) return 3;
     return 0;
   }();
   return v;
 }
+
+// The tensor-core kernel (mma.cu) takes dense products only when MEMRA_GEMV_PATH=mma:
+// on GB300 it does not beat the CUDA-core kernels (memra_q8_0_gemm_small_m_mma).
+bool use_mma() { return gemv_path_override() == 3; }
 
 int64_t max_units_per_cta(int64_t units, int64_t grid) { return (units + grid - 1) / grid; }
 
@@ -1365,6 +1370,11 @@ extern "C" memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t
     return MEMRA_ERR_ALIGNMENT;
   if (!x_fits(pass_rows(M), K)) return MEMRA_ERR_UNSUPPORTED;
   return in_passes(M, [&](int64_t m0, int64_t rows) {
+    if (use_mma()) {
+      const memra_status st = run_mma_product(wq, wd, N, K, (int)rows, xq + m0 * K,
+                                              xd + m0 * (K / 32), y + m0 * N, stream);
+      if (st != MEMRA_ERR_UNSUPPORTED) return st;
+    }
     Params p{};
     p.wq = wq;
     p.wd = wd;
@@ -1376,6 +1386,26 @@ extern "C" memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t
     p.y = y + m0 * N;
     p.units = N;
     return dispatch_m<kDense, kXq8>(p, (int)rows, stream);
+  });
+}
+
+extern "C" memra_status memra_q8_0_gemm_small_m_mma(const int8_t* wq, const uint16_t* wd,
+                                                    int64_t N, int64_t K, int64_t M,
+                                                    const int8_t* xq, const float* xd, float* y,
+                                                    cudaStream_t stream) {
+  if (N < 0 || K < 0 || M < 0 || K % 32 != 0) return MEMRA_ERR_INVALID_ARG;
+  if (M > MEMRA_MAX_M) return MEMRA_ERR_UNSUPPORTED;
+  if (N > INT32_MAX || K > INT32_MAX) return MEMRA_ERR_UNSUPPORTED;
+  if (N == 0 || M == 0) return MEMRA_OK;
+  if (!y) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(y, 4)) return MEMRA_ERR_ALIGNMENT;
+  if (K == 0) return zero_fill(y, M * N, stream);
+  if (!wq || !wd || !xq || !xd) return MEMRA_ERR_INVALID_ARG;
+  if (!aligned(wq, 16) || !aligned(wd, 16) || !aligned(xq, 16) || !aligned(xd, 16))
+    return MEMRA_ERR_ALIGNMENT;
+  return in_passes(M, [&](int64_t m0, int64_t rows) {
+    return run_mma_product(wq, wd, N, K, (int)rows, xq + m0 * K, xd + m0 * (K / 32),
+                           y + m0 * N, stream);
   });
 }
 

@@ -119,6 +119,25 @@ memra_status memra_q8_0_gemm_small_m(const int8_t* wq, const uint16_t* wd, int64
                                      cudaStream_t stream);
 
 /*
+ * memra_q8_0_gemm_small_m with the exact int32 block sums formed on the tensor cores
+ * (one int8 mma.sync m16n8k32 per 32-element block of 16 weight rows and up to 8
+ * activation rows) instead of dp4a.  The pages credit memra with an int8 tensor-core
+ * GEMM (memra wiki, feature list); the workload definition allows tensor cores for the
+ * verify GEMM only where they beat the CUDA-core path.  On GB300 they do not (the
+ * int8 MMA rate equals the dp4a rate, and the kernel is latency-bound), so
+ * memra_q8_0_gemm_small_m does not use this kernel; it is kept as an explicit entry
+ * point for comparison.  The fp32 arithmetic around the block sums is the library's
+ * one order, so y is bit-identical to memra_q8_0_gemm_small_m for every row.
+ * Same arguments and results as memra_q8_0_gemm_small_m, with narrower support:
+ * K a multiple of 1024 and at most 5120, N >= 16, wq, wd, xq, xd 16-byte aligned;
+ * other shapes return MEMRA_ERR_UNSUPPORTED (misaligned pointers MEMRA_ERR_ALIGNMENT)
+ * and launch nothing.  Empty sizes and K = 0 behave as in memra_q8_0_gemm_small_m.
+ */
+memra_status memra_q8_0_gemm_small_m_mma(const int8_t* wq, const uint16_t* wd, int64_t N,
+                                         int64_t K, int64_t M, const int8_t* xq,
+                                         const float* xd, float* y, cudaStream_t stream);
+
+/*
  * Q4_0 weights, the pages' other split-plane decode format (memra wiki, feature
  * list, which names NVFP4, Q4_0 and Q8_0 decode through split-plane matvecs).  The
  * pages print nothing of it; this library's reading is GGUF's Q4_0 block: 32 consecutive

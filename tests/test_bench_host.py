@@ -80,3 +80,20 @@ def test_workload_rows_and_tokens():
 def test_unknown_workload_is_rejected():
     with pytest.raises(SystemExit):
         bench.main(["--workload", "no_such_workload"])
+
+
+def test_verify_legs_share_the_sweep_weights():
+    """The verify configurations reuse the dense sweep's weight tensors (no second copy)
+    with M seeded activation rows per product."""
+    ops = []
+    for t, (name, N, K) in enumerate((("a", 8, 64), ("b", 4, 64), ("c", 16, 64), ("d", 4, 128))):
+        wq = torch.zeros((N, K), dtype=torch.int8)
+        wd = torch.zeros((N, K // 32), dtype=torch.float16)
+        ops.append(bench.Gemv(wq, wd, torch.zeros((1, K), dtype=torch.bfloat16), name))
+    rows = bench.sweep_rows_like(ops, 4)
+    assert len(rows) == len(ops)
+    for a, b in zip(ops, rows):
+        assert b.wq.data_ptr() == a.wq.data_ptr() and b.wd.data_ptr() == a.wd.data_ptr()
+        assert b.x.shape == (4, a.x.shape[1]) and b.y.shape == (4, a.wq.shape[0])
+    again = bench.sweep_rows_like(ops, 4)
+    assert all(torch.equal(p.x, q.x) for p, q in zip(rows, again))   # seeded

@@ -110,7 +110,7 @@ def run_pair(mem, orc, N, K, M, seed, x_dtype=torch.bfloat16, outliers=0.001):
 
 
 @pytest.mark.parametrize("N,K", [(1003, 1184), (257, 17408), (4096, 4096), (64, 32),
-                                 (130, 768), (1, 5120)])
+                                 (130, 768), (1, 5120), (1000, 3072), (40, 2048)])
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_gemm_parity(mem, orc, N, K, M):
     (wq, wd, xq, xd), (oq, od, oxq, oxd) = run_pair(mem, orc, N, K, M, seed=N * 31 + K + M)
@@ -124,6 +124,38 @@ def test_gemm_parity(mem, orc, N, K, M):
     y_ref = orc.gemm(oq, od, oxq, oxd)
     terms = abs_terms(orc.block_dots(oq, oxq), od, oxd)
     assert_within(np_(y.view), y_ref, terms, "gemm N=%d K=%d M=%d" % (N, K, M))
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (1000, 3072), (40, 2048), (777, 5120),
+                                 (17, 1024), (16, 2048)])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 11, 16])
+def test_tensor_core_gemm_parity(mem, orc, N, K, M):
+    """The tensor-core entry point: against the oracle, and bit for bit the CUDA-core
+    product (every row, one and two weight passes; tiles of 16 rows moved back at the
+    end of a CTA's rows, N = 16 and 17 included)."""
+    (wq, wd, xq, xd), (oq, od, oxq, oxd) = run_pair(mem, orc, N, K, M, seed=N * 7 + K + M)
+    y = Guarded((M, N), torch.float32)
+    mem.memra_q8_0_gemm_small_m_mma(wq, wd, xq, xd, y=y.view)
+    ref = mem.memra_q8_0_gemm_small_m(wq, wd, xq, xd)
+    torch.cuda.synchronize()
+    assert y.intact()
+    assert_within(np_(y.view), orc.gemm(oq, od, oxq, oxd),
+                  abs_terms(orc.block_dots(oq, oxq), od, oxd), "mma N=%d K=%d M=%d" % (N, K, M))
+    assert torch.equal(y.view.view(torch.int32), ref.view(torch.int32))
+
+
+@pytest.mark.parametrize("N,K", [(4096, 17408), (15, 1024), (100, 1056)])
+def test_tensor_core_gemm_refuses_other_shapes(mem, N, K):
+    wq = torch.zeros((N, K), dtype=torch.int8, device="cuda")
+    wd = torch.zeros((N, K // 32), dtype=torch.float16, device="cuda")
+    xq = torch.zeros((2, K), dtype=torch.int8, device="cuda")
+    xd = torch.zeros((2, K // 32), dtype=torch.float32, device="cuda")
+    y = torch.full((2, N), 5.0, device="cuda")
+    with pytest.raises(mem.MemraError) as e:
+        mem.memra_q8_0_gemm_small_m_mma(wq, wd, xq, xd, y=y)
+    assert e.value.status == 3
+    torch.cuda.synchronize()
+    assert bool((y == 5.0).all())
 
 
 def test_rows_do_not_depend_on_m(mem, orc):

@@ -1,9 +1,12 @@
-"""The two product kernels (shared-memory bulk-copy stream and register stream)
-implement one summation order, so they must agree bit for bit.  Each child process
-pins the kernel choice with MEMRA_GEMV_PATH (read once per process): the default
-selection, the register kernel everywhere, and the bulk-copy kernel wherever it
-applies (also for M > 1).  The shapes include products with many ring stages per
-CTA (12289 x 4096 ends in a one-row stage; 5120 x 17408 has one-row stages)."""
+"""The product kernels (shared-memory bulk-copy stream, register stream, and the
+tensor-core kernel for several activation rows) implement one summation order, so they
+must agree bit for bit.  Each child process pins the kernel choice with
+MEMRA_GEMV_PATH (read once per process): the default selection, the register kernel
+everywhere, the bulk-copy kernel wherever it applies (also for M > 1), and the
+tensor-core kernel wherever it applies (also for M = 1).  The shapes include products
+with many ring stages per CTA (12289 x 4096 ends in a one-row stage; 5120 x 17408 has
+one-row stages), tensor-core tiles moved back over the previous tile (N = 17, 40, 1000
+rows), a single 16-row tile (N = 16), and two-pass batches (M = 11, 16)."""
 import os
 import subprocess
 import sys
@@ -22,7 +25,9 @@ import synth
 import block_quantized_decode_quantize_gb300 as mem
 out = {}
 for (N, K, M) in [(1003, 4096, 1), (777, 5120, 1), (513, 2048, 4), (300, 5120, 8), (4100, 768, 1),
-                  (64, 17408, 1), (12289, 4096, 1), (5120, 17408, 1), (12289, 4096, 2)]:
+                  (64, 17408, 1), (12289, 4096, 1), (5120, 17408, 1), (12289, 4096, 2),
+                  (1000, 1024, 3), (16, 1024, 8), (17, 2048, 5), (40, 3072, 7),
+                  (5120, 5120, 16), (4096, 4096, 11), (2050, 17408, 8)]:
     w = synth.weights_fp32(N, K, 70, N, K, device="cuda")
     x = synth.activations_bf16(M, K, 71, N, K, M, outlier_frac=0.001, device="cuda")
     wq, wd = mem.memra_quantize_q8_0(w)
@@ -58,13 +63,13 @@ def run_child(tmp_path, env_path):
     return torch.load(path)
 
 
-def test_tma_and_register_kernels_agree_bitwise(tmp_path):
+def test_product_kernels_agree_bitwise(tmp_path):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from block_quantized_decode_quantize_gb300 import build
     build.build()
     a = run_child(tmp_path, None)
-    for other in ("reg", "tma"):
+    for other in ("reg", "tma", "mma"):
         b = run_child(tmp_path, other)
         assert a.keys() == b.keys()
         for k in a:
