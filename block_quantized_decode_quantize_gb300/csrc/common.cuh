@@ -260,8 +260,14 @@ __device__ __forceinline__ float exp_cody_waite(float x) {
   return __fmul_rn(p, __int_as_float((k + 127) << 23));
 }
 
-// h[i] = (g[i] / (1 + exp(-g[i]))) * u[i] for 8 consecutive values, each fp32
-// operation rounded once in that order (SwiGLU of the routed-expert FFN).
+// h = (g / (1 + exp(-g))) * u, each fp32 operation rounded once in that order (SwiGLU
+// of the routed-expert FFN).
+__device__ __forceinline__ float swiglu1(float g, float u) {
+  const float den = __fadd_rn(1.0f, exp_cody_waite(-g));
+  return __fmul_rn(__fdiv_rn(g, den), u);
+}
+
+// swiglu1 of 8 consecutive values.
 __device__ __forceinline__ void swiglu8(const float* g, const float* u, float h[8]) {
   const float4 g0 = *reinterpret_cast<const float4*>(g);
   const float4 g1 = *reinterpret_cast<const float4*>(g + 4);
@@ -270,11 +276,7 @@ __device__ __forceinline__ void swiglu8(const float* g, const float* u, float h[
   const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
   const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float den = __fadd_rn(1.0f, exp_cody_waite(-gv[i]));
-    const float sg = __fdiv_rn(gv[i], den);
-    h[i] = __fmul_rn(sg, uv[i]);
-  }
+  for (int i = 0; i < 8; ++i) h[i] = swiglu1(gv[i], uv[i]);
 }
 
 // 8 bf16 values (16 bytes) to fp32, exactly.

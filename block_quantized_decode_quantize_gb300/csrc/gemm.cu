@@ -180,6 +180,11 @@ struct Params {
   // Gated routed product whose CTA takes all of its top_k segments (rps rows each at
   // most) in one packed stage: segment k's rows at stage rows [k*n, (k+1)*n).
   int packed;
+  // Ungated routed product over gate|up pairs (the routed FFN's first launch): each
+  // expert has 2N rows, gate rows 0..N-1 and up rows N..2N-1, and unit (k, j) is the pair
+  // (gate j, up j) of slot k.  A stage holds n gate rows, then the same n up rows; the
+  // epilogue writes y[k][j] = silu(g) u and y[k][N + j] = u (y: [slots][2N]).
+  int pairs;
   // TMA kernel layout
   int rps;                 // rows per stage
   int ns;                  // stages in the ring
@@ -196,7 +201,7 @@ template <int XIN>
 __device__ __forceinline__ const void* xin_row(const void* xin, int64_t row, int64_t K) {
   if (XIN == kXbf16) return static_cast<const uint16_t*>(xin) + row * K;
   if (XIN == kXf32) return static_cast<const float*>(xin) + row * K;
-  return static_cast<const float*>(xin) + row * 2 * K;
+  return static_cast<const float*>(xin) + row * 2 * K;  // kXswiglu, kXhalf: rows of 2K
 }
 
 struct Seg {
@@ -239,12 +244,13 @@ __device__ __forceinline__ Seg get_seg(const Params& p, int64_t u0, int64_t u1, 
     const int64_t lo = (u0 > k * p.N ? u0 : k * p.N) - k * p.N;
     const int64_t hi = (u1 < (k + 1) * p.N ? u1 : (k + 1) * p.N) - k * p.N;
     const int e = s_ids[k];
+    const int64_t er = p.pairs ? 2 * p.N : p.N;  // weight rows (and outputs) per slot
     g.k = (int)k;
     g.valid = e >= 0;
-    g.row0 = (int64_t)(e < 0 ? 0 : e) * p.N + lo;
+    g.row0 = (int64_t)(e < 0 ? 0 : e) * er + lo;
     g.nrows = (int)(hi - lo);
     g.xrow = p.xpe ? (int)(p.xdiv > 1 ? k / p.xdiv : k) : 0;
-    g.out0 = k * p.N + lo;
+    g.out0 = k * er + lo;
   }
   return g;
 }
@@ -390,16 +396,21 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         const Seg g = get_seg<MODE>(p, u0, u1, cur_si, s_ids);
         if (!g.valid || cur_r0 >= g.nrows) {
           if (!g.valid && MODE == kMoeUngated)
-            for (int i = lane; i < g.nrows; i += 32) p.y[g.out0 + i] = 0.0f;
+            for (int i = lane; i < g.nrows; i += 32) {
+              p.y[g.out0 + i] = 0.0f;
+              if (p.pairs) p.y[g.out0 + p.N + i] = 0.0f;
+            }
           ++cur_si;
           cur_r0 = 0;
           continue;
         }
+        // A pairs stage takes rps / 2 pairs: rps rows.
+        const int step = MODE == kMoeUngated && p.pairs ? p.rps / 2 : p.rps;
         m.seg = cur_si;
         m.r0 = cur_r0;
-        m.nr = min(p.rps, g.nrows - cur_r0);
+        m.nr = min(step, g.nrows - cur_r0) * (MODE == kMoeUngated && p.pairs ? 2 : 1);
         m.xrow = g.xrow - xlo;
-        cur_r0 += p.rps;
+        cur_r0 += step;
         return true;
       }
       return false;
@@ -428,6 +439,26 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         return;
       }
       const Seg g = seg_of(mt.seg);
+      if (MODE == kMoeUngated && p.pairs) {
+        // Rows [0, n) are gate rows j, rows [n, 2n) the same up rows (M == 1).
+        const int n = mt.nr / 2;
+        for (int i = lane; i < n; i += 32) {
+          float tg = pp[(size_t)i * S];
+          float tu = pp[(size_t)(n + i) * S];
+          for (int s = 1; s < S; ++s) {
+            tg = __fadd_rn(tg, pp[(size_t)i * S + s]);
+            tu = __fadd_rn(tu, pp[(size_t)(n + i) * S + s]);
+          }
+          if (FMT == kNv4) {
+            tg = __fmul_rn(s_gsc[g.k], tg);
+            tu = __fmul_rn(s_gsc[g.k], tu);
+          }
+          p.y[g.out0 + mt.r0 + i] = swiglu1(tg, tu);
+          p.y[g.out0 + p.N + mt.r0 + i] = tu;
+        }
+        __syncwarp();
+        return;
+      }
       for (int i = lane; i < mt.nr * M; i += 32) {
         const int r = i / M;
         const int m = i - r * M;
@@ -468,8 +499,22 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
           const uint32_t db = (uint32_t)(m->nr * nb * 2);
           const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
           mbar_arrive_expect_tx(full_bar(slot), qb + db);
-          bulk_g2s_hint(dst, p.wq + (g.row0 + m->r0) * p.qrow, qb, full_bar(slot), policy);
-          bulk_g2s_hint(dst + p.wd_off, p.wd + (g.row0 + m->r0) * nb, db, full_bar(slot), policy);
+          if (MODE == kMoeUngated && p.pairs) {
+            // n gate rows, then the n up rows N further on.
+            const int n = m->nr / 2;
+            const int64_t gr = g.row0 + m->r0;
+            const int64_t ur = gr + p.N;
+            bulk_g2s_hint(dst, p.wq + gr * p.qrow, qb / 2, full_bar(slot), policy);
+            bulk_g2s_hint(dst + (uint32_t)(n * p.qrow), p.wq + ur * p.qrow, qb / 2, full_bar(slot),
+                          policy);
+            bulk_g2s_hint(dst + p.wd_off, p.wd + gr * nb, db / 2, full_bar(slot), policy);
+            bulk_g2s_hint(dst + p.wd_off + (uint32_t)(n * nb * 2), p.wd + ur * nb, db / 2,
+                          full_bar(slot), policy);
+          } else {
+            bulk_g2s_hint(dst, p.wq + (g.row0 + m->r0) * p.qrow, qb, full_bar(slot), policy);
+            bulk_g2s_hint(dst + p.wd_off, p.wd + (g.row0 + m->r0) * nb, db, full_bar(slot),
+                          policy);
+          }
         } else {
           meta[slot] = StageMeta{0, 0, 0, 0};  // sentinel: no more stages
           mbar_arrive(full_bar(slot));
@@ -554,6 +599,12 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       const float nan = __int_as_float(0x7fc00000);
       if (MODE == kMoeGated) {
         for (int64_t i = lane; i < u1 - u0; i += 32) p.y[u0 + i] = nan;
+      } else if (MODE == kMoeUngated && p.pairs) {
+        for (int64_t i = u0 + lane; i < u1; i += 32) {
+          const int64_t k = i / p.N;
+          p.y[i + k * p.N] = nan;          // k * 2N + j
+          p.y[i + k * p.N + p.N] = nan;
+        }
       } else if (MODE == kMoeUngated) {
         for (int64_t i = u0 + lane; i < u1; i += 32) p.y[i] = nan;
       } else {
@@ -1133,11 +1184,13 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   if (XIN == kXq8 && (!aligned(p.xd, 16) || !aligned(p.xq, 16))) return false;
   const size_t row_bytes = (size_t)p.qrow + (size_t)p.nb * 2;
   const int64_t maxu = max_units_per_cta(p.units, grid);
+  const bool pairs = MODE == kMoeUngated && p.pairs;
+  const int64_t upr = pairs ? 2 : 1;  // weight rows per unit
   // A routed product whose CTA share is a few stages long (one token's slots) takes
   // smaller stages; batches of tokens, with shares many stages long, keep the
   // dense size.
   const bool short_routed =
-      MODE != kDense && (size_t)maxu * row_bytes <= 4 * tune.stage_target;
+      MODE != kDense && (size_t)(maxu * upr) * row_bytes <= 4 * tune.stage_target;
   const size_t target = M > 1 ? tune.multi_stage_target
                         : (short_routed ? tune.routed_stage_target : tune.stage_target);
   int rps = (int)std::max<size_t>(1, target /
@@ -1145,8 +1198,10 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   // A stage never spans two segments, and no segment is longer than a CTA's share
   // of the units (routed: of one expert's rows): size stages, and so the ring's
   // depth, by what a stage can actually hold.
-  rps = (int)std::min<int64_t>(rps, MODE == kMoeUngated ? std::min<int64_t>(maxu, p.N) : maxu);
+  rps = (int)std::min<int64_t>(
+      rps, MODE == kMoeUngated ? upr * std::min<int64_t>(maxu, p.N) : maxu);
   rps = std::max(R, rps / R * R);
+  if (pairs) rps = std::max(2, rps / 2 * 2);  // whole pairs: n gate rows and n up rows
   // Gated routed products whose segments are a few rows each pack all of a CTA's
   // segments into one stage.
   p.packed = 0;
@@ -1276,7 +1331,8 @@ memra_status run_product(Params p, cudaStream_t stream) {
     return launch(q8_tma_kernel<M, R, MODE, XIN, FMT>, grid, tma_threads(M), smem, stream, info,
                   p);
   }
-  if (FMT != kQ8) return MEMRA_ERR_UNSUPPORTED;  // 4-bit formats run on the bulk-copy kernel only
+  // 4-bit formats and gate|up pairs run on the bulk-copy kernel only.
+  if (FMT != kQ8 || p.pairs) return MEMRA_ERR_UNSUPPORTED;
   grid = std::min<int64_t>(p.units, (int64_t)info.sms * reg_grid_ctas_per_sm(M));
   if (plan_reg<M, R, MODE, XIN>(p, info, grid, &smem))
     return launch(q8_reg_kernel<M, R, MODE, XIN>, grid, kRegThreads, smem, stream, info, p);
@@ -1759,11 +1815,12 @@ memra_status moe_ffn(const int8_t* gu_q, const uint16_t* gu_d, const int8_t* dn_
       !aligned(workspace, 16))
     return MEMRA_ERR_ALIGNMENT;
   if (!x_fits(1, H) || !x_fits(top_k, F)) return MEMRA_ERR_UNSUPPORTED;
-  // gate|up rows of every selected expert: workspace[k][0, 2F) = W_gu[ids[k]] x.
+  // gate|up of every selected expert, as (gate j, up j) pairs: workspace[k][j] =
+  // silu(g_j) u_j and workspace[k][F + j] = u_j, with (g, u) = W_gu[ids[k]] x.
   Params a{};
   a.wq = gu_q;
   a.wd = gu_d;
-  a.N = 2 * F;
+  a.N = F;
   a.K = H;
   a.xin = x;
   a.xrows = 1;
@@ -1774,12 +1831,25 @@ memra_status moe_ffn(const int8_t* gu_q, const uint16_t* gu_d, const int8_t* dn_
   a.xpe = 0;
   a.status = dev_status;
   a.gexp = ggu;
-  a.units = top_k * 2 * F;
-  memra_status st = dtype == MEMRA_BF16
-                        ? run_product<1, 1, kMoeUngated, kXbf16, FMT>(a, stream)
-                        : run_product<1, 1, kMoeUngated, kXf32, FMT>(a, stream);
+  a.pairs = 1;
+  a.units = top_k * F;
+  auto gate_up = [&](const Params& q) {
+    return dtype == MEMRA_BF16 ? run_product<1, 1, kMoeUngated, kXbf16, FMT>(q, stream)
+                               : run_product<1, 1, kMoeUngated, kXf32, FMT>(q, stream);
+  };
+  memra_status st = gate_up(a);
+  const bool paired = st != MEMRA_ERR_UNSUPPORTED;
+  if (!paired) {
+    // Shapes the bulk-copy kernel does not take: plain gate|up rows (workspace[k][0, 2F)
+    // = W_gu[ids[k]] x), SwiGLU in the down launch's prologue.
+    a.N = 2 * F;
+    a.pairs = 0;
+    a.units = top_k * 2 * F;
+    st = gate_up(a);
+  }
   if (st != MEMRA_OK) return st;
-  // down rows with SwiGLU + q8_1 of each expert's gate|up row in the prologue.
+  // down rows with q8_1 of each expert's SwiGLU row (paired) or SwiGLU + q8_1 of its
+  // gate|up row in the prologue.
   Params b{};
   b.wq = dn_q;
   b.wd = dn_d;
@@ -1797,6 +1867,7 @@ memra_status moe_ffn(const int8_t* gu_q, const uint16_t* gu_d, const int8_t* dn_
   b.routing_ready = 1;  // the gate|up kernel above waited for the routing
   b.gexp = gdn;
   b.units = H;
+  if (paired) return run_product<1, 1, kMoeGated, kXhalf, FMT>(b, stream);
   return run_product<1, 1, kMoeGated, kXswiglu, FMT>(b, stream);
 }
 

@@ -89,8 +89,9 @@ __device__ __forceinline__ float block_term_acc(float acc, uint16_t dw_bits, flo
 }
 
 // Activation input of a product: q8_1 planes, or values quantised in the kernel's
-// prologue (bf16, fp32, or SwiGLU of an fp32 gate|up row pair).
-enum XIn { kXq8 = 0, kXbf16 = 1, kXf32 = 2, kXswiglu = 3 };
+// prologue (bf16, fp32, SwiGLU of an fp32 gate|up row pair, or the first K floats of
+// fp32 rows of 2K floats: the SwiGLU rows a paired gate|up product writes).
+enum XIn { kXq8 = 0, kXbf16 = 1, kXf32 = 2, kXswiglu = 3, kXhalf = 4 };
 
 // The 8 activation values of group g (row-major [rows][K], K % 8 == 0).
 template <int XIN>
@@ -99,6 +100,10 @@ __device__ __forceinline__ void load_x_group(const void* xin, int g, int K, floa
     load8_bf16(static_cast<const uint16_t*>(xin) + (size_t)g * 8, v);
   } else if (XIN == kXf32) {
     load8_f32(static_cast<const float*>(xin) + (size_t)g * 8, v);
+  } else if (XIN == kXhalf) {
+    const int gpr = K / 8;
+    const int row = g / gpr;
+    load8_f32(static_cast<const float*>(xin) + (size_t)row * 2 * K + (g - row * gpr) * 8, v);
   } else {
     const int gpr = K / 8;
     const int row = g / gpr;

@@ -338,18 +338,21 @@ memra_status memra_swiglu_quantize_q8_1(const float* gu, int64_t R, int64_t F, i
 
 /*
  * One routed-expert FFN layer for one token, in two kernels:
- *   y = sum_k gate_w[k] * W_dn[ids[k]] q8_1( swiglu( W_gu[ids[k]] q8_1(x) ) ),
- * with the gate|up product quantising x in its prologue and the down product
- * computing SwiGLU and its q8_1 quantisation of each expert's gate|up row in its
- * own prologue (the same arithmetic as memra_swiglu_quantize_q8_1).  Bit-identical
- * to memra_quantize_q8_1, memra_q8_0_moe_gemv (no gate weights, shared x),
- * memra_swiglu_quantize_q8_1 and memra_q8_0_moe_gemv (gate weights, x per expert)
- * run in sequence.
+ *   y = sum_k gate_w[k] * W_dn[ids[k]] q8_1( swiglu( W_gu[ids[k]] q8_1(x) ) ).
+ * The gate|up product quantises x in its prologue and streams each expert's gate row
+ * j together with its up row j, so that its epilogue computes h_j = silu(g_j) u_j once
+ * per row (the arithmetic of memra_swiglu_quantize_q8_1); the down product quantises
+ * the h rows to q8_1 in its prologue.  Bit-identical to memra_quantize_q8_1,
+ * memra_q8_0_moe_gemv (no gate weights, shared x), memra_swiglu_quantize_q8_1 and
+ * memra_q8_0_moe_gemv (gate weights, x per expert) run in sequence.
  *   gu_q [E][2F][H], gu_d [E][2F][H/32]: gate rows [0, F), up rows [F, 2F).
  *   dn_q [E][H][F], dn_d [E][H][F/32].  x [H] (dtype bf16 bits or fp32, 16-byte
  *   aligned).  ids, gate_w [top_k] (device).  y fp32 [H].
- *   workspace: caller-allocated device fp32 [top_k][2F], 16-byte aligned; it holds
- *   the gate|up outputs between the two kernels and keeps them after the call.
+ *   workspace: caller-allocated device fp32 [top_k][2F], 16-byte aligned.  After the
+ *   call row k holds [h (F floats) | up (F floats)] of slot k, h = silu(gate) * up.
+ *   (Shapes the bulk-copy kernel does not take, K % 256 != 0 or planes not 16-byte
+ *   aligned, run unpaired: row k then holds [gate | up] and the down product computes
+ *   SwiGLU in its prologue; the result y is the same.)
  * Bad ids behave as in memra_q8_0_moe_gemv.  H % 32 == 0, F % 32 == 0.
  */
 memra_status memra_q8_0_moe_ffn(const int8_t* gu_q, const uint16_t* gu_d, const int8_t* dn_q,
@@ -490,7 +493,7 @@ memra_status memra_nvfp4_moe_ffn_tokens(const uint8_t* gu_codes, const uint8_t* 
  *   - Every call shares the one array.  Calls that may overlap on the GPU (on
  *     different streams, or before an earlier one has finished on another stream)
  *     race on it; keep such calls on one stream.  The array keeps the last call's
- *     gate|up outputs; nothing in it needs clearing because each call writes every
+ *     workspace rows; nothing in it needs clearing because each call writes every
  *     element it later reads.
  */
 #define MEMRA_MOE_NOALLOC_SCRATCH_FLOATS 65536

@@ -183,8 +183,24 @@ def test_layer_matches_oracle(mem, orc, fmt, T):
         # gate|up: every selected expert's rows within the product tolerance
         pr = [oracle_product(orc, fmt, gu_o, e, xq, xd) for e in sel]
         ygu_ref = np.stack([p[0][0] for p in pr])
-        assert_within(ygu[t], ygu_ref, np.stack([p[1][0] for p in pr]),
-                      "%s gate|up t=%d" % (fmt, t))
+        tol = 1e-4 * np.stack([p[1][0] for p in pr]) + 1e-6
+        if T > 1:  # the batched layer keeps the gate|up rows
+            assert_within(ygu[t], ygu_ref, np.stack([p[1][0] for p in pr]),
+                          "%s gate|up t=%d" % (fmt, t))
+        else:
+            # the single-token layer keeps [silu(g) u | u]: the up rows within the
+            # product tolerance, the SwiGLU rows within what the tolerances of g and u
+            # allow (|silu'| <= 1.1) plus a few roundings
+            assert_within(ygu[t][:, F:], ygu_ref[:, F:], np.stack([p[1][0] for p in pr])[:, F:],
+                          "%s up t=%d" % (fmt, t))
+            gr = ygu_ref[:, :F].astype(np.float64)
+            ur = ygu_ref[:, F:].astype(np.float64)
+            h_ref = orc.swiglu(ygu_ref).astype(np.float64)
+            tg, tu = tol[:, :F], tol[:, F:]
+            bound = (1.1 * tg * (np.abs(ur) + tu) + (np.abs(gr / (1 + np.exp(-gr))) + 1.1 * tg) * tu
+                     + 1e-6 * np.abs(h_ref) + 1e-30)
+            err = np.abs(ygu[t][:, :F].astype(np.float64) - h_ref)
+            assert np.all(err <= bound), (fmt, "swiglu rows", float((err - bound).max()))
         # down from the oracle's own SwiGLU rows; gated sum in ascending k from 0
         hq, hd = orc.swiglu_quantize_q8_1(ygu_ref)
         y_ref = np.zeros(H, np.float32)

@@ -493,7 +493,12 @@ def test_moe_ffn_matches_four_step_pipeline(mem, orc, dtype, E, H, F, top_k):
     y4 = mem.memra_q8_0_moe_gemv(dq, dd, ids, gw, hq, hd, True)
     torch.cuda.synchronize()
     assert int(st1.item()) == 0
-    assert torch.equal(ws.view(torch.int32), ygu.view(torch.int32))
+    # the workspace keeps each slot's [silu(gate) up | up]: the up rows are the routed
+    # GEMV's bit for bit, the SwiGLU rows the oracle's SwiGLU of the same gate|up bits
+    assert torch.equal(ws[:, F:].contiguous().view(torch.int32),
+                       ygu[:, F:].contiguous().view(torch.int32))
+    h_ref = orc.swiglu(np_(ygu))
+    assert np.array_equal(np_(ws[:, :F]).view(np.uint32), h_ref.view(np.uint32))
     assert torch.equal(y.view(torch.int32), y4.view(torch.int32))
     xo = bf16_bits_np(x.cpu()) if dtype == torch.bfloat16 else np_(x)
     oxq, oxd = orc.quantize_q8_1(xo[None])
