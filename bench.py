@@ -235,11 +235,18 @@ class MoeLayer:
             self.run_tokens(mem, fused)
             return
         if fused:
-            if self.fmt != "q8_0":
-                raise ValueError("the two-kernel routed FFN takes Q8_0 banks")
-            mem.memra_q8_0_moe_ffn(self.gq, self.gd, self.dq, self.dd, self.ids, self.gw,
-                                   self.x[0], y=self.y, workspace=self.ygu,
-                                   dev_status=self.status)
+            if self.fmt == "q4_0":
+                mem.memra_q4_0_moe_ffn(self.gq, self.gd, self.dq, self.dd, self.ids, self.gw,
+                                       self.x[0], y=self.y, workspace=self.ygu.view(-1),
+                                       dev_status=self.status)
+            elif self.fmt == "nvfp4":
+                mem.memra_nvfp4_moe_ffn(self.gq, self.gd, self.ggu, self.dq, self.dd, self.gdn,
+                                        self.ids, self.gw, self.x[0], y=self.y,
+                                        workspace=self.ygu.view(-1), dev_status=self.status)
+            else:
+                mem.memra_q8_0_moe_ffn(self.gq, self.gd, self.dq, self.dd, self.ids, self.gw,
+                                       self.x[0], y=self.y, workspace=self.ygu,
+                                       dev_status=self.status)
             return
         mem.memra_quantize_q8_1(self.x, self.xq, self.xd)
         self.gemv(mem, self.gq, self.gd, self.ids, None, self.xq[0], self.xd[0], False,
@@ -311,12 +318,10 @@ def run_gemv_op(mem, op, quantize=True, fused=False, mma=False):
 class Workload:
     """A step = a fixed list of library calls; captured once into a CUDA graph."""
 
-    def __init__(self, name, mem, device, layers=None, fused=False, chain=False, ops=None,
-                 mma=False):
+    def __init__(self, name, mem, device, layers=None, fused=False, ops=None, mma=False):
         self.name = name
         self.fused = fused
         self.mma = mma
-        self.chain = None
         self.mem = mem
         self.device = device
         self.moe = None
@@ -348,11 +353,6 @@ class Workload:
         else:
             raise ValueError(name)
         self._pack_arenas()
-        if chain:
-            if self.moe is not None or any(op.x.shape[0] != 1 or op.fmt != "q8_0"
-                                           for op in self.ops):
-                raise ValueError("--chain runs M = 1 dense Q8_0 products only")
-            self.chain = mem.GemvChain([(op.wq, op.wd, op.x[0], op.y[0]) for op in self.ops])
         torch.cuda.synchronize(device)
 
     @property
@@ -395,14 +395,12 @@ class Workload:
     @property
     def passes(self):
         """Product launches per dense product: batches above 8 rows take two passes."""
-        if self.moe is not None or self.chain is not None:
+        if self.moe is not None:
             return 1
         return 2 if self.ops[0].xq.shape[0] > 8 else 1
 
     @property
     def launches_per_step(self):
-        if self.chain is not None:
-            return 1
         if self.moe is not None:
             if self.moe[0].tokens > 1:  # + the gated sum per token
                 return (3 if self.fused else 5) * len(self.moe)
@@ -411,16 +409,11 @@ class Workload:
 
     @property
     def gemv_launches_per_step(self):
-        if self.chain is not None:
-            return 1
         if self.moe is not None:
             return 2 * len(self.moe)
         return self.passes * len(self.ops)
 
     def step(self):
-        if self.chain is not None:
-            self.chain.run()
-            return
         if self.moe is not None:
             for m in self.moe:
                 m.run(self.mem, fused=self.fused)
@@ -430,9 +423,7 @@ class Workload:
 
     def gemv_only(self):
         """The step's weight-streaming kernels alone (activations already quantised)."""
-        if self.chain is not None:
-            self.chain.run()  # one launch streams every product of the step
-        elif self.moe is not None and self.fused:
+        if self.moe is not None and self.fused:
             self.step()  # both launches of the fused layer stream weights
         elif self.moe is not None:
             for m in self.moe:
@@ -800,11 +791,9 @@ def run_memra(args):
 
     # Dense products quantise with a separate launch unless --fused; the routed FFN
     # uses its two-kernel entry point unless --unfused.
-    fused = ((not args.unfused) if args.workload in ("moe_top8", "moe_top8_tokens8",
-                                                     "moe_top8_tokens16")
-             else args.fused)
+    fused = ((not args.unfused) if args.workload.startswith("moe_top8") else args.fused)
     wl = Workload(args.workload, mem, device, layers=args.layers, fused=fused,
-                  chain=args.chain, mma=args.mma)
+                  mma=args.mma)
     stream = torch.cuda.Stream(device)
     step_graph = wl.capture(wl.step)
     gemv_graph = wl.capture(wl.gemv_only)
@@ -847,7 +836,6 @@ def run_memra(args):
                 "kernel": "%s product kernel (%s, M=%s)" % (
                     {"q4_0": "Q4_0", "nvfp4": "NVFP4"}.get(
                         wl.ops[0].fmt if wl.ops else wl.moe[0].fmt, "Q8_0"),
-                    "chained, one launch per step" if wl.chain is not None else
                     "routed experts" if wl.moe is not None else
                     ("quantise fused" if wl.fused else "q8_1 input"),
                     1 if wl.moe is not None else "%d%s" % (
@@ -911,10 +899,7 @@ def run_memra(args):
     if rank == 0:
         cfg = workload_config(args.workload, wl)
         cfg["parallelism"] = "replicas x%d (no data-path collective)" % world
-        if wl.chain is not None:
-            cfg["activation_quantise"] = ("in the chained kernel, after a grid barrier on the "
-                                          "previous product (memra_q8_0_gemv_chain)")
-        elif wl.moe is None:
+        if wl.moe is None:
             if wl.mma:
                 cfg["products"] = ("memra_q8_0_gemm_small_m_mma (tensor cores) where K is a "
                                    "multiple of 1024 up to 5120, else memra_q8_0_gemm_small_m")
@@ -927,7 +912,8 @@ def run_memra(args):
                                       "quantize, moe_gemv_tokens, swiglu_quantize, "
                                       "moe_gemv_tokens (gated: + per-token sum)")
             else:
-                cfg["layer_calls"] = ("memra_q8_0_moe_ffn (2 kernels)" if wl.fused else
+                cfg["layer_calls"] = ("memra_%s_moe_ffn (2 kernels)" % wl.moe[0].fmt
+                                      if wl.fused else
                                       "quantize, moe_gemv, swiglu_quantize, moe_gemv")
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -1009,14 +995,12 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true",
                     help="dense workloads: quantise activations in the product's prologue "
                          "(memra_q8_0_quant_gemm) instead of a separate q8_1 launch")
-    ap.add_argument("--chain", action="store_true",
-                    help="dense M = 1 workloads: the whole step as one memra_q8_0_gemv_chain "
-                         "launch")
     ap.add_argument("--mma", action="store_true",
                     help="dense workloads: the tensor-core entry point "
                          "(memra_q8_0_gemm_small_m_mma) for the products it takes")
     ap.add_argument("--unfused", action="store_true",
-                    help="moe_top8: four calls per layer instead of memra_q8_0_moe_ffn")
+                    help="moe_top8 workloads: four calls per layer instead of the two-kernel "
+                         "routed FFN entry point")
     ap.add_argument("--no-configs", action="store_true",
                     help="default workload: skip the short measurements of the other "
                          "configurations")

@@ -88,15 +88,8 @@ _SIGS = {
     "memra_q8_0_moe_ffn_noalloc": [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p, _i32, _p,
                                    _p, _p],
     "memra_q8_0_block_dots": [_p, _i64, _i64, _p, _i64, _p, _p],
-    "memra_q8_0_gemv_chain": [_p, _p, _i32, _p, _p, _p],
+    "memra_debug_set_wait_test": [_i64, _i64],
 }
-
-
-class Q8Step(ctypes.Structure):
-    """memra_q8_0_step: one M = 1 product of a chain."""
-    _fields_ = [("wq", ctypes.c_void_p), ("wd", ctypes.c_void_p), ("x", ctypes.c_void_p),
-                ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
-                ("x_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 def library_path():
@@ -120,8 +113,6 @@ def lib():
         L.memra_status_string.restype = ctypes.c_char_p
         L.memra_last_cuda_error.restype = ctypes.c_int32
         L.memra_version.restype = ctypes.c_char_p
-        L.memra_q8_0_gemv_chain_sync_bytes.argtypes = [ctypes.c_int32]
-        L.memra_q8_0_gemv_chain_sync_bytes.restype = ctypes.c_size_t
         _lib = L
     return _lib
 
@@ -832,57 +823,12 @@ def memra_q8_0_block_dots(wq, xq, s=None):
     return s
 
 
-class GemvChain:
-    """A prepared memra_q8_0_gemv_chain call: a list of (wq, wd, x, y) M = 1 products
-    (x [K] bf16 or fp32, y [N] float32) whose descriptors are copied to the device
-    once.  run() enqueues the whole chain (one memset and one cooperative launch)
-    on the current stream, so it can be captured in a CUDA graph."""
-
-    def __init__(self, products, dev_status=None):
-        if not products:
-            raise ValueError("empty chain")
-        dev = products[0][0].device
-        self.products = list(products)   # keep the tensors alive
-        n = len(products)
-        host = (Q8Step * n)()
-        for i, (wq, wd, x, y) in enumerate(products):
-            _need(wq, "wq", torch.int8, dev)
-            N, K = wq.shape
-            _need(wd, "wd", torch.float16, dev, (N, K // 32))
-            if x.dtype == torch.bfloat16:
-                dt = MEMRA_BF16
-            elif x.dtype == torch.float32:
-                dt = MEMRA_F32
-            else:
-                raise TypeError("x must be bfloat16 or float32")
-            _need(x, "x", x.dtype, dev, (K,))
-            _need(y, "y", torch.float32, dev, (N,))
-            host[i] = Q8Step(wq.data_ptr(), wd.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, dt, 0)
-        self.host = host
-        raw = bytes(host)
-        self.device_steps = torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(dev)
-        nbytes = lib().memra_q8_0_gemv_chain_sync_bytes(n)
-        self.sync = torch.zeros(nbytes // 4, dtype=torch.int32, device=dev)
-        if dev_status is not None:
-            _need(dev_status, "dev_status", torch.int32, dev, (1,))
-        self.dev_status = dev_status
-        self.device = dev
-        self.n = n
-
-    def run(self):
-        with torch.cuda.device(self.device):
-            _check("memra_q8_0_gemv_chain",
-                   lib().memra_q8_0_gemv_chain(_ptr(self.device_steps),
-                                               ctypes.cast(self.host, ctypes.c_void_p), self.n,
-                                               _ptr(self.sync), _ptr(self.dev_status),
-                                               _stream(self.device_steps)))
-
-
-def memra_q8_0_gemv_chain(products, dev_status=None):
-    """Run a chain of M = 1 products once (see GemvChain)."""
-    plan = GemvChain(products, dev_status)
-    plan.run()
-    return plan
+def memra_debug_set_wait_test(wait_limit_cycles=0, stall_after_stages=-1):
+    """Test hook: later product launches give up waiting after wait_limit_cycles SM
+    cycles and, with stall_after_stages >= 0, stall after that many stages per CTA, so
+    that their abort path runs (NaN outputs, status bit 2).  Defaults switch it off."""
+    _check("memra_debug_set_wait_test",
+           lib().memra_debug_set_wait_test(int(wait_limit_cycles), int(stall_after_stages)))
 
 
 def version():

@@ -86,17 +86,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The default limit of a bounded wait: about a second of SM cycles.
+constexpr long long kWaitLimitCycles = 1ll << 31;
+
 // Bounded wait for barrier phase `parity`.  Gives up when `*abort` is set by
-// another thread or after ~2^31 SM cycles (about a second), setting `*abort`;
-// returns whether the phase completed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// another thread or after `limit` SM cycles, setting `*abort`; returns whether the
+// phase completed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 0) {
       if (*abort) return false;
-      if (clock64() - t0 > (1ll << 31)) {
+      if (clock64() - t0 > limit) {
         *abort = 1;
         return false;
       }

@@ -34,6 +34,7 @@
 //   into registers (256-bit loads, a slice's blocks issued together), activations
 //   staged in shared memory.
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -185,6 +186,11 @@ struct Params {
   // (gate j, up j) of slot k.  A stage holds n gate rows, then the same n up rows; the
   // epilogue writes y[k][j] = silu(g) u and y[k][N + j] = u (y: [slots][2N]).
   int pairs;
+  // Bounded waits give up after wait_limit SM cycles.  stall_after >= 0 (test hook):
+  // each CTA's producer stops after that many stages and leaves one more stage that
+  // nothing completes, so that the waits run out and the abort path runs.
+  long long wait_limit;
+  int stall_after;
   // TMA kernel layout
   int rps;                 // rows per stage
   int ns;                  // stages in the ring
@@ -482,7 +488,8 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       if (acquired) return true;
       const int slot = issued % ns;
       if (issued >= (uint32_t)ns) {
-        if (!mbar_wait(empty_bar(slot), ((issued / ns) - 1) & 1, abort_flag)) return false;
+        if (!mbar_wait(empty_bar(slot), ((issued / ns) - 1) & 1, abort_flag, p.wait_limit))
+          return false;
         epilogue(slot);
       }
       acquired = true;
@@ -556,6 +563,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         ok = false;
       }
     }
+    bool stalled = false;
     for (;;) {
       StageMeta m;
       if ((MODE == kMoeGated && p.packed) || !static_next(m)) break;
@@ -563,9 +571,16 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         ok = false;
         break;
       }
+      if (p.stall_after >= 0 && issued == (uint32_t)p.stall_after) {
+        // Test hook: a stage that no copy and no arrival will ever complete.
+        ++issued;
+        acquired = false;
+        stalled = true;
+        break;
+      }
       fill(&m);
     }
-    if (ok) {
+    if (ok && !stalled) {
       if (acquire()) {
         fill(nullptr);
       } else {
@@ -575,10 +590,10 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
     // Drain: the partials of the stages still in the ring (after a normal end the
     // last slot filled holds the sentinel).
     const uint32_t first = issued > (uint32_t)ns ? issued - ns : 0;
-    const uint32_t last = ok ? issued - 1 : issued;
+    const uint32_t last = ok && !stalled ? issued - 1 : issued;
     for (uint32_t j = first; j < last && ok; ++j) {
       const int slot = j % ns;
-      if (!mbar_wait(empty_bar(slot), (j / ns) & 1, abort_flag)) {
+      if (!mbar_wait(empty_bar(slot), (j / ns) & 1, abort_flag, p.wait_limit)) {
         ok = false;
         break;
       }
@@ -593,9 +608,10 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       for (uint32_t j = first; j < issued; ++j) {
         const int slot = j % ns;
         const long long t0 = clock64();
-        while (!mbar_try_wait(full_bar(slot), (j / ns) & 1) && clock64() - t0 < (1ll << 30)) {
+        while (!mbar_try_wait(full_bar(slot), (j / ns) & 1) && clock64() - t0 < p.wait_limit) {
         }
       }
+      if (p.status && lane == 0) atomicOr(p.status, 2);
       const float nan = __int_as_float(0x7fc00000);
       if (MODE == kMoeGated) {
         for (int64_t i = lane; i < u1 - u0; i += 32) p.y[u0 + i] = nan;
@@ -669,7 +685,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
     for (;;) {
       // Every warp waits for every stage, tasks or not: an arrival on the stage's
       // empty barrier must never run ahead of the stage itself.
-      if (!mbar_wait(full_bar(slot), phase, abort_flag)) return;
+      if (!mbar_wait(full_bar(slot), phase, abort_flag, p.wait_limit)) return;
       const StageMeta mt = meta[slot];
       if (mt.nr <= 0) break;
       const int nr = mt.nr;
@@ -1306,10 +1322,17 @@ int reg_grid_ctas_per_sm(int M) {
   return v > 0 && v < built ? (int)v : built;
 }
 
+// The wait test hook (memra_debug_set_wait_test): 0 and -1 when off.
+std::atomic<long long> g_test_wait_limit{0};
+std::atomic<long long> g_test_stall_after{-1};
+
 template <int M, int R, int MODE, int XIN, int FMT = kQ8>
 memra_status run_product(Params p, cudaStream_t stream) {
   DeviceInfo info;
   if (!device_info(&info)) return MEMRA_ERR_CUDA;
+  const long long wl = g_test_wait_limit.load(std::memory_order_relaxed);
+  p.wait_limit = wl > 0 ? wl : kWaitLimitCycles;
+  p.stall_after = (int)g_test_stall_after.load(std::memory_order_relaxed);
   p.qrow = FMT == kQ8 ? p.K : p.K / 2;
   p.nb = (int)(p.K / 32);
   p.cpr = (p.nb + 31) / 32;
@@ -2096,5 +2119,13 @@ extern "C" memra_status memra_q8_0_block_dots(const int8_t* wq, int64_t N, int64
   cudaError_t e = launch_kernel(block_dots_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
                                 wq, N, K, xq, M, s);
   if (e != cudaSuccess) return cuda_fail(e);
+  return MEMRA_OK;
+}
+
+extern "C" memra_status memra_debug_set_wait_test(int64_t wait_limit_cycles,
+                                                  int64_t stall_after_stages) {
+  if (stall_after_stages > INT32_MAX) return MEMRA_ERR_INVALID_ARG;
+  memra::g_test_wait_limit.store(wait_limit_cycles > 0 ? wait_limit_cycles : 0);
+  memra::g_test_stall_after.store(stall_after_stages >= 0 ? stall_after_stages : -1);
   return MEMRA_OK;
 }

@@ -1,6 +1,6 @@
-// Device routines shared by the product kernels (gemm.cu) and the chained-product
-// kernel (chain.cu): the one fp32 summation order of a row, the exact dp4a block
-// dot, and the in-kernel q8_1 quantisation of activations.  sm_103a only.
+// Device routines of the product kernels (gemm.cu): the one fp32 summation order of a
+// row, the exact dp4a block dot, and the in-kernel q8_1 quantisation of activations.
+// sm_103a only.
 #pragma once
 
 #include "common.cuh"

@@ -243,51 +243,6 @@ memra_status memra_q8_0_quant_gemm(const int8_t* wq, const uint16_t* wd, int64_t
                                    cudaStream_t stream);
 
 /*
- * One M = 1 product of a chain (memra_q8_0_gemv_chain).  wq [N][K] (32-byte
- * aligned) and wd [N][K/32] (16-byte aligned) are the Q8_0 planes, x [K] the
- * unquantised activation (bf16 bits or fp32 per x_dtype, 16-byte aligned), y [N]
- * the output.  K must be a positive multiple of 256.
- */
-typedef struct memra_q8_0_step {
-  const int8_t* wq;
-  const uint16_t* wd;
-  const void* x;
-  float* y;
-  int64_t N;
-  int64_t K;
-  int32_t x_dtype;
-  int32_t reserved;
-} memra_q8_0_step;
-
-/*
- * A decode step's chain of M = 1 products in one persistent launch: for i = 0, 1,
- * ..., n_steps-1, y_i = W_i q8_1(x_i), where x_i is read only after every output of
- * steps 0..i-1 is written (so x_i may be one of those outputs, fp32, or an
- * independent input).  The pages drive a decode token as one CUDA-graph replay
- * (memra wiki, feature list: CUDA-graph decode); this is the GB300 counterpart:
- * the weights of step i+1 stream while step i finishes, instead of every product
- * paying its own launch ramp and drain.  Each y_i is bit-identical to
- * memra_q8_0_quant_gemm(W_i, x_i) with M = 1.
- *   steps: DEVICE array of n_steps descriptors (16-byte aligned); host_steps: the
- *   same descriptors in host memory (validated and used to size the launch).
- *   N <= 2^30 per step.
- *   sync_words: caller-allocated device scratch of at least
- *   memra_q8_0_gemv_chain_sync_bytes(n_steps) bytes, 16-byte aligned: per-step row
- *   counters and an abort word, zeroed by this call (on `stream`) before the launch.
- *   Two chains in flight at once need separate sync_words.
- *   dev_status (nullable): OR-ed with 2 if the kernel gave up waiting (bounded wait
- *   of about a second; outputs are then incomplete).
- * The launch is cooperative (every CTA resident at once); MEMRA_ERR_CUDA if the
- * device cannot host the grid.
- */
-memra_status memra_q8_0_gemv_chain(const memra_q8_0_step* steps,
-                                   const memra_q8_0_step* host_steps, int32_t n_steps,
-                                   uint32_t* sync_words, int32_t* dev_status, cudaStream_t stream);
-
-/* Bytes of sync_words that memra_q8_0_gemv_chain needs for n_steps >= 0 steps. */
-size_t memra_q8_0_gemv_chain_sync_bytes(int32_t n_steps);
-
-/*
  * Routed-expert GEMV for one token (memra wiki, feature list: MoE routed experts).
  * Bank: wq_bank [E][N][K], wd_bank [E][N][K/32] (expert e's planes are the slices
  * at e*N*K and e*N*(K/32)).  ids: device int32 [top_k]; gate_w: device fp32
@@ -522,6 +477,22 @@ memra_status memra_q8_0_block_dots(const int8_t* wq, int64_t N, int64_t K, const
  */
 memra_status memra_read_stream(const void* buf, int64_t bytes, uint32_t* sink,
                                int32_t ctas_per_sm, cudaStream_t stream);
+
+/*
+ * Test hook for the device-side failure handling; the pages have no counterpart.  The
+ * bulk-copy product kernel bounds every wait on its shared-memory barriers (about a
+ * second of SM cycles by default): when a wait runs out, the CTA raises an abort flag
+ * that releases its other warps, lets the copies it issued land, writes NaN into the
+ * outputs it owns, ORs 2 into *dev_status (routed entry points, when given) and
+ * returns; nothing traps.  This hook lets a test make those waits run out without a
+ * fault: launches made after it, in this process, give up waiting after
+ * wait_limit_cycles SM cycles (<= 0: the default), and, with stall_after_stages >= 0,
+ * each CTA's producer stops after that many stages and leaves one more stage that no
+ * copy completes.  Set both off again (0, -1) for normal operation.  Launches already
+ * enqueued or captured in a CUDA graph keep the settings they were made with; calls
+ * made from several host threads at once see whichever setting was current.
+ */
+memra_status memra_debug_set_wait_test(int64_t wait_limit_cycles, int64_t stall_after_stages);
 
 /* Static text for a status code. */
 const char* memra_status_string(memra_status status);

@@ -192,39 +192,3 @@ def test_block_dots_argument_errors(L):
     assert L.memra_q8_0_block_dots(A256, 4, 40, A256, 1, A256, None) == 1
     assert L.memra_q8_0_block_dots(A256 + 16, 4, 64, A256, 1, A256, None) == 2
     assert L.memra_q8_0_block_dots(None, 0, 64, None, 1, None, None) == 0
-
-
-def test_chain_sync_bytes(L):
-    f = L.memra_q8_0_gemv_chain_sync_bytes
-    f.restype = ctypes.c_size_t
-    # a claim and a completion counter per step plus one abort word, rounded up to
-    # 16 bytes
-    assert [f(n) for n in (0, 1, 3, 4, 256)] == [16, 16, 32, 48, 2064]
-
-
-def test_chain_argument_errors(L):
-    import block_quantized_decode_quantize_gb300 as m
-    f = L.memra_q8_0_gemv_chain
-
-    def steps(*specs):
-        arr = (m.Q8Step * len(specs))()
-        for i, (N, K, dt, wq) in enumerate(specs):
-            arr[i] = m.Q8Step(wq, A256, A256, A256, N, K, dt, 0)
-        return arr
-
-    ok = steps((64, 256, m.MEMRA_BF16, A256))
-    host = ctypes.cast(ok, ctypes.c_void_p)
-    assert f(A256, host, -1, A256, None, None) == 1                     # negative count
-    assert f(None, None, 0, None, None, None) == 0                      # nothing to do
-    assert f(None, host, 1, A256, None, None) == 1                      # null device steps
-    assert f(A256, host, 1, None, None, None) == 1                      # null sync words
-    assert f(A256 + 8, host, 1, A256, None, None) == 2                  # steps not 16-aligned
-    assert f(A256, host, 1, A256 + 4, None, None) == 2                  # sync not 16-aligned
-    for bad, want in (((64, 96, m.MEMRA_BF16, A256), 1),                # K % 256 != 0
-                      ((64, 0, m.MEMRA_BF16, A256), 1),                 # K = 0
-                      ((-1, 256, m.MEMRA_BF16, A256), 1),               # negative N
-                      ((64, 256, 7, A256), 1),                          # unknown dtype
-                      ((64, 256, m.MEMRA_F32, A256 + 16), 2),           # wq not 32-aligned
-                      ((1 << 31, 256, m.MEMRA_F32, A256), 3)):          # N > 2^30
-        arr = steps((64, 256, m.MEMRA_BF16, A256), bad)
-        assert f(A256, ctypes.cast(arr, ctypes.c_void_p), 2, A256, None, None) == want, bad
