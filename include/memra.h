@@ -48,6 +48,29 @@
  *     the quantiser inputs 16 bytes; wd 2 bytes; xd, y, ids, gate_w 4 bytes.  The
  *     4-bit formats' planes and their q8_1 inputs: 16 bytes.
  *   - Inputs must be finite.
+ *
+ * Run-time switches.  The defaults are the configurations measured best on GB300;
+ * the environment variables below override them for benchmarking and tests.  Each is
+ * read once per process, on the first call that needs it; a value that does not parse
+ * keeps the default.  No result bit depends on them (every kernel computes the same
+ * fp32 order), only the kernel choice and launch shapes.
+ *   MEMRA_GEMV_PATH   "reg": dense Q8_0 products on the register-stream kernel;
+ *                     "tma": on the bulk-copy kernel wherever it applies (also below
+ *                     the size threshold); "mma": memra_q8_0_gemm_small_m on the
+ *                     tensor-core kernel where it applies (as
+ *                     memra_q8_0_gemm_small_m_mma).  Unset: per-shape dispatch.
+ *   MEMRA_PDL         "0": launch without programmatic dependent launch.
+ *   MEMRA_TMA_STAGE_KB, MEMRA_TMA_RING_KB, MEMRA_TMA_ROUTED_STAGE_KB,
+ *   MEMRA_TMA_SMEM_LIMIT_KB, MEMRA_TMA_CTAS_PER_SM, MEMRA_TMA_PACKED_KB,
+ *   MEMRA_TMA_MULTI_RING_KB, MEMRA_TMA_MULTI_STAGE_KB, MEMRA_TMA_MULTI,
+ *   MEMRA_TMA_DENSE_MIN_MB, MEMRA_REG_CTAS_PER_SM
+ *                     stage, ring and shared-memory sizes (KB), CTAs per SM, the
+ *                     M > 1 bulk-copy switch and the register/bulk-copy size
+ *                     threshold (MB) of the product kernels.
+ * The same names, defined as macros when the library is compiled, change the
+ * compiled-in defaults (also MEMRA_TMA_CONSUMER_WARPS,
+ * MEMRA_TMA_FEW_M_CONSUMER_WARPS, MEMRA_TMA_MIN_BLOCKS, MEMRA_SLICE_PARTS; the last
+ * changes the fp32 summation order and with it the result bits).
  */
 #ifndef MEMRA_H
 #define MEMRA_H
