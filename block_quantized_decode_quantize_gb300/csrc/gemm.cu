@@ -79,6 +79,15 @@
 #ifndef MEMRA_TMA_MIN_BLOCKS
 #define MEMRA_TMA_MIN_BLOCKS 2
 #endif
+// Dense products: stages a CTA issues before its consumers have staged the activation
+// (0: no limit).  The activation's loads, issued after the grid-dependency wait, queue
+// behind the weight copies already in flight to the SM; with two stages per CTA
+// instead of the whole ring they return sooner, and the dependent chain of products
+// and quantise launches moves faster (64-layer sweep: 4.28 -> 4.12 ms per token; one
+// stage: 4.33 ms).
+#ifndef MEMRA_TMA_PREFILL
+#define MEMRA_TMA_PREFILL 2
+#endif
 
 namespace memra {
 namespace {
@@ -191,6 +200,10 @@ struct Params {
   // nothing completes, so that the waits run out and the abort path runs.
   long long wait_limit;
   int stall_after;
+  // Dense products: stages a CTA's producer issues before its consumers have staged the
+  // activation (0: no limit).  A short queue of weight copies in flight lets the
+  // activation's loads, issued after the grid-dependency wait, return sooner.
+  int prefill_stages;
   // TMA kernel layout
   int rps;                 // rows per stage
   int ns;                  // stages in the ring
@@ -295,6 +308,7 @@ constexpr int kMaxStages = 16;
 // Shared-memory header: full[kMaxStages] | empty[kMaxStages] mbarriers, the abort
 // flag, the stage metadata, the routed ids and gate weights.
 constexpr int kOffAbort = 8 * 2 * kMaxStages;
+constexpr int kOffXready = kOffAbort + 8;  // mbarrier: the consumers staged the activation
 constexpr int kOffMeta = kOffAbort + 16;
 constexpr int kOffIds = kOffMeta + 16 * kMaxStages;
 constexpr int kOffGate = kOffIds + 4 * kMaxTopK;
@@ -348,6 +362,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
   }
   auto full_bar = [&](int i) { return smem_addr(bars + i); };
   auto empty_bar = [&](int i) { return smem_addr(bars + kMaxStages + i); };
+  const uint32_t xready_bar = smem_addr(smem + kOffXready);
 
   if (MODE == kDense) pdl_launch_dependents();
   // Start-up.  The producer warp initialises the barriers (and, for routed
@@ -360,6 +375,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         mbar_init(full_bar(i), 1);
         mbar_init(empty_bar(i), kConsumerWarps);
       }
+      mbar_init(xready_bar, 1);
       *abort_flag = 0;
       mbar_init_fence();
     }
@@ -571,6 +587,14 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         ok = false;
         break;
       }
+      if (MODE == kDense && p.prefill_stages > 0 && issued == (uint32_t)p.prefill_stages) {
+        bool ready = true;
+        if (lane == 0) ready = mbar_wait(xready_bar, 0, abort_flag, p.wait_limit);
+        if (!__shfl_sync(kFullMask, ready ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+      }
       if (p.stall_after >= 0 && issued == (uint32_t)p.stall_after) {
         // Test hook: a stage that no copy and no arrival will ever complete.
         ++issued;
@@ -648,6 +672,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
                                  kConsumerWarps, lane);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    if (threadIdx.x == 32) mbar_arrive(xready_bar);
     // Q4_0: s_b = sum_i (c_i - 8) x_i = (sum_i c_i x_i) - 8 sum_i x_i, with the
     // activation's per-block sums taken once here.
     int32_t* xsum = reinterpret_cast<int32_t*>(smem + p.off_xsum);
@@ -1129,6 +1154,7 @@ struct TmaTuning {
   size_t routed_stage_target; // M = 1 routed experts: bytes per ring stage
   bool multi_default;        // M > 1 products use this kernel by default
   int64_t dense_min_bytes;  // smaller dense products use the register kernel
+  int prefill_stages;       // dense: stages issued before the activation is staged (0: all)
 };
 
 long env_long(const char* name, long dflt, long lo) {
@@ -1158,6 +1184,7 @@ const TmaTuning& tma_tuning() {
     r.ctas_per_sm = (int)env_long("MEMRA_TMA_CTAS_PER_SM", MEMRA_TMA_CTAS_PER_SM, 1);
     r.dense_min_bytes =
         (int64_t)env_long("MEMRA_TMA_DENSE_MIN_MB", MEMRA_TMA_DENSE_MIN_MB, 0) * 1024 * 1024;
+    r.prefill_stages = (int)env_long("MEMRA_TMA_PREFILL", MEMRA_TMA_PREFILL, 0);
     return r;
   }();
   return t;
@@ -1330,6 +1357,7 @@ template <int M, int R, int MODE, int XIN, int FMT = kQ8>
 memra_status run_product(Params p, cudaStream_t stream) {
   DeviceInfo info;
   if (!device_info(&info)) return MEMRA_ERR_CUDA;
+  p.prefill_stages = tma_tuning().prefill_stages;
   const long long wl = g_test_wait_limit.load(std::memory_order_relaxed);
   p.wait_limit = wl > 0 ? wl : kWaitLimitCycles;
   p.stall_after = (int)g_test_stall_after.load(std::memory_order_relaxed);
