@@ -88,6 +88,9 @@
 #ifndef MEMRA_TMA_PREFILL
 #define MEMRA_TMA_PREFILL 2
 #endif
+#ifndef MEMRA_TMA_ROUTED_PREFILL
+#define MEMRA_TMA_ROUTED_PREFILL 1
+#endif
 
 namespace memra {
 namespace {
@@ -232,16 +235,26 @@ struct Seg {
   bool valid;
 };
 
+// The slot of a CTA's first unit (ungated routed products; 0 otherwise): the one
+// 64-bit division a CTA needs, taken once.
 template <int MODE>
-__device__ __forceinline__ int num_segs(const Params& p, int64_t u0, int64_t u1) {
+__device__ __forceinline__ int64_t first_slot(const Params& p, int64_t u0) {
+  return MODE == kMoeUngated ? u0 / p.N : 0;
+}
+
+template <int MODE>
+__device__ __forceinline__ int num_segs(const Params& p, int64_t u0, int64_t u1, int64_t k0) {
   if (MODE == kDense) return 1;
   if (MODE == kMoeGated) return p.top_k;
-  return (int)((u1 - 1) / p.N - u0 / p.N + 1);
+  // slots k0 .. k with k N <= u1 - 1 < (k + 1) N
+  int64_t k = k0;
+  while ((k + 1) * p.N <= u1 - 1) ++k;
+  return (int)(k - k0 + 1);
 }
 
 template <int MODE>
 __device__ __forceinline__ Seg get_seg(const Params& p, int64_t u0, int64_t u1, int si,
-                                       const int32_t* s_ids) {
+                                       const int32_t* s_ids, int64_t k0) {
   Seg g;
   if (MODE == kDense) {
     g.row0 = u0;
@@ -259,7 +272,7 @@ __device__ __forceinline__ Seg get_seg(const Params& p, int64_t u0, int64_t u1, 
     g.xrow = p.xpe ? si : 0;
     g.out0 = u0;
   } else {
-    const int64_t k = u0 / p.N + si;
+    const int64_t k = k0 + si;
     const int64_t lo = (u0 > k * p.N ? u0 : k * p.N) - k * p.N;
     const int64_t hi = (u1 < (k + 1) * p.N ? u1 : (k + 1) * p.N) - k * p.N;
     const int e = s_ids[k];
@@ -354,11 +367,13 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
   const int64_t u1 = p.units * (blockIdx.x + 1) / gridDim.x;
   // Activation rows this CTA stages: [xlo, xlo + nxr).  An ungated routed product
   // with an activation row per slot group stages only the rows of its own segments.
+  const int64_t k0 = first_slot<MODE>(p, u0);
+  const int nseg = num_segs<MODE>(p, u0, u1, k0);
   int xlo = 0, nxr = p.xrows;
   if (MODE == kMoeUngated && p.xpe) {
-    const int64_t d = p.xdiv > 1 ? p.xdiv : 1;
-    xlo = (int)((u0 / p.N) / d);
-    nxr = (int)(((u1 - 1) / p.N) / d) - xlo + 1;
+    const int d = p.xdiv > 1 ? p.xdiv : 1;
+    xlo = (int)k0 / d;
+    nxr = (int)(k0 + nseg - 1) / d - xlo + 1;
   }
   auto full_bar = [&](int i) { return smem_addr(bars + i); };
   auto empty_bar = [&](int i) { return smem_addr(bars + kMaxStages + i); };
@@ -402,8 +417,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
   // same call (routing_ready) can read the same routing before it waits.
   if (MODE != kDense) pdl_launch_dependents();
 
-  const int nseg = num_segs<MODE>(p, u0, u1);
-  auto seg_of = [&](int si) { return get_seg<MODE>(p, u0, u1, si, s_ids); };
+  auto seg_of = [&](int si) { return get_seg<MODE>(p, u0, u1, si, s_ids, k0); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -415,7 +429,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
     int cur_si = 0, cur_r0 = 0;
     auto static_next = [&](StageMeta& m) -> bool {
       while (cur_si < nseg) {
-        const Seg g = get_seg<MODE>(p, u0, u1, cur_si, s_ids);
+        const Seg g = get_seg<MODE>(p, u0, u1, cur_si, s_ids, k0);
         if (!g.valid || cur_r0 >= g.nrows) {
           if (!g.valid && MODE == kMoeUngated)
             for (int i = lane; i < g.nrows; i += 32) {
@@ -587,7 +601,7 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         ok = false;
         break;
       }
-      if (MODE == kDense && p.prefill_stages > 0 && issued == (uint32_t)p.prefill_stages) {
+      if (p.prefill_stages > 0 && issued == (uint32_t)p.prefill_stages) {
         bool ready = true;
         if (lane == 0) ready = mbar_wait(xready_bar, 0, abort_flag, p.wait_limit);
         if (!__shfl_sync(kFullMask, ready ? 1 : 0, 0)) {
@@ -998,10 +1012,11 @@ __global__ void __launch_bounds__(kRegThreads, reg_ctas_per_sm(M)) q8_reg_kernel
   stage_x_split<XIN>(p, xs, xds, warp, kRegWarps, lane, threadIdx.x, kRegThreads);
   __syncthreads();
 
-  const int nseg = num_segs<MODE>(p, u0, u1);
+  const int64_t k0 = first_slot<MODE>(p, u0);
+  const int nseg = num_segs<MODE>(p, u0, u1, k0);
   bool any_valid = false;
   for (int si = 0; si < nseg; ++si) {
-    const Seg g = get_seg<MODE>(p, u0, u1, si, s_ids);
+    const Seg g = get_seg<MODE>(p, u0, u1, si, s_ids, k0);
     if (!g.valid) {
       if (MODE == kMoeUngated)
         for (int i = threadIdx.x; i < g.nrows; i += kRegThreads) p.y[g.out0 + i] = 0.0f;
@@ -1155,6 +1170,7 @@ struct TmaTuning {
   bool multi_default;        // M > 1 products use this kernel by default
   int64_t dense_min_bytes;  // smaller dense products use the register kernel
   int prefill_stages;       // dense: stages issued before the activation is staged (0: all)
+  int routed_prefill;       // the same for routed products
 };
 
 long env_long(const char* name, long dflt, long lo) {
@@ -1185,6 +1201,7 @@ const TmaTuning& tma_tuning() {
     r.dense_min_bytes =
         (int64_t)env_long("MEMRA_TMA_DENSE_MIN_MB", MEMRA_TMA_DENSE_MIN_MB, 0) * 1024 * 1024;
     r.prefill_stages = (int)env_long("MEMRA_TMA_PREFILL", MEMRA_TMA_PREFILL, 0);
+    r.routed_prefill = (int)env_long("MEMRA_TMA_ROUTED_PREFILL", MEMRA_TMA_ROUTED_PREFILL, 0);
     return r;
   }();
   return t;
@@ -1357,7 +1374,8 @@ template <int M, int R, int MODE, int XIN, int FMT = kQ8>
 memra_status run_product(Params p, cudaStream_t stream) {
   DeviceInfo info;
   if (!device_info(&info)) return MEMRA_ERR_CUDA;
-  p.prefill_stages = tma_tuning().prefill_stages;
+  p.prefill_stages =
+      MODE == kDense ? tma_tuning().prefill_stages : tma_tuning().routed_prefill;
   const long long wl = g_test_wait_limit.load(std::memory_order_relaxed);
   p.wait_limit = wl > 0 ? wl : kWaitLimitCycles;
   p.stall_after = (int)g_test_stall_after.load(std::memory_order_relaxed);
