@@ -226,6 +226,13 @@ __device__ __forceinline__ const void* xin_row(const void* xin, int64_t row, int
   return static_cast<const float*>(xin) + row * 2 * K;  // kXswiglu, kXhalf: rows of 2K
 }
 
+// The unit range [u0, u1) of CTA b of G: units * b / G with 32-bit arithmetic when the
+// products fit (every workload here), else 64-bit.
+__device__ __forceinline__ int64_t cta_unit(int64_t units, unsigned b, unsigned G) {
+  if (units <= (int64_t)(0xffffffffu / G)) return (int64_t)((uint32_t)units * b / G);
+  return units * b / G;
+}
+
 struct Seg {
   int64_t row0;   // first weight row (absolute row index into the plane)
   int nrows;
@@ -363,8 +370,8 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
   const int nb = p.nb;
   const int S = p.S;
   const int ns = p.ns;
-  const int64_t u0 = p.units * blockIdx.x / gridDim.x;
-  const int64_t u1 = p.units * (blockIdx.x + 1) / gridDim.x;
+  const int64_t u0 = cta_unit(p.units, blockIdx.x, gridDim.x);
+  const int64_t u1 = cta_unit(p.units, blockIdx.x + 1, gridDim.x);
   // Activation rows this CTA stages: [xlo, xlo + nxr).  An ungated routed product
   // with an activation row per slot group stages only the rows of its own segments.
   const int64_t k0 = first_slot<MODE>(p, u0);
@@ -953,8 +960,8 @@ __global__ void __launch_bounds__(kRegThreads, reg_ctas_per_sm(M)) q8_reg_kernel
   float* s_gate = reinterpret_cast<float*>(s_ids + kMaxTopK);
   int* s_slice = reinterpret_cast<int*>(s_gate + kMaxTopK);
 
-  const int64_t u0 = p.units * blockIdx.x / gridDim.x;
-  const int64_t u1 = p.units * (blockIdx.x + 1) / gridDim.x;
+  const int64_t u0 = cta_unit(p.units, blockIdx.x, gridDim.x);
+  const int64_t u1 = cta_unit(p.units, blockIdx.x + 1, gridDim.x);
   // Lanes past the end of a row's last part hold no block.
   const bool last_ok = lane < nb - (p.cpr - 1) * 32;
 
