@@ -86,6 +86,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, letting the hardware suspend the thread for up to `ns` nanoseconds
+// while the phase is incomplete; the thread resumes as soon as the phase completes.
+// A waiting warp then retries a few times per wait instead of polling, which leaves
+// the issue slots to the warps with work.
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+#ifndef MEMRA_WAIT_SUSPEND_NS
+#define MEMRA_WAIT_SUSPEND_NS 8192
+#endif
+
 // The default limit of a bounded wait: about a second of SM cycles.
 constexpr long long kWaitLimitCycles = 1ll << 31;
 
@@ -96,14 +115,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0) {
-      if (*abort) return false;
-      if (clock64() - t0 > limit) {
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_for(bar, parity, MEMRA_WAIT_SUSPEND_NS)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit) {
+      *abort = 1;
+      return false;
     }
   }
 }

@@ -129,8 +129,13 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-__device__ __forceinline__ int nv4_dot16(uint32_t c0, uint32_t c1, const uint4& x) {
-  constexpr uint32_t kLo = 0x03020100u, kHi = 0x0C080604u;
+// The lookup bytes: kNv4Lo | kNv4Hi.  The kernels read them from shared memory into
+// registers once, so that the compiler keeps them there rather than rebuilding the
+// two constants for every lookup.
+constexpr uint32_t kNv4Lo = 0x03020100u, kNv4Hi = 0x0C080604u;
+
+__device__ __forceinline__ int nv4_dot16(uint32_t c0, uint32_t c1, const uint4& x, uint32_t kLo,
+                                         uint32_t kHi) {
   const uint32_t n0 = c0 ^ 0x88888888u;
   const uint32_t n1 = c1 ^ 0x88888888u;
   int p = __dp4a((int)prmt(kLo, kHi, c0), (int)x.x, 0);
@@ -333,7 +338,8 @@ constexpr int kOffMeta = kOffAbort + 16;
 constexpr int kOffIds = kOffMeta + 16 * kMaxStages;
 constexpr int kOffGate = kOffIds + 4 * kMaxTopK;
 constexpr int kOffGsc = kOffGate + 4 * kMaxTopK;  // NVFP4 routed: half each slot's g
-constexpr int kHeaderBytes = (kOffGsc + 4 * kMaxTopK + 127) / 128 * 128;
+constexpr int kOffTab = kOffGsc + 4 * kMaxTopK;  // NVFP4: the lookup bytes
+constexpr int kHeaderBytes = (kOffTab + 8 + 127) / 128 * 128;
 
 // What the producer put in a ring slot: rows [r0, r0 + nr) of segment `seg`, with
 // activation row `xrow`.  nr == 0 marks the end of the CTA's stages.  A packed stage
@@ -345,6 +351,88 @@ struct StageMeta {
   int nr;
   int xrow;
 };
+
+// Add one 32-block part of R weight rows against M activation rows to acc: this lane's
+// block q parts past wl[r] (quants) and dl[r] (scales), and past xl / xdl / xsl (the
+// activation row's quants, scales and Q4_0 block sums; further rows Ki bytes and nb
+// blocks on).  h1: which 16-byte half of a Q8_0 block this lane loads first; xh: the
+// same for the activation (0 for NVFP4, which reads both halves in element order).
+// Format constants: Q4_0 nibble masks q4m0 / q4m1 and shift q4s0 of this lane; NVFP4
+// lookup bytes tlo | thi.
+struct PartConsts {
+  uint32_t q4m0, q4m1;
+  int q4s0;
+  uint32_t tlo, thi;
+};
+
+template <int M, int R, int FMT>
+__device__ __forceinline__ void add_part(float (&acc)[R][M], const int8_t* const (&wl)[R],
+                                         const uint16_t* const (&dl)[R], const int8_t* xl,
+                                         const float* xdl, const int32_t* xsl, int q, int Ki,
+                                         int nb, int h1, int xh, const PartConsts& pc) {
+  constexpr int kBlockBytes = FMT == kQ8 ? 32 : 16;
+  constexpr int kPartBytes = 32 * kBlockBytes;
+  uint4 w0[R], w1[R];
+  uint16_t dw[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    // Q8_0: the two halves in this lane quad's order (see the file comment).
+    // Q4_0 and NVFP4: the block's 16 bytes of codes in one load.
+    w0[r] = *reinterpret_cast<const uint4*>(wl[r] + q * kPartBytes);
+    if (FMT == kQ8) w1[r] = *reinterpret_cast<const uint4*>(wl[r] + q * kPartBytes + 16 - 32 * h1);
+    dw[r] = dl[r][q * 32];
+  }
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int8_t* xm = xl + (size_t)m * Ki + q * 1024;
+    const uint4 x0 = *reinterpret_cast<const uint4*>(xm);
+    const uint4 x1 = *reinterpret_cast<const uint4*>(xm + 16 - 32 * xh);
+    const float dx = xdl[(size_t)m * nb + q * 32];
+    if (FMT == kQ4) {
+      // x0 holds half h1 of the block (elements 16*h1 ..), x1 the other half.  The
+      // lane pairs x0 with the nibbles of half h1 (mask m0) and x1 with the other
+      // nibbles (m1).  A high-nibble mask leaves 16 times the codes in place, which
+      // makes that dp4a exactly 16 times the half's dot (a multiple of 16 below 2^19),
+      // undone by the shift.
+      const uint32_t q4m0 = pc.q4m0, q4m1 = pc.q4m1;
+      const int q4s0 = pc.q4s0;
+      const int sx = xsl[(size_t)m * nb + q * 32];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const uint4 c = w0[r];
+        int a = dp4a_us(c.x & q4m0, (int)x0.x, 0);
+        a = dp4a_us(c.y & q4m0, (int)x0.y, a);
+        a = dp4a_us(c.z & q4m0, (int)x0.z, a);
+        a = dp4a_us(c.w & q4m0, (int)x0.w, a);
+        int b = dp4a_us(c.x & q4m1, (int)x1.x, 0);
+        b = dp4a_us(c.y & q4m1, (int)x1.y, b);
+        b = dp4a_us(c.z & q4m1, (int)x1.z, b);
+        b = dp4a_us(c.w & q4m1, (int)x1.w, b);
+        const int dot = (a >> q4s0) + (b >> (4 - q4s0));
+        acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, dot - 8 * sx);
+      }
+    } else if (FMT == kNv4) {
+      // Code bytes 0..7 are the block's elements 0..15 (first E4M3 scale), bytes 8..15
+      // elements 16..31; x0 and x1 hold the same halves (xh = 0).  Each half's exact
+      // sum, then the two terms in element order.
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const uint4 c = w0[r];
+        const int sa = nv4_dot16(c.x, c.y, x0, pc.tlo, pc.thi);  // elements 0..15
+        const int sb = nv4_dot16(c.z, c.w, x1, pc.tlo, pc.thi);  // elements 16..31
+        const float2 sc = e4m3x2_to_float2(dw[r]);
+        acc[r][m] = __fmaf_rn(__fmul_rn(sc.x, dx), (float)sa, acc[r][m]);
+        acc[r][m] = __fmaf_rn(__fmul_rn(sc.y, dx), (float)sb, acc[r][m]);
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int sb = dot_halves(w0[r], w1[r], x0, x1);
+        acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, sb);
+      }
+    }
+  }
+}
 
 template <int M, int R, int MODE, int XIN, int FMT = kQ8>
 __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS : 1)
@@ -399,6 +487,10 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       }
       mbar_init(xready_bar, 1);
       *abort_flag = 0;
+      if (FMT == kNv4) {
+        reinterpret_cast<uint32_t*>(smem + kOffTab)[0] = kNv4Lo;
+        reinterpret_cast<uint32_t*>(smem + kOffTab)[1] = kNv4Hi;
+      }
       mbar_init_fence();
     }
     if (MODE != kDense) {
@@ -717,10 +809,16 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
     constexpr int kBlockBytes = FMT == kQ8 ? 32 : 16;
     constexpr int kPartBytes = 32 * kBlockBytes;
     const int Qrow = (int)p.qrow;
-    // Q4_0 nibble masks and shifts of this lane (see the block dot below).
-    const uint32_t q4m0 = h1 ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
-    const uint32_t q4m1 = ~q4m0;
-    const int q4s0 = h1 ? 4 : 0;
+    // Q4_0 nibble masks and shift of this lane (see add_part); the NVFP4 lookup bytes.
+    PartConsts pc;
+    pc.q4m0 = h1 ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+    pc.q4m1 = ~pc.q4m0;
+    pc.q4s0 = h1 ? 4 : 0;
+    pc.tlo = FMT == kNv4 ? reinterpret_cast<const uint32_t*>(smem + kOffTab)[0] : 0u;
+    pc.thi = FMT == kNv4 ? reinterpret_cast<const uint32_t*>(smem + kOffTab)[1] : 0u;
+    // NVFP4 reads the activation halves in element order (xh = 0): it is issue-bound,
+    // and the half order's selects cost more there than a 2-way bank conflict.
+    const int xh = FMT == kNv4 ? 0 : h1;
     uint32_t tbase = 0;  // tasks in all earlier stages: deals tasks round-robin over warps
     // A warp's tasks are kConsumerWarps apart: in (group, slice) form a step of
     // (dgi, dsl) with a carry, so no task needs a division.
@@ -775,11 +873,9 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
           wl[r] = ws + row * Qrow + (plo * 32 + lane) * kBlockBytes + (FMT == kQ8 ? h1 * 16 : 0);
           dl[r] = ds + row * nb + plo * 32 + lane;
         }
-        // NVFP4 reads the activation halves in element order (xh = 0): it is issue-bound,
-        // and the half order's selects cost more there than a 2-way bank conflict.
-        const int xh = FMT == kNv4 ? 0 : h1;
         const int8_t* xl = xs + (size_t)xrow * Ki + (plo * 32 + lane) * 32 + xh * 16;
         const float* xdl = xds + (size_t)xrow * nb + plo * 32 + lane;
+        const int32_t* xsl = xsum + (size_t)xrow * nb + plo * 32 + lane;
         float acc[R][M];
 #pragma unroll
         for (int r = 0; r < R; ++r)
@@ -791,67 +887,8 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
 #pragma unroll
         for (int q = 0; q < kSlicePartsMax; ++q) {
           const int pt = plo + q;
-          if (pt < phi && (pt < p.cpr - 1 || last_ok)) {
-            uint4 w0[R], w1[R];
-            uint16_t dw[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-              // Q8_0: the two halves in this lane quad's order (see the file comment).
-              // Q4_0: the block's 16 bytes of codes in one load.
-              w0[r] = *reinterpret_cast<const uint4*>(wl[r] + q * kPartBytes);
-              if (FMT == kQ8)
-                w1[r] = *reinterpret_cast<const uint4*>(wl[r] + q * kPartBytes + 16 - 32 * h1);
-              dw[r] = dl[r][q * 32];
-            }
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-              const int8_t* xm = xl + (size_t)m * Ki + q * 1024;
-              const uint4 x0 = *reinterpret_cast<const uint4*>(xm);
-              const uint4 x1 = *reinterpret_cast<const uint4*>(xm + 16 - 32 * xh);
-              const float dx = xdl[(size_t)m * nb + q * 32];
-              if (FMT == kQ4) {
-                // x0 holds half h1 of the block (elements 16*h1 ..), x1 the other half.
-                // The lane pairs x0 with the nibbles of half h1 (mask m0) and x1 with the
-                // other nibbles (m1).  A high-nibble mask leaves 16 times the codes in
-                // place, which makes that dp4a exactly 16 times the half's dot (a
-                // multiple of 16 below 2^19), undone by the shift.
-                const int sx = xsum[(size_t)(xrow + m) * nb + pt * 32 + lane];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                  const uint4 c = w0[r];
-                  int a = dp4a_us(c.x & q4m0, (int)x0.x, 0);
-                  a = dp4a_us(c.y & q4m0, (int)x0.y, a);
-                  a = dp4a_us(c.z & q4m0, (int)x0.z, a);
-                  a = dp4a_us(c.w & q4m0, (int)x0.w, a);
-                  int b = dp4a_us(c.x & q4m1, (int)x1.x, 0);
-                  b = dp4a_us(c.y & q4m1, (int)x1.y, b);
-                  b = dp4a_us(c.z & q4m1, (int)x1.z, b);
-                  b = dp4a_us(c.w & q4m1, (int)x1.w, b);
-                  const int dot = (a >> q4s0) + (b >> (4 - q4s0));
-                  acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, dot - 8 * sx);
-                }
-              } else if (FMT == kNv4) {
-                // Code bytes 0..7 are the block's elements 0..15 (first E4M3 scale),
-                // bytes 8..15 elements 16..31; x0 and x1 hold the same halves (xh = 0).
-                // Each half's exact sum, then the two terms in element order.
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                  const uint4 c = w0[r];
-                  const int sa = nv4_dot16(c.x, c.y, x0);  // elements 0..15
-                  const int sb = nv4_dot16(c.z, c.w, x1);  // elements 16..31
-                  const float2 sc = e4m3x2_to_float2(dw[r]);
-                  acc[r][m] = __fmaf_rn(__fmul_rn(sc.x, dx), (float)sa, acc[r][m]);
-                  acc[r][m] = __fmaf_rn(__fmul_rn(sc.y, dx), (float)sb, acc[r][m]);
-                }
-              } else {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                  const int sb = dot_halves(w0[r], w1[r], x0, x1);
-                  acc[r][m] = block_term_acc(acc[r][m], dw[r], dx, sb);
-                }
-              }
-            }
-          }
+          if (pt < phi && (pt < p.cpr - 1 || last_ok))
+            add_part<M, R, FMT>(acc, wl, dl, xl, xdl, xsl, q, Ki, nb, h1, xh, pc);
         }
         store_partials<R, M>(acc, lane, pp, rbase, nr - rbase, s, S);
       }

@@ -6,7 +6,8 @@ everywhere, the bulk-copy kernel wherever it applies (also for M > 1), and the
 tensor-core kernel wherever it applies (also for M = 1).  The shapes include products
 with many ring stages per CTA (12289 x 4096 ends in a one-row stage; 5120 x 17408 has
 one-row stages), tensor-core tiles moved back over the previous tile (N = 17, 40, 1000
-rows), a single 16-row tile (N = 16), and two-pass batches (M = 11, 16)."""
+rows), a single 16-row tile (N = 16), and two-pass batches (M = 11, 16).  Q4_0 and NVFP4
+products run on the bulk-copy kernel only; their children compare its stage geometries."""
 import os
 import subprocess
 import sys
@@ -45,17 +46,45 @@ xq, xd = mem.memra_quantize_q8_1(x)
 out["moe_u"] = mem.memra_q8_0_moe_gemv(bq, bd, ids, None, xq, xd, True).cpu()
 out["moe_g"] = mem.memra_q8_0_moe_gemv(bq, bd, ids, gw, xq, xd, True).cpu()
 out["moe_s"] = mem.memra_q8_0_moe_gemv(bq, bd, ids, gw, xq[0], xd[0], False).cpu()
+# 4-bit dense products (bulk-copy kernel only): its stage geometries must agree.
+for (N, K, M) in [(777, 5120, 1), (2050, 17408, 1), (3000, 5120, 1), (513, 2048, 4),
+                  (300, 5120, 8), (1000, 4096, 2)]:
+    w = synth.weights_fp32(N, K, 74, N, K, device="cuda")
+    x = synth.activations_bf16(M, K, 75, N, K, M, outlier_frac=0.001, device="cuda")
+    xq, xd = mem.memra_quantize_q8_1(x)
+    c4, d4 = mem.memra_quantize_q4_0(w)
+    out["q4_%%d_%%d_%%d" %% (N, K, M)] = mem.memra_q4_0_gemm_small_m(c4, d4, xq, xd).cpu()
+    cn, sn, gn = mem.memra_quantize_nvfp4(w)
+    out["nv_%%d_%%d_%%d" %% (N, K, M)] = mem.memra_nvfp4_gemm_small_m(cn, sn, float(gn.item()),
+                                                                   xq, xd).cpu()
 torch.cuda.synchronize()
 torch.save(out, sys.argv[1])
 """
 
 
-def run_child(tmp_path, env_path):
-    path = str(tmp_path / ("out_%s.pt" % (env_path or "default")))
+# Children: (name, environment).  Besides the kernel choice, the bulk-copy kernel's
+# stage geometry (read once per process): small stages, so that every CTA wraps its
+# ring many times and the tasks fall differently on the consumer warps, and no limit
+# or a one-stage limit on the stages issued before the activation is staged.
+VARIANTS = [
+    ("reg", {"MEMRA_GEMV_PATH": "reg"}),
+    ("tma", {"MEMRA_GEMV_PATH": "tma"}),
+    ("mma", {"MEMRA_GEMV_PATH": "mma"}),
+    ("tma_small_stages", {"MEMRA_GEMV_PATH": "tma", "MEMRA_TMA_STAGE_KB": "6",
+                          "MEMRA_TMA_MULTI_STAGE_KB": "6", "MEMRA_TMA_ROUTED_STAGE_KB": "6"}),
+    ("tma_prefill_all", {"MEMRA_GEMV_PATH": "tma", "MEMRA_TMA_PREFILL": "0"}),
+    ("tma_prefill_1", {"MEMRA_GEMV_PATH": "tma", "MEMRA_TMA_PREFILL": "1"}),
+]
+_KNOBS = ("MEMRA_GEMV_PATH", "MEMRA_TMA_STAGE_KB", "MEMRA_TMA_MULTI_STAGE_KB",
+          "MEMRA_TMA_ROUTED_STAGE_KB", "MEMRA_TMA_PREFILL")
+
+
+def run_child(tmp_path, name, extra):
+    path = str(tmp_path / ("out_%s.pt" % name))
     env = dict(os.environ)
-    env.pop("MEMRA_GEMV_PATH", None)
-    if env_path:
-        env["MEMRA_GEMV_PATH"] = env_path
+    for k in _KNOBS:
+        env.pop(k, None)
+    env.update(extra)
     src = CHILD % {"root": ROOT}
     r = subprocess.run([sys.executable, "-c", src, path], env=env, capture_output=True, text=True,
                        timeout=600)
@@ -68,9 +97,9 @@ def test_product_kernels_agree_bitwise(tmp_path):
         pytest.skip("no CUDA device")
     from block_quantized_decode_quantize_gb300 import build
     build.build()
-    a = run_child(tmp_path, None)
-    for other in ("reg", "tma", "mma"):
-        b = run_child(tmp_path, other)
+    a = run_child(tmp_path, "default", {})
+    for name, extra in VARIANTS:
+        b = run_child(tmp_path, name, extra)
         assert a.keys() == b.keys()
         for k in a:
-            assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), (other, k)
+            assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), (name, k)
