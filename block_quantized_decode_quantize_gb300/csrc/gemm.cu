@@ -355,7 +355,8 @@ struct StageMeta {
 // Add one 32-block part of R weight rows against M activation rows to acc: this lane's
 // block q parts past wl[r] (quants) and dl[r] (scales), and past xl / xdl / xsl (the
 // activation row's quants, scales and Q4_0 block sums; further rows Ki bytes and nb
-// blocks on).  h1: which 16-byte half of a Q8_0 block this lane loads first; xh: the
+// blocks on).  All are 32-bit shared-window addresses, so that each part's offsets are
+// immediates of its loads.  h1: which 16-byte half of a Q8_0 block this lane loads first; xh: the
 // same for the activation (0 for NVFP4, which reads both halves in element order).
 // Format constants: Q4_0 nibble masks q4m0 / q4m1 and shift q4s0 of this lane; NVFP4
 // lookup bytes tlo | thi.
@@ -366,10 +367,10 @@ struct PartConsts {
 };
 
 template <int M, int R, int FMT>
-__device__ __forceinline__ void add_part(float (&acc)[R][M], const int8_t* const (&wl)[R],
-                                         const uint16_t* const (&dl)[R], const int8_t* xl,
-                                         const float* xdl, const int32_t* xsl, int q, int Ki,
-                                         int nb, int h1, int xh, const PartConsts& pc) {
+__device__ __forceinline__ void add_part(float (&acc)[R][M], const uint32_t (&wl)[R],
+                                         const uint32_t (&dl)[R], uint32_t xl, uint32_t xdl,
+                                         uint32_t xsl, int q, int Ki, int nb, int h1, int xh,
+                                         const PartConsts& pc) {
   constexpr int kBlockBytes = FMT == kQ8 ? 32 : 16;
   constexpr int kPartBytes = 32 * kBlockBytes;
   uint4 w0[R], w1[R];
@@ -378,16 +379,16 @@ __device__ __forceinline__ void add_part(float (&acc)[R][M], const int8_t* const
   for (int r = 0; r < R; ++r) {
     // Q8_0: the two halves in this lane quad's order (see the file comment).
     // Q4_0 and NVFP4: the block's 16 bytes of codes in one load.
-    w0[r] = *reinterpret_cast<const uint4*>(wl[r] + q * kPartBytes);
-    if (FMT == kQ8) w1[r] = *reinterpret_cast<const uint4*>(wl[r] + q * kPartBytes + 16 - 32 * h1);
-    dw[r] = dl[r][q * 32];
+    w0[r] = lds_v4(wl[r] + q * kPartBytes);
+    if (FMT == kQ8) w1[r] = lds_v4(wl[r] + q * kPartBytes + 16 - 32 * h1);
+    dw[r] = lds_u16(dl[r] + q * 64);
   }
 #pragma unroll
   for (int m = 0; m < M; ++m) {
-    const int8_t* xm = xl + (size_t)m * Ki + q * 1024;
-    const uint4 x0 = *reinterpret_cast<const uint4*>(xm);
-    const uint4 x1 = *reinterpret_cast<const uint4*>(xm + 16 - 32 * xh);
-    const float dx = xdl[(size_t)m * nb + q * 32];
+    const uint32_t xm = xl + m * Ki + q * 1024;
+    const uint4 x0 = lds_v4(xm);
+    const uint4 x1 = lds_v4(xm + 16 - 32 * xh);
+    const float dx = lds_f32(xdl + (m * nb + q * 32) * 4);
     if (FMT == kQ4) {
       // x0 holds half h1 of the block (elements 16*h1 ..), x1 the other half.  The
       // lane pairs x0 with the nibbles of half h1 (mask m0) and x1 with the other
@@ -396,7 +397,7 @@ __device__ __forceinline__ void add_part(float (&acc)[R][M], const int8_t* const
       // undone by the shift.
       const uint32_t q4m0 = pc.q4m0, q4m1 = pc.q4m1;
       const int q4s0 = pc.q4s0;
-      const int sx = xsl[(size_t)m * nb + q * 32];
+      const int sx = lds_s32(xsl + (m * nb + q * 32) * 4);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const uint4 c = w0[r];
@@ -819,11 +820,18 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
     // NVFP4 reads the activation halves in element order (xh = 0): it is issue-bound,
     // and the half order's selects cost more there than a 2-way bank conflict.
     const int xh = FMT == kNv4 ? 0 : h1;
+    const uint32_t ring_a = smem_addr(ring);
+    const uint32_t xs_a = smem_addr(xs);
+    const uint32_t xds_a = smem_addr(xds);
+    const uint32_t xsum_a = smem_addr(xsum);
     uint32_t tbase = 0;  // tasks in all earlier stages: deals tasks round-robin over warps
     // A warp's tasks are kConsumerWarps apart: in (group, slice) form a step of
     // (dgi, dsl) with a carry, so no task needs a division.
     const int dgi = kConsumerWarps / S;
     const int dsl = kConsumerWarps - dgi * S;
+    // t0 / S for a warp's first task in a stage (t0 < kConsumerWarps) as a multiply-high
+    // by ceil(2^32 / S), exact for t0 < 2^17 and S <= 256.
+    const uint32_t sinv = S > 1 ? (uint32_t)((0x100000000ull + S - 1) / S) : 0u;
     int slot = 0;
     uint32_t phase = 0;
     for (;;) {
@@ -839,11 +847,10 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       const int t0 =
           (int)((cw + kConsumerWarps - (int)(tbase % kConsumerWarps)) % kConsumerWarps);
       tbase += ntasks;
-      const int8_t* ws = reinterpret_cast<const int8_t*>(ring + (size_t)slot * p.stage_bytes);
-      const uint16_t* ds =
-          reinterpret_cast<const uint16_t*>(ring + (size_t)slot * p.stage_bytes + p.wd_off);
+      const uint32_t ws = ring_a + slot * p.stage_bytes;
+      const uint32_t ds = ws + p.wd_off;
       float* pp = part + (size_t)slot * p.rps * S * M;
-      int ngi = t0 / S;
+      int ngi = S > 1 ? (int)__umulhi((uint32_t)t0, sinv) : t0;
       int nsl = t0 - ngi * S;
       for (int t = t0; t < ntasks; t += kConsumerWarps) {
         const int gi = ngi;
@@ -863,19 +870,20 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         }
         const int plo = s_slice[s];
         const int phi = s_slice[s + 1];
-        // Per-lane pointers at the task's first block; a part is kPartBytes on.
-        const int8_t* wl[R];
-        const uint16_t* dl[R];
+        // Per-lane shared-window addresses at the task's first block; a part is
+        // kPartBytes on.
+        uint32_t wl[R], dl[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           // Rows past the stage's end reuse a valid row; their sums are dropped.
           const int row = rbase + r < nr ? rbase + r : rbase;
           wl[r] = ws + row * Qrow + (plo * 32 + lane) * kBlockBytes + (FMT == kQ8 ? h1 * 16 : 0);
-          dl[r] = ds + row * nb + plo * 32 + lane;
+          dl[r] = ds + (row * nb + plo * 32 + lane) * 2;
         }
-        const int8_t* xl = xs + (size_t)xrow * Ki + (plo * 32 + lane) * 32 + xh * 16;
-        const float* xdl = xds + (size_t)xrow * nb + plo * 32 + lane;
-        const int32_t* xsl = xsum + (size_t)xrow * nb + plo * 32 + lane;
+        const int xb = xrow * nb + plo * 32 + lane;  // the task's first activation block
+        const uint32_t xl = xs_a + xb * 32 + xh * 16;
+        const uint32_t xdl = xds_a + xb * 4;
+        const uint32_t xsl = xsum_a + xb * 4;
         float acc[R][M];
 #pragma unroll
         for (int r = 0; r < R; ++r)
