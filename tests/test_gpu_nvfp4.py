@@ -2,9 +2,11 @@
 
 The weight ingest must match the oracle bit for bit (codes, E4M3 scales and the tensor
 scale).  Products must match the oracle within |y - y_ref| <= 1e-4 * sum |term| + 1e-6,
-with one term per 16-element half-block, |(g/2) s d_x S|; each row must equal, bit for
-bit, the M = 1 product of that row.  Each side runs its own pipeline from the same
-seeded inputs.
+with one term per 16-element half-block, |(g/2) s d_x S|, twice over: against the
+oracle's fp32 product (exact half-block sums, the scale terms in block order), and
+against the plain definition summed element by element in fp64, sum_e g s e2m1 d_x q_x,
+which shares no grouping with the kernel.  Each row must equal, bit for bit, the M = 1
+product of that row.  Each side runs its own pipeline from the same seeded inputs.
 """
 import json
 import os
@@ -85,8 +87,10 @@ def test_nvfp4_gemm_parity(mem, orc, N, K, M):
     torch.cuda.synchronize()
     assert y.intact()
     y_ref = orc.gemm_nvfp4(oc, os_, og, oxq, oxd)
-    assert_within(np_(y.view), y_ref, nvfp4_terms(orc, oc, os_, og, oxq, oxd),
-                  "nvfp4 N=%d K=%d M=%d" % (N, K, M))
+    terms = nvfp4_terms(orc, oc, os_, og, oxq, oxd)
+    assert_within(np_(y.view), y_ref, terms, "nvfp4 N=%d K=%d M=%d" % (N, K, M))
+    y64 = orc.nvfp4_dequant_gemm_f64(oc, os_, og, oxq, oxd)
+    assert_within(np_(y.view), y64, terms, "nvfp4 vs element-order fp64 N=%d K=%d M=%d" % (N, K, M))
     for m in sorted({0, M - 1}):
         y1 = mem.memra_nvfp4_gemv(codes, scales, g, xq[m], xd[m])
         torch.cuda.synchronize()

@@ -138,6 +138,9 @@ def test_dense27b_nvfp4_layer_sampled(mem, orc):
         terms = np.abs(0.5 * float(og) * orc.e4m3_to_f32(osc[rows]).astype(np.float64) *
                        np.repeat(oxd[0].astype(np.float64), 2)[None] * S).sum(axis=1)
         assert_within(np_(op.y)[:, rows], y_ref, terms[None], "nvfp4 L0 %s" % name)
+        # and against the plain definition, summed element by element in fp64
+        y64 = orc.nvfp4_dequant_gemm_f64(oc[rows], osc[rows], og, oxq, oxd)
+        assert_within(np_(op.y)[:, rows], y64, terms[None], "nvfp4 L0 %s (fp64)" % name)
         del codes, scales, op, oc, osc
     torch.cuda.empty_cache()
 
