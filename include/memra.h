@@ -67,9 +67,13 @@
  *                     stage, ring and shared-memory sizes (KB), CTAs per SM, the
  *                     M > 1 bulk-copy switch and the register/bulk-copy size
  *                     threshold (MB) of the product kernels.
+ *   MEMRA_TMA_PREFILL, MEMRA_TMA_ROUTED_PREFILL
+ *                     stages a dense (routed) product's producer issues before its
+ *                     consumers have staged the activation (0: the whole ring).
  * The same names, defined as macros when the library is compiled, change the
  * compiled-in defaults (also MEMRA_TMA_CONSUMER_WARPS,
- * MEMRA_TMA_FEW_M_CONSUMER_WARPS, MEMRA_TMA_MIN_BLOCKS, MEMRA_SLICE_PARTS; the last
+ * MEMRA_TMA_FEW_M_CONSUMER_WARPS, MEMRA_TMA_MIN_BLOCKS, MEMRA_WAIT_SUSPEND_NS (the
+ * suspend-time hint of a barrier wait's retries, ns), MEMRA_SLICE_PARTS; the last
  * changes the fp32 summation order and with it the result bits).
  */
 #ifndef MEMRA_H
