@@ -1,5 +1,6 @@
-// Q8_0 x q8_1 products: the M = 1 decode GEMV, the M <= 8 verify skinny GEMM and
-// the routed-expert (MoE) GEMV.
+// Block-quantised weight x q8_1 activation products: the M = 1 decode GEMV, the
+// M <= 8 verify skinny GEMM (two passes up to 16 rows), the routed-expert (MoE)
+// GEMVs and the routed FFN layer, on Q8_0, Q4_0 and NVFP4 weights.
 //
 // Arithmetic (one definition for every kernel below, so that a row's result is
 // the same bit for bit whichever kernel, M, grid or batch produced it):
@@ -7,11 +8,12 @@
 //   slices; slice s covers parts [s*cpr/S, (s+1)*cpr/S).
 //   Within a slice, lane l owns blocks b = 32p + l and accumulates, in ascending
 //   p:  acc = fma(fl(float(d_w[b]) * d_x[b]), float(s_b), acc), from acc = 0,
-//   where s_b is the exact int32 block dot (8 dp4a).
+//   where s_b is the exact int32 block dot (8 dp4a for Q8_0; the 4-bit formats'
+//   exact forms are at their block dots below).
 //   part[s] = xor-butterfly sum over the 32 lanes (masks 16, 8, 4, 2, 1).
 //   y = part[0] + part[1] + ... + part[S-1], sequentially.
 //
-// Two kernels implement it.
+// Two kernels implement it (a third, the tensor-core verify kernel, is mma.cu).
 //
 // q8_tma_kernel (the GB300 path; K % 256 == 0 and 16-byte aligned planes): two
 //   CTAs per SM for M = 1 (one, with a deeper ring and more registers per thread,
@@ -21,18 +23,19 @@
 //   of shared-memory stages with cp.async.bulk, completing on per-stage mbarriers,
 //   records each stage's rows in shared memory, closes the stream with a sentinel
 //   stage, and reduces each finished stage's slice partials into y.  Warps 1..12
-//   consume stages: each task is (R rows, one slice), read from shared memory with
-//   128-bit loads whose half-block order alternates between lane quads so that no
-//   two lanes of a phase hit the same banks.  The HBM stream is set by the ring
-//   (about 176 KB in flight per SM), not by how tasks divide among warps.  With
-//   programmatic dependent launch the producer starts the ring as soon as the CTA
-//   is resident, before the preceding kernel has finished (dense weights do not
-//   depend on it); the consumers wait for that kernel and then stage the
-//   activation with plain loads.
+//   consume stages: each task is (R rows, one slice), dealt round-robin, and each
+//   32-block part of it runs through one routine (add_part) whose shared-memory
+//   loads are 128-bit at 32-bit shared-window addresses.  The HBM stream is set by
+//   the ring (about 176 KB in flight per SM), not by how tasks divide among warps.
+//   With programmatic dependent launch the producer starts the ring as soon as the
+//   CTA is resident, before the preceding kernel has finished (dense weights do not
+//   depend on it), but issues only the first two stages until its consumers, which
+//   wait for that kernel, have staged the activation with plain loads: those loads
+//   then wait behind a short queue of weight copies.
 //
-// q8_reg_kernel (everything else): the same tasks with weights loaded straight
-//   into registers (256-bit loads, a slice's blocks issued together), activations
-//   staged in shared memory.
+// q8_reg_kernel (Q8_0 products below about 24 MB, K % 256 != 0, unaligned planes):
+//   the same tasks with weights loaded straight into registers (256-bit loads, a
+//   slice's blocks issued together), activations staged in shared memory.
 #include <algorithm>
 #include <atomic>
 #include <cstdlib>
@@ -806,9 +809,8 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     }
-    // Bytes of one block and of one 32-block part in the ring's quant rows.
+    // Bytes of one block in the ring's quant rows.
     constexpr int kBlockBytes = FMT == kQ8 ? 32 : 16;
-    constexpr int kPartBytes = 32 * kBlockBytes;
     const int Qrow = (int)p.qrow;
     // Q4_0 nibble masks and shift of this lane (see add_part); the NVFP4 lookup bytes.
     PartConsts pc;
