@@ -94,6 +94,16 @@
 #ifndef MEMRA_TMA_ROUTED_PREFILL
 #define MEMRA_TMA_ROUTED_PREFILL 1
 #endif
+// Dense M = 1 products on 4-bit weights: their consumers take longer per byte than
+// Q8_0's, and a deeper ring hides more of the stream's latency (64-layer sweeps,
+// 28 KB stages in 88 KB -> 34 KB in 104 KB: Q4_0 3.046 -> 2.994 ms per token, NVFP4
+// 3.488 -> 3.471; Q8_0 gains nothing from it).
+#ifndef MEMRA_TMA_STAGE_KB_4BIT
+#define MEMRA_TMA_STAGE_KB_4BIT 34
+#endif
+#ifndef MEMRA_TMA_RING_KB_4BIT
+#define MEMRA_TMA_RING_KB_4BIT 104
+#endif
 
 namespace memra {
 namespace {
@@ -1215,6 +1225,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct TmaTuning {
   size_t stage_target;    // bytes per ring stage (rounded to whole rows)
   size_t ring_budget;     // bytes of ring per CTA
+  size_t stage_target_4bit;  // the same for dense M = 1 products on 4-bit weights
+  size_t ring_budget_4bit;
   size_t smem_pair_limit; // shared memory of one CTA when two must fit on an SM
   int ctas_per_sm;
   size_t packed_max;         // gated routed: largest packed stage (bytes)
@@ -1241,6 +1253,10 @@ const TmaTuning& tma_tuning() {
     TmaTuning r;
     r.stage_target = (size_t)env_long("MEMRA_TMA_STAGE_KB", MEMRA_TMA_STAGE_KB, 1) * 1024;
     r.ring_budget = (size_t)env_long("MEMRA_TMA_RING_KB", MEMRA_TMA_RING_KB, 1) * 1024;
+    r.stage_target_4bit =
+        (size_t)env_long("MEMRA_TMA_STAGE_KB_4BIT", MEMRA_TMA_STAGE_KB_4BIT, 1) * 1024;
+    r.ring_budget_4bit =
+        (size_t)env_long("MEMRA_TMA_RING_KB_4BIT", MEMRA_TMA_RING_KB_4BIT, 1) * 1024;
     r.smem_pair_limit =
         (size_t)env_long("MEMRA_TMA_SMEM_LIMIT_KB", MEMRA_TMA_SMEM_LIMIT_KB, 1) * 1024;
     r.packed_max = (size_t)env_long("MEMRA_TMA_PACKED_KB", 48, 0) * 1024;
@@ -1305,8 +1321,10 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   // dense size.
   const bool short_routed =
       MODE != kDense && (size_t)(maxu * upr) * row_bytes <= 4 * tune.stage_target;
+  const bool dense4 = MODE == kDense && FMT != kQ8;  // its sizes apply at M = 1
   const size_t target = M > 1 ? tune.multi_stage_target
-                        : (short_routed ? tune.routed_stage_target : tune.stage_target);
+                        : (short_routed ? tune.routed_stage_target
+                                        : (dense4 ? tune.stage_target_4bit : tune.stage_target));
   int rps = (int)std::max<size_t>(1, target /
                                           row_bytes);
   // A stage never spans two segments, and no segment is longer than a CTA's share
@@ -1341,7 +1359,8 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   size_t limit = M > 1 ? (size_t)info.max_smem_optin
                        : std::max<size_t>(tune.smem_pair_limit, fixed + 2 * (stage + part_per_stage));
   limit = std::min<size_t>(limit, (size_t)info.max_smem_optin);
-  const size_t budget = M > 1 ? tune.multi_ring_budget : tune.ring_budget;
+  const size_t budget =
+      M > 1 ? tune.multi_ring_budget : (dense4 ? tune.ring_budget_4bit : tune.ring_budget);
   int ns = (int)std::min<size_t>(kMaxStages, std::max<size_t>(2, budget / stage));
   // A dense product whose CTA share is a little more than the ring holds: stretch the
   // stages so that the whole share is in flight at once (no stage waits for a slot).
