@@ -95,14 +95,18 @@
 #define MEMRA_TMA_ROUTED_PREFILL 1
 #endif
 // Dense M = 1 products on 4-bit weights: their consumers take longer per byte than
-// Q8_0's, and a deeper ring hides more of the stream's latency (64-layer sweeps,
-// 28 KB stages in 88 KB -> 34 KB in 104 KB: Q4_0 3.046 -> 2.994 ms per token, NVFP4
-// 3.488 -> 3.471; Q8_0 gains nothing from it).
+// Q8_0's, and a deeper ring hides more of the stream's latency, with one stage issued
+// before the activation is staged (64-layer sweeps, from 28 KB stages in 88 KB and two
+// stages: Q4_0 3.061 -> 2.919 ms per token, NVFP4 3.483 -> 3.349; 24-28 KB or 40-52 KB
+// stages, or two stages before the activation, are slower; Q8_0 gains nothing).
 #ifndef MEMRA_TMA_STAGE_KB_4BIT
 #define MEMRA_TMA_STAGE_KB_4BIT 34
 #endif
 #ifndef MEMRA_TMA_RING_KB_4BIT
 #define MEMRA_TMA_RING_KB_4BIT 104
+#endif
+#ifndef MEMRA_TMA_PREFILL_4BIT
+#define MEMRA_TMA_PREFILL_4BIT 1
 #endif
 
 namespace memra {
@@ -1237,6 +1241,7 @@ struct TmaTuning {
   int64_t dense_min_bytes;  // smaller dense products use the register kernel
   int prefill_stages;       // dense: stages issued before the activation is staged (0: all)
   int routed_prefill;       // the same for routed products
+  int prefill_4bit;         // the same for dense M = 1 products on 4-bit weights
 };
 
 long env_long(const char* name, long dflt, long lo) {
@@ -1272,6 +1277,7 @@ const TmaTuning& tma_tuning() {
         (int64_t)env_long("MEMRA_TMA_DENSE_MIN_MB", MEMRA_TMA_DENSE_MIN_MB, 0) * 1024 * 1024;
     r.prefill_stages = (int)env_long("MEMRA_TMA_PREFILL", MEMRA_TMA_PREFILL, 0);
     r.routed_prefill = (int)env_long("MEMRA_TMA_ROUTED_PREFILL", MEMRA_TMA_ROUTED_PREFILL, 0);
+    r.prefill_4bit = (int)env_long("MEMRA_TMA_PREFILL_4BIT", MEMRA_TMA_PREFILL_4BIT, 0);
     return r;
   }();
   return t;
@@ -1447,8 +1453,9 @@ template <int M, int R, int MODE, int XIN, int FMT = kQ8>
 memra_status run_product(Params p, cudaStream_t stream) {
   DeviceInfo info;
   if (!device_info(&info)) return MEMRA_ERR_CUDA;
-  p.prefill_stages =
-      MODE == kDense ? tma_tuning().prefill_stages : tma_tuning().routed_prefill;
+  p.prefill_stages = MODE != kDense ? tma_tuning().routed_prefill
+                     : (FMT != kQ8 && M == 1 ? tma_tuning().prefill_4bit
+                                             : tma_tuning().prefill_stages);
   const long long wl = g_test_wait_limit.load(std::memory_order_relaxed);
   p.wait_limit = wl > 0 ? wl : kWaitLimitCycles;
   p.stall_after = (int)g_test_stall_after.load(std::memory_order_relaxed);

@@ -69,9 +69,10 @@
  *                     M > 1 bulk-copy switch and the register/bulk-copy size
  *                     threshold (MB) of the product kernels (the _4BIT sizes: dense
  *                     M = 1 products on Q4_0 and NVFP4 weights).
- *   MEMRA_TMA_PREFILL, MEMRA_TMA_ROUTED_PREFILL
- *                     stages a dense (routed) product's producer issues before its
- *                     consumers have staged the activation (0: the whole ring).
+ *   MEMRA_TMA_PREFILL, MEMRA_TMA_ROUTED_PREFILL, MEMRA_TMA_PREFILL_4BIT
+ *                     stages a dense (routed; dense M = 1 4-bit) product's producer
+ *                     issues before its consumers have staged the activation (0: the
+ *                     whole ring).
  * The same names, defined as macros when the library is compiled, change the
  * compiled-in defaults (also MEMRA_TMA_CONSUMER_WARPS,
  * MEMRA_TMA_FEW_M_CONSUMER_WARPS, MEMRA_TMA_MIN_BLOCKS, MEMRA_WAIT_SUSPEND_NS (the
