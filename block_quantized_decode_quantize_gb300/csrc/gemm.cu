@@ -26,7 +26,7 @@
 //   consume stages: each task is (R rows, one slice), dealt round-robin, and each
 //   32-block part of it runs through one routine (add_part) whose shared-memory
 //   loads are 128-bit at 32-bit shared-window addresses.  The HBM stream is set by
-//   the ring (about 176 KB in flight per SM), not by how tasks divide among warps.
+//   the ring (about 208 KB in flight per SM), not by how tasks divide among warps.
 //   With programmatic dependent launch the producer starts the ring as soon as the
 //   CTA is resident, before the preceding kernel has finished (dense weights do not
 //   depend on it), but issues only the first two stages until its consumers, which
@@ -46,14 +46,17 @@
 #include "product.cuh"
 
 // Ring and stage sizes measured on GB300: two CTAs per SM, each streaming through
-// about 88 KB of 28-KB stages, keep HBM busiest (bulk copies below ~16 KB stream
-// markedly slower per CTA).  Each can be overridden at run time by the environment
-// variable of the same name (read once per process; see TmaTuning).
+// about 104 KB of 34-KB stages, keep HBM busiest (bulk copies below ~16 KB stream
+// markedly slower per CTA).  From 28 KB in 88 KB: 64-layer sweep 4.133 -> 4.089 ms per
+// token, top-8 MoE batches of 8 / 16 tokens 3.00 -> 2.83 / 5.45 -> 4.94 ms (32 in 96
+// and 36 in 108 the same; the LM head 0.6 % slower).  Each can be overridden at run
+// time by the environment variable of the same name (read once per process; see
+// TmaTuning).
 #ifndef MEMRA_TMA_RING_KB
-#define MEMRA_TMA_RING_KB 88
+#define MEMRA_TMA_RING_KB 104
 #endif
 #ifndef MEMRA_TMA_STAGE_KB
-#define MEMRA_TMA_STAGE_KB 28
+#define MEMRA_TMA_STAGE_KB 34
 #endif
 // Routed experts at M = 1 for one token move a few tens of rows per CTA: smaller
 // stages keep more of them in flight (top-8 MoE layer: 0.967 ms per 48-layer token
@@ -94,17 +97,10 @@
 #ifndef MEMRA_TMA_ROUTED_PREFILL
 #define MEMRA_TMA_ROUTED_PREFILL 1
 #endif
-// Dense M = 1 products on 4-bit weights: their consumers take longer per byte than
-// Q8_0's, and a deeper ring hides more of the stream's latency, with one stage issued
-// before the activation is staged (64-layer sweeps, from 28 KB stages in 88 KB and two
-// stages: Q4_0 3.061 -> 2.919 ms per token, NVFP4 3.483 -> 3.349; 24-28 KB or 40-52 KB
-// stages, or two stages before the activation, are slower; Q8_0 gains nothing).
-#ifndef MEMRA_TMA_STAGE_KB_4BIT
-#define MEMRA_TMA_STAGE_KB_4BIT 34
-#endif
-#ifndef MEMRA_TMA_RING_KB_4BIT
-#define MEMRA_TMA_RING_KB_4BIT 104
-#endif
+// Dense M = 1 products on 4-bit weights, whose consumers take longer per byte than
+// Q8_0's, issue one stage before the activation is staged (64-layer sweeps with 34 KB
+// stages in 104 KB: Q4_0 3.00 -> 2.92 ms per token, NVFP4 3.46 -> 3.35; Q8_0 is best
+// with two).
 #ifndef MEMRA_TMA_PREFILL_4BIT
 #define MEMRA_TMA_PREFILL_4BIT 1
 #endif
@@ -1229,8 +1225,6 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct TmaTuning {
   size_t stage_target;    // bytes per ring stage (rounded to whole rows)
   size_t ring_budget;     // bytes of ring per CTA
-  size_t stage_target_4bit;  // the same for dense M = 1 products on 4-bit weights
-  size_t ring_budget_4bit;
   size_t smem_pair_limit; // shared memory of one CTA when two must fit on an SM
   int ctas_per_sm;
   size_t packed_max;         // gated routed: largest packed stage (bytes)
@@ -1258,10 +1252,6 @@ const TmaTuning& tma_tuning() {
     TmaTuning r;
     r.stage_target = (size_t)env_long("MEMRA_TMA_STAGE_KB", MEMRA_TMA_STAGE_KB, 1) * 1024;
     r.ring_budget = (size_t)env_long("MEMRA_TMA_RING_KB", MEMRA_TMA_RING_KB, 1) * 1024;
-    r.stage_target_4bit =
-        (size_t)env_long("MEMRA_TMA_STAGE_KB_4BIT", MEMRA_TMA_STAGE_KB_4BIT, 1) * 1024;
-    r.ring_budget_4bit =
-        (size_t)env_long("MEMRA_TMA_RING_KB_4BIT", MEMRA_TMA_RING_KB_4BIT, 1) * 1024;
     r.smem_pair_limit =
         (size_t)env_long("MEMRA_TMA_SMEM_LIMIT_KB", MEMRA_TMA_SMEM_LIMIT_KB, 1) * 1024;
     r.packed_max = (size_t)env_long("MEMRA_TMA_PACKED_KB", 48, 0) * 1024;
@@ -1327,10 +1317,8 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   // dense size.
   const bool short_routed =
       MODE != kDense && (size_t)(maxu * upr) * row_bytes <= 4 * tune.stage_target;
-  const bool dense4 = MODE == kDense && FMT != kQ8;  // its sizes apply at M = 1
   const size_t target = M > 1 ? tune.multi_stage_target
-                        : (short_routed ? tune.routed_stage_target
-                                        : (dense4 ? tune.stage_target_4bit : tune.stage_target));
+                        : (short_routed ? tune.routed_stage_target : tune.stage_target);
   int rps = (int)std::max<size_t>(1, target /
                                           row_bytes);
   // A stage never spans two segments, and no segment is longer than a CTA's share
@@ -1365,8 +1353,7 @@ bool plan_tma(Params& p, const DeviceInfo& info, int64_t grid, size_t* smem_out)
   size_t limit = M > 1 ? (size_t)info.max_smem_optin
                        : std::max<size_t>(tune.smem_pair_limit, fixed + 2 * (stage + part_per_stage));
   limit = std::min<size_t>(limit, (size_t)info.max_smem_optin);
-  const size_t budget =
-      M > 1 ? tune.multi_ring_budget : (dense4 ? tune.ring_budget_4bit : tune.ring_budget);
+  const size_t budget = M > 1 ? tune.multi_ring_budget : tune.ring_budget;
   int ns = (int)std::min<size_t>(kMaxStages, std::max<size_t>(2, budget / stage));
   // A dense product whose CTA share is a little more than the ring holds: stretch the
   // stages so that the whole share is in flight at once (no stage waits for a slot).

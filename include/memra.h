@@ -63,12 +63,10 @@
  *   MEMRA_TMA_STAGE_KB, MEMRA_TMA_RING_KB, MEMRA_TMA_ROUTED_STAGE_KB,
  *   MEMRA_TMA_SMEM_LIMIT_KB, MEMRA_TMA_CTAS_PER_SM, MEMRA_TMA_PACKED_KB,
  *   MEMRA_TMA_MULTI_RING_KB, MEMRA_TMA_MULTI_STAGE_KB, MEMRA_TMA_MULTI,
- *   MEMRA_TMA_DENSE_MIN_MB, MEMRA_REG_CTAS_PER_SM, MEMRA_TMA_STAGE_KB_4BIT,
- *   MEMRA_TMA_RING_KB_4BIT
+ *   MEMRA_TMA_DENSE_MIN_MB, MEMRA_REG_CTAS_PER_SM
  *                     stage, ring and shared-memory sizes (KB), CTAs per SM, the
  *                     M > 1 bulk-copy switch and the register/bulk-copy size
- *                     threshold (MB) of the product kernels (the _4BIT sizes: dense
- *                     M = 1 products on Q4_0 and NVFP4 weights).
+ *                     threshold (MB) of the product kernels.
  *   MEMRA_TMA_PREFILL, MEMRA_TMA_ROUTED_PREFILL, MEMRA_TMA_PREFILL_4BIT
  *                     stages a dense (routed; dense M = 1 4-bit) product's producer
  *                     issues before its consumers have staged the activation (0: the

@@ -71,16 +71,14 @@ VARIANTS = [
     ("tma", {"MEMRA_GEMV_PATH": "tma"}),
     ("mma", {"MEMRA_GEMV_PATH": "mma"}),
     ("tma_small_stages", {"MEMRA_GEMV_PATH": "tma", "MEMRA_TMA_STAGE_KB": "6",
-                          "MEMRA_TMA_MULTI_STAGE_KB": "6", "MEMRA_TMA_ROUTED_STAGE_KB": "6",
-                          "MEMRA_TMA_STAGE_KB_4BIT": "6"}),
+                          "MEMRA_TMA_MULTI_STAGE_KB": "6", "MEMRA_TMA_ROUTED_STAGE_KB": "6"}),
     ("tma_prefill_all", {"MEMRA_GEMV_PATH": "tma", "MEMRA_TMA_PREFILL": "0",
                          "MEMRA_TMA_PREFILL_4BIT": "0"}),
     ("tma_prefill_1", {"MEMRA_GEMV_PATH": "tma", "MEMRA_TMA_PREFILL": "1",
                        "MEMRA_TMA_PREFILL_4BIT": "2"}),
 ]
 _KNOBS = ("MEMRA_GEMV_PATH", "MEMRA_TMA_STAGE_KB", "MEMRA_TMA_MULTI_STAGE_KB",
-          "MEMRA_TMA_ROUTED_STAGE_KB", "MEMRA_TMA_STAGE_KB_4BIT", "MEMRA_TMA_PREFILL",
-          "MEMRA_TMA_PREFILL_4BIT")
+          "MEMRA_TMA_ROUTED_STAGE_KB", "MEMRA_TMA_PREFILL", "MEMRA_TMA_PREFILL_4BIT")
 
 
 def run_child(tmp_path, name, extra):
