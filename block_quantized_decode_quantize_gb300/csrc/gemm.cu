@@ -1475,16 +1475,18 @@ memra_status run_product(Params p, cudaStream_t stream) {
   return MEMRA_ERR_UNSUPPORTED;
 }
 
-// Q4_0 products (dense, q8_1 input).  A Q4_0 block costs as many dp4a as a Q8_0 block
-// in half the bytes, so the consumers, not the stream, set the pace: M = 1 takes
-// 2-row tasks, which share each block's activation loads between two rows (measured
-// on the 64-layer sweep: 3.44 ms per token with 1-row tasks, 3.16 with 2, 3.32 with
-// 4).  M = 8 takes 2-row tasks too: with K = 17408 the activation planes and their
-// block sums leave room for 2-row stages only.
+// Q4_0 and NVFP4 products (dense, q8_1 input).  A 4-bit block costs as many dp4a as
+// a Q8_0 block (NVFP4 twice as many) in half the bytes, so the consumers, not the
+// stream, set the pace: M = 1 takes 3-row tasks, which share each block's activation
+// loads between three rows, and whose 34 KB stages hold 12 rows at K = 5120 and 3 at
+// K = 17408 (64-layer sweeps, Q4_0 / NVFP4 ms per token: 1-row tasks 3.00 / 3.55,
+// 2-row 2.91 / 3.36, 3-row 2.86 / 3.33, 4-row 3.01 / 3.51).  M = 8 takes 2-row tasks:
+// with K = 17408 the activation planes and their block sums leave room for 2-row
+// stages only.
 template <int FMT>
 memra_status dispatch_m_4bit(const Params& p, int M, cudaStream_t s) {
   switch (M) {
-    case 1: return run_product<1, 2, kDense, kXq8, FMT>(p, s);
+    case 1: return run_product<1, 3, kDense, kXq8, FMT>(p, s);
     case 2: return run_product<2, 1, kDense, kXq8, FMT>(p, s);
     case 3: return run_product<3, 1, kDense, kXq8, FMT>(p, s);
     case 4: return run_product<4, 2, kDense, kXq8, FMT>(p, s);
