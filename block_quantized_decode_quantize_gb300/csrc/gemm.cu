@@ -882,8 +882,8 @@ __global__ void __launch_bounds__(tma_threads(M), M == 1 ? MEMRA_TMA_MIN_BLOCKS 
         }
         const int plo = s_slice[s];
         const int phi = s_slice[s + 1];
-        // Per-lane shared-window addresses at the task's first block; a part is
-        // kPartBytes on.
+        // Per-lane shared-window addresses at the task's first block; add_part reaches
+        // part q of the slice at an immediate offset from them.
         uint32_t wl[R], dl[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
