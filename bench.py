@@ -975,8 +975,8 @@ def run_reference(args):
         "dtype": "int8 (int32 block sums, fp32 scale-accumulate)",
         "data": "synthetic (seeded N(0,0.02) weights, bf16 N(0,1) activations)",
         "config": {"workload": "dense27b_sweep", "layers_sampled": 1, "M": 1},
-        "cpu_baseline": {"value": round(value, 3), "kind": "oracle", "cores": cs.threads,
-                         "sample": sample},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "kind": "oracle",
+                         "cores": cs.threads, "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

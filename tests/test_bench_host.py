@@ -1,7 +1,11 @@
 """Host-side logic of bench.py: argument rules, rank aggregation over gloo (world
-size 2 on CPU), workload byte counts."""
+size 2 on CPU), workload byte counts, and the reference arm's JSON line (the CPU
+oracle, which runs without a GPU)."""
+import json
 import os
 import socket
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -97,3 +101,33 @@ def test_verify_legs_share_the_sweep_weights():
         assert b.x.shape == (4, a.x.shape[1]) and b.y.shape == (4, a.wq.shape[0])
     again = bench.sweep_rows_like(ops, 4)
     assert all(torch.equal(p.x, q.x) for p, q in zip(rows, again))   # seeded
+
+
+def test_reference_arm_prints_one_contract_line():
+    """The reference arm times the oracle on the host cores and prints the JSON line the
+    driver reads: the same metric and unit as the main arm, impl "reference", a CPU
+    baseline describing the run and an e2e object with no host-device bytes."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3"], cwd=root, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"]["workload"] == "dense27b_sweep"
+    cpu = d["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["value"] == d["value"] and cpu["unit"] == "GB/s"
+    assert cpu["cores"] >= 1 and cpu["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == "GB/s"
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
